@@ -1,0 +1,327 @@
+"""The oracle: a plain CPU statement of NVFP4 block-scaled quantization (numpy in, numpy out).
+
+TEST INFRASTRUCTURE ONLY. The parity tests, the smoke check and the benchmark's CPU-baseline
+leg are the only callers. The CUDA library (the product) never imports this package and shares
+no code with it; the arithmetic lives in ``nvfp4_oracle.c`` (plain scalar C, IEEE binary32,
+each step cited there to the page "[nvfp4_training] Optimize CuteDSL kernels for NVFP4
+training", pytorch/ao pull request #4798).
+
+BF16 tensors are passed as their 16-bit patterns (``numpy.uint16``). Outputs follow the
+layouts of the C library: rowwise codes [M, N/2] and scales [M, N/16]; columnwise (transposed)
+codes [N, M/2] and scales [N, M/16]; global scales as ``[amax, S_dec]``.
+
+Parity status: every function here is pinned by the ``-m "not gpu"`` oracle tests, except the
+rounding rule of stochastic rounding (reading R8 in ``nvfp4_oracle.c``), which is pinned by
+its statistical properties there and otherwise rests on the PTX description of ``cvt`` with
+``.rs`` rounding.
+"""
+import ctypes
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_i64 = ctypes.c_int64
+
+
+def lib():
+    """Load (building first if needed) the oracle's shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        sig = {
+            "oracle_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+            "oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
+            "oracle_e4m3_decode": (ctypes.c_float, [ctypes.c_uint8]),
+            "oracle_e2m1_encode_rn": (ctypes.c_uint8, [ctypes.c_float]),
+            "oracle_e2m1_encode_sr": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_uint32]),
+            "oracle_e2m1_decode": (ctypes.c_float, [ctypes.c_uint8]),
+            "oracle_philox4x32_10": (None, [_u32p, _u32p, _u32p]),
+            "oracle_fwht16": (None, [_f32p]),
+            "oracle_rht16": (None, [_f32p, ctypes.c_uint32, _f32p]),
+            "oracle_global_scale": (None, [ctypes.c_float, _f32p]),
+            "oracle_block_scale": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_float]),
+            "oracle_element_multiplier": (ctypes.c_float, [ctypes.c_uint8, ctypes.c_float]),
+            "oracle_quantize_block16": (None, [_f32p, ctypes.c_float, ctypes.c_float, _u32p,
+                                               _u8p, _u8p]),
+            "oracle_amax": (ctypes.c_float, [_u16p, _i64, _i64]),
+            "oracle_amax_rht": (ctypes.c_float, [_u16p, _i64, _i64, ctypes.c_uint32]),
+            "oracle_quantize_rowwise": (None, [_u16p, _i64, _i64, ctypes.c_float, ctypes.c_int,
+                                               ctypes.c_uint64, ctypes.c_uint32, _u8p, _u8p,
+                                               _f32p]),
+            "oracle_quantize_colwise": (None, [_u16p, _i64, _i64, ctypes.c_float, ctypes.c_int,
+                                               ctypes.c_uint32, ctypes.c_int, ctypes.c_uint64,
+                                               ctypes.c_uint32, _u8p, _u8p, _f32p]),
+            "oracle_quantize_2d": (None, [_u16p, _i64, _i64, ctypes.c_float, _u8p, _u8p, _u8p,
+                                          _u8p, _f32p]),
+            "oracle_quantize_grouped": (ctypes.c_int, [_u16p, _i64, _i64, _i32p, ctypes.c_int32,
+                                                       _i64, ctypes.c_int, ctypes.c_int,
+                                                       ctypes.c_int, ctypes.c_uint32,
+                                                       ctypes.c_uint64, ctypes.c_uint32,
+                                                       _u8p, _u8p, _f32p, _u8p, _u8p, _f32p]),
+            "oracle_dequantize": (None, [_u8p, _u8p, ctypes.c_float, _i64, _i64, _f32p]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(a, t):
+    return a.ctypes.data_as(t) if a is not None else None
+
+
+def as_bf16_bits(x) -> np.ndarray:
+    """BF16 input as a C-contiguous uint16 array of bit patterns (torch bf16 tensors accepted)."""
+    if hasattr(x, "dtype") and str(getattr(x, "dtype", "")) == "torch.bfloat16":
+        import torch  # plumbing only: reinterpret the tensor's storage as 16-bit integers
+        return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.uint16:
+        raise TypeError("expected uint16 BF16 bit patterns or a torch.bfloat16 tensor")
+    return a
+
+
+# ----------------------------------------------------------------------------------------
+# Scalar primitives (vectorised over numpy arrays with plain Python loops: small inputs only)
+# ----------------------------------------------------------------------------------------
+
+def f32_to_bf16(values) -> np.ndarray:
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib().oracle_f32_to_bf16(float(f)) for f in v], dtype=np.uint16)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib().oracle_e4m3_encode(float(f)) for f in v], dtype=np.uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib().oracle_e4m3_decode(int(b)) for b in c], dtype=np.float32)
+
+
+def e2m1_encode_rn(values) -> np.ndarray:
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib().oracle_e2m1_encode_rn(float(f)) for f in v], dtype=np.uint8)
+
+
+def e2m1_encode_sr(values, rand8) -> np.ndarray:
+    v = np.asarray(values, dtype=np.float32).ravel()
+    r = np.broadcast_to(np.asarray(rand8, dtype=np.uint32), v.shape)
+    return np.array([lib().oracle_e2m1_encode_sr(float(f), int(b)) for f, b in zip(v, r)],
+                    dtype=np.uint8)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib().oracle_e2m1_decode(int(b)) for b in c], dtype=np.float32)
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().oracle_philox4x32_10(_ptr(c, _u32p), _ptr(k, _u32p), _ptr(out, _u32p))
+    return out
+
+
+def fwht16(v) -> np.ndarray:
+    w = np.array(v, dtype=np.float32).copy()
+    assert w.shape == (16,)
+    lib().oracle_fwht16(_ptr(w, _f32p))
+    return w
+
+
+def rht16(v, sign_mask: int) -> np.ndarray:
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    y = np.zeros(16, dtype=np.float32)
+    lib().oracle_rht16(_ptr(a, _f32p), sign_mask, _ptr(y, _f32p))
+    return y
+
+
+def global_scale(amax: float):
+    out = np.zeros(2, dtype=np.float32)
+    lib().oracle_global_scale(float(np.float32(amax)), _ptr(out, _f32p))
+    return out[0], out[1]
+
+
+def block_scale(bamax: float, s_enc: float) -> int:
+    return lib().oracle_block_scale(float(np.float32(bamax)), float(np.float32(s_enc)))
+
+
+def element_multiplier(s: int, s_dec: float) -> np.float32:
+    return np.float32(lib().oracle_element_multiplier(s, float(np.float32(s_dec))))
+
+
+def quantize_block16(v, s_enc, s_dec, rand=None):
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    r = None if rand is None else np.ascontiguousarray(rand, dtype=np.uint32)
+    codes = np.zeros(8, dtype=np.uint8)
+    scale = np.zeros(1, dtype=np.uint8)
+    lib().oracle_quantize_block16(_ptr(a, _f32p), float(np.float32(s_enc)),
+                                  float(np.float32(s_dec)), _ptr(r, _u32p),
+                                  _ptr(codes, _u8p), _ptr(scale, _u8p))
+    return codes, int(scale[0])
+
+
+# ----------------------------------------------------------------------------------------
+# Tensors
+# ----------------------------------------------------------------------------------------
+
+def amax(x) -> np.float32:
+    xb = as_bf16_bits(x)
+    M, N = xb.shape
+    return np.float32(lib().oracle_amax(_ptr(xb, _u16p), M, N))
+
+
+def amax_rht(x, sign_mask: int) -> np.float32:
+    xb = as_bf16_bits(x)
+    M, N = xb.shape
+    assert M % 16 == 0
+    return np.float32(lib().oracle_amax_rht(_ptr(xb, _u16p), M, N, sign_mask))
+
+
+def quantize_rowwise(x, amax_value=None, sr=False, seed=0, offset=0):
+    xb = as_bf16_bits(x)
+    M, N = xb.shape
+    assert N % 16 == 0
+    if amax_value is None:
+        amax_value = amax(xb)
+    codes = np.zeros((M, N // 2), dtype=np.uint8)
+    scales = np.zeros((M, N // 16), dtype=np.uint8)
+    gs = np.zeros(2, dtype=np.float32)
+    lib().oracle_quantize_rowwise(_ptr(xb, _u16p), M, N, float(amax_value), int(bool(sr)),
+                                  seed, offset, _ptr(codes, _u8p), _ptr(scales, _u8p),
+                                  _ptr(gs, _f32p))
+    return codes, scales, gs
+
+
+def quantize_colwise(x, amax_value=None, rht=False, sign_mask=0, sr=False, seed=0, offset=0):
+    xb = as_bf16_bits(x)
+    M, N = xb.shape
+    assert M % 16 == 0
+    if amax_value is None:
+        amax_value = amax_rht(xb, sign_mask) if rht else amax(xb)
+    codes = np.zeros((N, M // 2), dtype=np.uint8)
+    scales = np.zeros((N, M // 16), dtype=np.uint8)
+    gs = np.zeros(2, dtype=np.float32)
+    lib().oracle_quantize_colwise(_ptr(xb, _u16p), M, N, float(amax_value), int(bool(rht)),
+                                  sign_mask, int(bool(sr)), seed, offset, _ptr(codes, _u8p),
+                                  _ptr(scales, _u8p), _ptr(gs, _f32p))
+    return codes, scales, gs
+
+
+def quantize_2d(x, amax_value=None):
+    xb = as_bf16_bits(x)
+    M, N = xb.shape
+    assert M % 16 == 0 and N % 16 == 0
+    if amax_value is None:
+        amax_value = amax(xb)
+    rc = np.zeros((M, N // 2), dtype=np.uint8)
+    rs = np.zeros((M, N // 16), dtype=np.uint8)
+    cc = np.zeros((N, M // 2), dtype=np.uint8)
+    cs = np.zeros((N, M // 16), dtype=np.uint8)
+    gs = np.zeros(2, dtype=np.float32)
+    lib().oracle_quantize_2d(_ptr(xb, _u16p), M, N, float(amax_value), _ptr(rc, _u8p),
+                             _ptr(rs, _u8p), _ptr(cc, _u8p), _ptr(cs, _u8p), _ptr(gs, _f32p))
+    return rc, rs, cc, cs, gs
+
+
+def padded_capacity(offsets) -> int:
+    """Sum over experts of the token count rounded up to 16 (columnwise output columns)."""
+    prev, total = 0, 0
+    for o in np.asarray(offsets).tolist():
+        total += (o - prev + 15) // 16 * 16
+        prev = o
+    return total
+
+
+def quantize_grouped(x, offsets, cap=None, rowwise=True, columnwise=True, round_row_sr=False,
+                     round_col_sr=False, rht_col=False, sign_mask=0, seed=0, offset=0,
+                     fill=0):
+    """Grouped quantization. Output buffers start filled with ``fill`` so that untouched
+    regions (the tail past the last offset, columns past the padded total) stay visible."""
+    xb = as_bf16_bits(x)
+    T, H = xb.shape
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    E = off.shape[0]
+    if cap is None:
+        cap = padded_capacity(off)
+    rc = np.full((T, H // 2), fill, dtype=np.uint8) if rowwise else None
+    rs = np.full((T, H // 16), fill, dtype=np.uint8) if rowwise else None
+    rg = np.zeros((E, 2), dtype=np.float32) if rowwise else None
+    cc = np.full((H, cap // 2), fill, dtype=np.uint8) if columnwise else None
+    cs = np.full((H, cap // 16), fill, dtype=np.uint8) if columnwise else None
+    cg = np.zeros((E, 2), dtype=np.float32) if columnwise else None
+    rc_ = rc if rowwise else None
+    status = lib().oracle_quantize_grouped(
+        _ptr(xb, _u16p), T, H, _ptr(off, _i32p), E, cap, int(bool(round_row_sr)),
+        int(bool(round_col_sr)), int(bool(rht_col)), sign_mask, seed, offset,
+        _ptr(rc_, _u8p), _ptr(rs, _u8p), _ptr(rg, _f32p), _ptr(cc, _u8p), _ptr(cs, _u8p),
+        _ptr(cg, _f32p))
+    if status != 0:
+        raise ValueError("invalid offsets or capacity for grouped quantization")
+    return rc, rs, rg, cc, cs, cg
+
+
+def dequantize(codes, scales, s_dec) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    R, half = c.shape
+    C = 2 * half
+    assert s.shape == (R, C // 16)
+    out = np.zeros((R, C), dtype=np.float32)
+    lib().oracle_dequantize(_ptr(c, _u8p), _ptr(s, _u8p), float(np.float32(s_dec)), R, C,
+                            _ptr(out, _f32p))
+    return out
+
+
+@dataclass
+class Config:
+    """The quantizer's options, named as in the C library's configuration."""
+    rowwise: bool = True
+    columnwise: bool = False
+    block2d: bool = False
+    round_row_sr: bool = False
+    round_col_sr: bool = False
+    rht_col: bool = False
+    sign_mask: int = 0
+    seed: int = 0
+    offset: int = 0
+
+
+def quantize(x, cfg: Config):
+    """All outputs one configuration produces, as a dict (the oracle's counterpart of one
+    library call with the amax computed inside)."""
+    xb = as_bf16_bits(x)
+    out = {}
+    if cfg.block2d:
+        rc, rs, cc, cs, gs = quantize_2d(xb)
+        out.update(row_codes=rc, row_scales=rs, row_gscale=gs)
+        if cfg.columnwise:
+            out.update(col_codes=cc, col_scales=cs, col_gscale=gs.copy())
+        if not cfg.rowwise:
+            for k in ("row_codes", "row_scales", "row_gscale"):
+                del out[k]
+        return out
+    if cfg.rowwise:
+        rc, rs, gs = quantize_rowwise(xb, sr=cfg.round_row_sr, seed=cfg.seed, offset=cfg.offset)
+        out.update(row_codes=rc, row_scales=rs, row_gscale=gs)
+    if cfg.columnwise:
+        cc, cs, gs = quantize_colwise(xb, rht=cfg.rht_col, sign_mask=cfg.sign_mask,
+                                      sr=cfg.round_col_sr, seed=cfg.seed, offset=cfg.offset)
+        out.update(col_codes=cc, col_scales=cs, col_gscale=gs)
+    return out
+

@@ -1,0 +1,539 @@
+/*
+ * nvfp4_oracle.c -- the oracle: a plain, scalar CPU statement of NVFP4 block-scaled
+ * quantization, written to be read against the pages, not to be fast.
+ *
+ * TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the benchmark's CPU-baseline
+ * leg load this file. The CUDA library never links, includes or calls it, and it shares no
+ * header, table or helper with the CUDA sources.
+ *
+ * Sources. "[PR4798]" is the page "[nvfp4_training] Optimize CuteDSL kernels for NVFP4
+ * training" (pytorch/ao pull request #4798); sections are named by its headings
+ * ("Optimization" items 1-7, "Fast math", "Grouped allocation tail", "Config surface and
+ * AUTO", "Correctness", and the "Philox divergence between CuteDSL and Triton" part of its
+ * summary). "[Perplexity]" is the page "CuTeDSL at Perplexity" (its Blackwell paragraph on
+ * NVFP4/MXFP8 block reductions).
+ *
+ * Arithmetic. Every step of the method is IEEE binary32 with round-to-nearest-even and
+ * subnormals kept -- the precision the pages fix (an FP32 global scale, packed f32 multiplies,
+ * a div.rn reciprocal, an FP32 Hadamard accumulator). Build with -ffp-contract=off and
+ * without fast-math so that no multiply-add is fused. The format encoders (E4M3, E2M1, BF16)
+ * are exact definitions and use double only where it is exact.
+ *
+ * Where the pages leave a step open, the reading taken is stated beside the code:
+ *   R1 global scale S_enc = 2688 / amax (448 * 6), S_enc = 1 when amax == 0, clamped to
+ *      FLT_MAX when the quotient overflows; S_dec = 1 / S_enc. Stored per tensor as
+ *      {amax, S_dec}.
+ *   R2 block scale s = E4M3_rn_satfinite((bamax / 6) * S_enc), in that order.
+ *   R3 element multiplier r = 1 / (float(s) * S_dec) correctly rounded, r = 0 when the
+ *      product is 0, clamped to FLT_MAX when the reciprocal overflows.
+ *   R4 E2M1 rounding keeps the sign of a value that rounds to zero (code 0x8).
+ *   R5 codes are packed two per byte, the even element in the low nibble.
+ *   R6 the columnwise RHT of a 16-element block v is y = bf16_rne(0.25 * FWHT16(d * v)), with
+ *      FWHT16 the natural-order (Sylvester) Hadamard computed by butterflies in stages
+ *      h = 1, 2, 4, 8, and d_i = -1 where bit i of the sign mask is set.
+ *   R7 stochastic rounding draws one Philox4x32-10 block per 16-element block with
+ *      key = (lo32(seed), hi32(seed)) and counter = (lo32(b), hi32(b), tag, offset), where b
+ *      is the block's linear index in its scale tensor and tag is 0 rowwise, 1 columnwise.
+ *      Word j drives elements 4j..4j+3, byte i of a word drives element 4j+i.
+ *   R8 a stochastically rounded magnitude rounds up by one E2M1 step when the 8 random bits,
+ *      added to the top 8 of the bits of |t| below the E2M1 step at |t|'s binade, carry out;
+ *      the result saturates at 6 (the PTX description of cvt with .rs rounding).
+ *   R9 columnwise outputs are the transposed tensors: codes [N][M/2], scales [N][M/16].
+ *   R10 2D (16x16) scales are written replicated into the rowwise [M][N/16] and columnwise
+ *      [N][M/16] scale tensors.
+ *   R11 grouped: expert e owns rows [off[e-1], off[e]) (off[-1] = 0); its columnwise output
+ *      starts at column sum_{j<e} pad16(n_j) and covers pad16(n_e) zero-padded tokens.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_API __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------------------------------ */
+/* Bit-level views                                                                             */
+/* ------------------------------------------------------------------------------------------ */
+
+static float f32_from_bits(uint32_t u) { float f; memcpy(&f, &u, sizeof f); return f; }
+static uint32_t bits_of_f32(float f) { uint32_t u; memcpy(&u, &f, sizeof u); return u; }
+
+/* BF16 is the upper half of a binary32, so widening is a 16-bit shift and exact
+ * ([PR4798] Optimization item 6). */
+static float bf16_to_f32(uint16_t h) { return f32_from_bits((uint32_t)h << 16); }
+
+/* binary32 -> BF16, round to nearest, ties to even. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u = bits_of_f32(f);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0) {
+    return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays a (quiet) NaN */
+  }
+  uint32_t upper = u >> 16;
+  uint32_t lower = u & 0xFFFFu;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u) != 0)) upper += 1u;
+  return (uint16_t)upper;
+}
+
+/* Round a non-negative double to the nearest integer, ties to the even integer. */
+static double round_half_even(double x) {
+  double f = floor(x);
+  double d = x - f;
+  if (d > 0.5) return f + 1.0;
+  if (d < 0.5) return f;
+  return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* E4M3 (FP8, 1 sign / 4 exponent bits, bias 7 / 3 mantissa bits, no infinities, largest      */
+/* finite 448 = 1.75 * 2^8, subnormals 0.mmm * 2^-6 down to 2^-9). The block-scale format.    */
+/* ------------------------------------------------------------------------------------------ */
+
+static uint8_t e4m3_encode_rn_satfinite(float v) {
+  uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  double a = fabs((double)v);
+  if (isnan(v)) return 0x7F;
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E); /* satfinite: clamp to the largest finite */
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: the value is an integer multiple of 2^-9; q == 8 is 2^-6 = code 0x08 */
+    double q = round_half_even(a * 512.0);
+    return (uint8_t)(sign | (uint8_t)q);
+  }
+  int e2;
+  double m = frexp(a, &e2); /* a = m * 2^e2, m in [0.5, 1) */
+  int e = e2 - 1;           /* a = (2m) * 2^e, 2m in [1, 2) */
+  double mant = round_half_even((2.0 * m - 1.0) * 8.0);
+  if (mant == 8.0) { mant = 0.0; e += 1; }
+  int code = ((e + 7) << 3) | (int)mant;
+  if (code > 0x7E) code = 0x7E;
+  return (uint8_t)(sign | code);
+}
+
+static float e4m3_decode(uint8_t c) {
+  int exp_bits = (c >> 3) & 0xF;
+  int man = c & 0x7;
+  double v;
+  if ((c & 0x7F) == 0x7F) return NAN;
+  if (exp_bits == 0) v = ldexp((double)man, -9);
+  else v = ldexp(1.0 + man / 8.0, exp_bits - 7);
+  return (float)((c & 0x80) ? -v : v);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* E2M1 (FP4, 1 sign / 2 exponent bits / 1 mantissa bit). Magnitudes by code 0..7.            */
+/* ------------------------------------------------------------------------------------------ */
+
+static const double E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+static float e2m1_decode(uint8_t nib) {
+  double v = E2M1_MAG[nib & 7];
+  return (float)((nib & 8) ? -v : v);
+}
+
+/* Round-to-nearest-even onto the E2M1 grid, saturating at 6 (cvt.rn.satfinite.e2m1x2.f32,
+ * [PR4798] Optimization item 1). Ties go to the code with a zero mantissa bit. Reading R4. */
+static uint8_t e2m1_encode_rn_satfinite(float t) {
+  uint8_t sign = signbit(t) ? 8 : 0;
+  double a = fabs((double)t);
+  if (a >= 6.0) return (uint8_t)(sign | 7);
+  int k = 0;
+  while (k < 6 && E2M1_MAG[k + 1] <= a) k++; /* E2M1_MAG[k] <= a < E2M1_MAG[k + 1] */
+  double below = a - E2M1_MAG[k];
+  double above = E2M1_MAG[k + 1] - a;
+  int code;
+  if (below < above) code = k;
+  else if (above < below) code = k + 1;
+  else code = (k % 2 == 0) ? k : k + 1;
+  return (uint8_t)(sign | code);
+}
+
+/* Stochastic rounding onto the E2M1 grid with 8 random bits (cvt.rs.satfinite.e2m1x4.f32,
+ * [PR4798] Optimization item 3). Reading R8: in the binade of |t| the grid step is 0.5 below
+ * 2, 1 in [2, 4) and 2 in [4, 8); |t| = (q + f) * step with q an integer and f in [0, 1).
+ * The discarded fraction f, cut to its top 8 bits, plus the random byte carries out of 8 bits
+ * exactly when the magnitude must round up by one step. Saturates at 6. */
+static uint8_t e2m1_encode_sr_satfinite(float t, uint32_t rand8) {
+  uint8_t sign = signbit(t) ? 8 : 0;
+  double a = fabs((double)t);
+  if (a >= 6.0) return (uint8_t)(sign | 7);
+  double step = (a < 2.0) ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+  double q = floor(a / step);            /* exact: step is a power of two */
+  double f = a / step - q;               /* exact */
+  uint32_t top8 = (uint32_t)floor(f * 256.0);
+  double mag = q * step;
+  if (top8 + (rand8 & 0xFFu) >= 256u) mag += step;
+  int code = 0;
+  while (code < 7 && E2M1_MAG[code] != mag) code++;
+  if (mag > 6.0) code = 7;
+  return (uint8_t)(sign | code);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",   */
+/* SC'11): ten rounds of two 32x32->64 multiplies; the key is bumped by the Weyl constants     */
+/* before every round after the first.                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+static void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; round++) {
+    if (round > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    uint64_t p0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    uint32_t n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The four random words of one 16-element block (reading R7; [PR4798] Optimization item 3:
+ * one counter per block, all four output words consumed). */
+static void block_random_words(uint64_t seed, uint32_t offset, uint32_t tag, uint64_t b,
+                               uint32_t words[4]) {
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t ctr[4] = {(uint32_t)b, (uint32_t)(b >> 32), tag, offset};
+  philox4x32_10(ctr, key, words);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* 16-point random Hadamard transform (reading R6; [PR4798] Optimization item 2 and "Fast      */
+/* math": an FP32 accumulator rounded through BF16 in exact mode).                             */
+/* ------------------------------------------------------------------------------------------ */
+
+static void fwht16(float w[16]) {
+  for (int h = 1; h < 16; h <<= 1) {
+    for (int i = 0; i < 16; i++) {
+      if ((i & h) == 0) {
+        float a = w[i];
+        float b = w[i + h];
+        w[i] = a + b;
+        w[i + h] = a - b;
+      }
+    }
+  }
+}
+
+static void rht16(const float v[16], uint32_t sign_mask, float y[16]) {
+  float w[16];
+  for (int i = 0; i < 16; i++) w[i] = ((sign_mask >> i) & 1u) ? -v[i] : v[i];
+  fwht16(w);
+  for (int i = 0; i < 16; i++) {
+    float scaled = 0.25f * w[i];
+    y[i] = bf16_to_f32(f32_to_bf16_rne(scaled));
+  }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Scales                                                                                      */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Reading R1 ([PR4798] "Fast math": the per-tensor global_decode_scale). */
+static void global_scale(float amax, float* s_enc, float* s_dec) {
+  float enc;
+  if (amax == 0.0f) {
+    enc = 1.0f;
+  } else {
+    enc = 2688.0f / amax;
+    if (!(enc <= FLT_MAX)) enc = FLT_MAX;
+  }
+  *s_enc = enc;
+  *s_dec = 1.0f / enc;
+}
+
+/* Reading R2: the E4M3 block scale from the block amax ([Perplexity] NVFP4 paragraph: a
+ * 16-element absolute maximum per block). */
+static uint8_t block_scale(float bamax, float s_enc) {
+  float per_code = bamax / 6.0f;
+  float s32 = per_code * s_enc;
+  return e4m3_encode_rn_satfinite(s32);
+}
+
+/* Reading R3 ([PR4798] "Fast math": exact mode takes the correctly rounded reciprocal of
+ * pvscale_fp8 * global_decode_scale). */
+static float element_multiplier(uint8_t s, float s_dec) {
+  float p = e4m3_decode(s) * s_dec;
+  if (p == 0.0f) return 0.0f;
+  float r = 1.0f / p;
+  if (!(r <= FLT_MAX)) r = FLT_MAX;
+  return r;
+}
+
+/* Quantize the 16 codes of one block with multiplier r; rand == NULL selects RTNE.
+ * Reading R5 for the packing. */
+static void encode_block(const float v[16], float r, const uint32_t* rand, uint8_t codes[8]) {
+  uint8_t q[16];
+  for (int i = 0; i < 16; i++) {
+    float t = v[i] * r;
+    if (rand) q[i] = e2m1_encode_sr_satfinite(t, (rand[i / 4] >> (8 * (i % 4))) & 0xFFu);
+    else q[i] = e2m1_encode_rn_satfinite(t);
+  }
+  for (int k = 0; k < 8; k++) codes[k] = (uint8_t)(q[2 * k] | (q[2 * k + 1] << 4));
+}
+
+static float abs_max16(const float v[16]) {
+  float m = 0.0f;
+  for (int i = 0; i < 16; i++) {
+    float a = fabsf(v[i]);
+    if (a > m) m = a;
+  }
+  return m;
+}
+
+/* One 1x16 block: block amax -> E4M3 scale -> multiplier -> codes. */
+static void quantize_block16(const float v[16], float s_enc, float s_dec, const uint32_t* rand,
+                             uint8_t codes[8], uint8_t* scale) {
+  uint8_t s = block_scale(abs_max16(v), s_enc);
+  encode_block(v, element_multiplier(s, s_dec), rand, codes);
+  *scale = s;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Exported primitives (pinned one by one in the oracle's own tests)                           */
+/* ------------------------------------------------------------------------------------------ */
+
+ORACLE_API uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+ORACLE_API uint8_t oracle_e4m3_encode(float v) { return e4m3_encode_rn_satfinite(v); }
+ORACLE_API float oracle_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
+ORACLE_API uint8_t oracle_e2m1_encode_rn(float t) { return e2m1_encode_rn_satfinite(t); }
+ORACLE_API uint8_t oracle_e2m1_encode_sr(float t, uint32_t r8) { return e2m1_encode_sr_satfinite(t, r8); }
+ORACLE_API float oracle_e2m1_decode(uint8_t n) { return e2m1_decode(n); }
+ORACLE_API void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  philox4x32_10(ctr, key, out);
+}
+ORACLE_API void oracle_fwht16(float w[16]) { fwht16(w); }
+ORACLE_API void oracle_rht16(const float v[16], uint32_t sign_mask, float y[16]) { rht16(v, sign_mask, y); }
+ORACLE_API void oracle_global_scale(float amax, float out[2]) { global_scale(amax, &out[0], &out[1]); }
+ORACLE_API uint8_t oracle_block_scale(float bamax, float s_enc) { return block_scale(bamax, s_enc); }
+ORACLE_API float oracle_element_multiplier(uint8_t s, float s_dec) { return element_multiplier(s, s_dec); }
+ORACLE_API void oracle_quantize_block16(const float v[16], float s_enc, float s_dec,
+                                        const uint32_t* rand, uint8_t codes[8], uint8_t* scale) {
+  quantize_block16(v, s_enc, s_dec, rand, codes, scale);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Tensors. x is BF16 [M][N] row-major, passed as its 16-bit patterns.                         */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Per-tensor amax over all elements ([PR4798] "Fast math": the amax kernels are exact). */
+ORACLE_API float oracle_amax(const uint16_t* x, int64_t M, int64_t N) {
+  float m = 0.0f;
+  for (int64_t i = 0; i < M * N; i++) {
+    float a = fabsf(bf16_to_f32(x[i]));
+    if (a > m) m = a;
+  }
+  return m;
+}
+
+/* Column block (16 rows starting at row r0, column n) of x, zero where row >= row_end. */
+static void load_column_block(const uint16_t* x, int64_t N, int64_t r0, int64_t row_end,
+                              int64_t n, float v[16]) {
+  for (int i = 0; i < 16; i++) {
+    int64_t r = r0 + i;
+    v[i] = (r < row_end) ? bf16_to_f32(x[r * N + n]) : 0.0f;
+  }
+}
+
+/* amax of the RHT output over every 16-row column block ("Linear RHT amax", [PR4798]
+ * Optimization item 5). Requires M % 16 == 0. */
+ORACLE_API float oracle_amax_rht(const uint16_t* x, int64_t M, int64_t N, uint32_t sign_mask) {
+  float m = 0.0f;
+  for (int64_t n = 0; n < N; n++) {
+    for (int64_t rb = 0; rb < M / 16; rb++) {
+      float v[16], y[16];
+      load_column_block(x, N, rb * 16, M, n, v);
+      rht16(v, sign_mask, y);
+      float a = abs_max16(y);
+      if (a > m) m = a;
+    }
+  }
+  return m;
+}
+
+/* Rowwise 1x16 quantization of rows [row_begin, row_end) with one global scale.
+ * codes [M][N/2], scales [M][N/16]. sr != 0 selects stochastic rounding (tag 0). */
+static void rowwise_rows(const uint16_t* x, int64_t N, int64_t row_begin, int64_t row_end,
+                         float s_enc, float s_dec, int sr, uint64_t seed, uint32_t offset,
+                         uint8_t* codes, uint8_t* scales) {
+  int64_t nb = N / 16;
+  for (int64_t r = row_begin; r < row_end; r++) {
+    for (int64_t b = 0; b < nb; b++) {
+      float v[16];
+      uint32_t rand[4];
+      for (int i = 0; i < 16; i++) v[i] = bf16_to_f32(x[r * N + 16 * b + i]);
+      if (sr) block_random_words(seed, offset, 0u, (uint64_t)(r * nb + b), rand);
+      quantize_block16(v, s_enc, s_dec, sr ? rand : NULL, &codes[r * (N / 2) + 8 * b],
+                       &scales[r * nb + b]);
+    }
+  }
+}
+
+ORACLE_API void oracle_quantize_rowwise(const uint16_t* x, int64_t M, int64_t N, float amax,
+                                        int sr, uint64_t seed, uint32_t offset,
+                                        uint8_t* codes, uint8_t* scales, float gscale[2]) {
+  float s_enc, s_dec;
+  global_scale(amax, &s_enc, &s_dec);
+  gscale[0] = amax;
+  gscale[1] = s_dec;
+  rowwise_rows(x, N, 0, M, s_enc, s_dec, sr, seed, offset, codes, scales);
+}
+
+/* Columnwise 1x16 quantization (blocks of 16 consecutive rows of one column), written
+ * transposed (reading R9). Rows [row_begin, row_begin + 16 * nblk) of x, zero-padded at and
+ * beyond row_end, become output columns [col0, col0 + 16 * nblk) of the [N][ld] output
+ * (ld = output row length in elements). SR uses tag 1 and the block's index in the
+ * [N][ld/16] scale tensor. */
+static void colwise_blocks(const uint16_t* x, int64_t N, int64_t row_begin, int64_t row_end,
+                           int64_t nblk, int64_t ld, int64_t col0, float s_enc, float s_dec,
+                           int rht, uint32_t sign_mask, int sr, uint64_t seed, uint32_t offset,
+                           uint8_t* codes, uint8_t* scales) {
+  for (int64_t n = 0; n < N; n++) {
+    for (int64_t k = 0; k < nblk; k++) {
+      float v[16], y[16];
+      uint32_t rand[4];
+      load_column_block(x, N, row_begin + 16 * k, row_end, n, v);
+      if (rht) rht16(v, sign_mask, y);
+      else memcpy(y, v, sizeof y);
+      int64_t b = n * (ld / 16) + col0 / 16 + k;
+      if (sr) block_random_words(seed, offset, 1u, (uint64_t)b, rand);
+      quantize_block16(y, s_enc, s_dec, sr ? rand : NULL, &codes[n * (ld / 2) + col0 / 2 + 8 * k],
+                       &scales[b]);
+    }
+  }
+}
+
+/* amax_col is the tensor amax, or the RHT amax when rht != 0. Requires M % 16 == 0. */
+ORACLE_API void oracle_quantize_colwise(const uint16_t* x, int64_t M, int64_t N, float amax_col,
+                                        int rht, uint32_t sign_mask, int sr, uint64_t seed,
+                                        uint32_t offset, uint8_t* codes, uint8_t* scales,
+                                        float gscale[2]) {
+  float s_enc, s_dec;
+  global_scale(amax_col, &s_enc, &s_dec);
+  gscale[0] = amax_col;
+  gscale[1] = s_dec;
+  colwise_blocks(x, N, 0, M, M / 16, M, 0, s_enc, s_dec, rht, sign_mask, sr, seed, offset,
+                 codes, scales);
+}
+
+/* 16x16 2D block scaling ([PR4798] Optimization item 2, the 2D weight kernel): one E4M3 scale
+ * per 16x16 tile from the tile amax, shared by the rowwise and the columnwise codes, written
+ * replicated (reading R10). RTNE only. Requires M % 16 == 0 and N % 16 == 0. */
+ORACLE_API void oracle_quantize_2d(const uint16_t* x, int64_t M, int64_t N, float amax,
+                                   uint8_t* row_codes, uint8_t* row_scales,
+                                   uint8_t* col_codes, uint8_t* col_scales, float gscale[2]) {
+  float s_enc, s_dec;
+  global_scale(amax, &s_enc, &s_dec);
+  gscale[0] = amax;
+  gscale[1] = s_dec;
+  for (int64_t tr = 0; tr < M / 16; tr++) {
+    for (int64_t tc = 0; tc < N / 16; tc++) {
+      float tile_amax = 0.0f;
+      for (int i = 0; i < 16; i++) {
+        for (int j = 0; j < 16; j++) {
+          float a = fabsf(bf16_to_f32(x[(16 * tr + i) * N + 16 * tc + j]));
+          if (a > tile_amax) tile_amax = a;
+        }
+      }
+      uint8_t s = block_scale(tile_amax, s_enc);
+      float r = element_multiplier(s, s_dec);
+      for (int i = 0; i < 16; i++) { /* the tile's 16 row segments */
+        int64_t row = 16 * tr + i;
+        float v[16];
+        for (int j = 0; j < 16; j++) v[j] = bf16_to_f32(x[row * N + 16 * tc + j]);
+        encode_block(v, r, NULL, &row_codes[row * (N / 2) + 8 * tc]);
+        row_scales[row * (N / 16) + tc] = s;
+      }
+      for (int j = 0; j < 16; j++) { /* the tile's 16 column segments */
+        int64_t col = 16 * tc + j;
+        float v[16];
+        for (int i = 0; i < 16; i++) v[i] = bf16_to_f32(x[(16 * tr + i) * N + col]);
+        encode_block(v, r, NULL, &col_codes[col * (M / 2) + 8 * tr]);
+        col_scales[col * (M / 16) + tr] = s;
+      }
+    }
+  }
+}
+
+/* Grouped (MoE) quantization ([PR4798] "Grouped allocation tail" and "Config surface and
+ * AUTO": a packed [T][H] tensor with device-side cumulative offsets; rows past the last offset
+ * are not written). Reading R11 for the columnwise layout. offsets[E] are cumulative ends.
+ * Per expert e: amax over its rows; rowwise with that expert's global scale; columnwise over
+ * its pad16(n_e) zero-padded tokens with the expert's (RHT) amax.
+ * Outputs: row_codes [T][H/2], row_scales [T][H/16], row_gscale [E][2]; col_codes [H][cap/2],
+ * col_scales [H][cap/16], col_gscale [E][2]. Either side may be skipped by passing NULL codes.
+ * Returns 0, or -1 when the offsets are not non-decreasing within [0, T] or the padded token
+ * total exceeds cap (then nothing is written). */
+ORACLE_API int oracle_quantize_grouped(const uint16_t* x, int64_t T, int64_t H,
+                                       const int32_t* offsets, int32_t E, int64_t cap,
+                                       int round_row_sr, int round_col_sr, int rht_col,
+                                       uint32_t sign_mask, uint64_t seed, uint32_t offset,
+                                       uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,
+                                       uint8_t* col_codes, uint8_t* col_scales, float* col_gscale) {
+  int64_t padded_total = 0;
+  int64_t prev = 0;
+  for (int32_t e = 0; e < E; e++) {
+    if (offsets[e] < prev || offsets[e] > T) return -1;
+    padded_total += ((offsets[e] - prev) + 15) / 16 * 16;
+    prev = offsets[e];
+  }
+  if (col_codes && padded_total > cap) return -1;
+
+  int64_t col_start = 0;
+  for (int32_t e = 0; e < E; e++) {
+    int64_t start = (e == 0) ? 0 : offsets[e - 1];
+    int64_t end = offsets[e];
+    int64_t n = end - start;
+    int64_t nblk = (n + 15) / 16;
+    float amax = oracle_amax(x + start * H, n, H);
+    if (row_codes) {
+      float s_enc, s_dec;
+      global_scale(amax, &s_enc, &s_dec);
+      row_gscale[2 * e] = amax;
+      row_gscale[2 * e + 1] = s_dec;
+      rowwise_rows(x, H, start, end, s_enc, s_dec, round_row_sr, seed, offset, row_codes,
+                   row_scales);
+    }
+    if (col_codes) {
+      float amax_col = amax;
+      if (rht_col) {
+        amax_col = 0.0f;
+        for (int64_t h = 0; h < H; h++) {
+          for (int64_t k = 0; k < nblk; k++) {
+            float v[16], y[16];
+            load_column_block(x, H, start + 16 * k, end, h, v);
+            rht16(v, sign_mask, y);
+            float a = abs_max16(y);
+            if (a > amax_col) amax_col = a;
+          }
+        }
+      }
+      float s_enc, s_dec;
+      global_scale(amax_col, &s_enc, &s_dec);
+      col_gscale[2 * e] = amax_col;
+      col_gscale[2 * e + 1] = s_dec;
+      colwise_blocks(x, H, start, end, nblk, cap, col_start, s_enc, s_dec, rht_col, sign_mask,
+                     round_col_sr, seed, offset, col_codes, col_scales);
+    }
+    col_start += 16 * nblk;
+  }
+  return 0;
+}
+
+/* Dequantization: x_hat = (e2m1(q) * float(s)) * S_dec. The inner product is exact (2 + 4
+ * significant bits). codes [R][C/2], scales [R][C/16], out [R][C]. */
+ORACLE_API void oracle_dequantize(const uint8_t* codes, const uint8_t* scales, float s_dec,
+                                  int64_t R, int64_t C, float* out) {
+  for (int64_t r = 0; r < R; r++) {
+    for (int64_t c = 0; c < C; c++) {
+      uint8_t byte = codes[r * (C / 2) + c / 2];
+      uint8_t nib = (c % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      float s = e4m3_decode(scales[r * (C / 16) + c / 16]);
+      float v = e2m1_decode(nib) * s;
+      out[r * C + c] = v * s_dec;
+    }
+  }
+}
