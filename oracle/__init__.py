@@ -45,6 +45,7 @@ def lib():
             "oracle_e2m1_encode_rn": (ctypes.c_uint8, [ctypes.c_float]),
             "oracle_e2m1_encode_sr": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_uint32]),
             "oracle_e2m1_decode": (ctypes.c_float, [ctypes.c_uint8]),
+            "oracle_sr_random16": (ctypes.c_uint32, [ctypes.c_uint32, ctypes.c_int32]),
             "oracle_philox4x32_10": (None, [_u32p, _u32p, _u32p]),
             "oracle_fwht16": (None, [_f32p]),
             "oracle_rht16": (None, [_f32p, ctypes.c_uint32, _f32p]),
@@ -117,11 +118,15 @@ def e2m1_encode_rn(values) -> np.ndarray:
     return np.array([lib().oracle_e2m1_encode_rn(float(f)) for f in v], dtype=np.uint8)
 
 
-def e2m1_encode_sr(values, rand8) -> np.ndarray:
+def e2m1_encode_sr(values, rand16) -> np.ndarray:
     v = np.asarray(values, dtype=np.float32).ravel()
-    r = np.broadcast_to(np.asarray(rand8, dtype=np.uint32), v.shape)
+    r = np.broadcast_to(np.asarray(rand16, dtype=np.uint32), v.shape)
     return np.array([lib().oracle_e2m1_encode_sr(float(f), int(b)) for f, b in zip(v, r)],
                     dtype=np.uint8)
+
+
+def sr_random16(word: int, i: int) -> int:
+    return lib().oracle_sr_random16(word, i)
 
 
 def e2m1_decode(codes) -> np.ndarray:

@@ -400,32 +400,50 @@ def test_2d_codes_transpose_and_tile_scale():
 # ------------------------------------------------------------------------------------------
 
 def test_sr_grid_values_are_fixed_points():
+    rng = np.random.Generator(np.random.PCG64(30))
+    u = np.concatenate([[0, 1, 0x8000, 0xFFFF], rng.integers(0, 1 << 16, 252)])
     for g in GRID:
         for sgn in (1.0, -1.0):
-            codes = oracle.e2m1_encode_sr(np.full(256, sgn * g, np.float32), np.arange(256))
+            codes = oracle.e2m1_encode_sr(np.full(u.size, sgn * g, np.float32), u)
             assert np.all(codes == oracle.e2m1_encode_rn([sgn * g])[0])
 
 
-def test_sr_mean_over_all_random_bytes_is_the_truncated_value():
-    """Averaging over the 256 random bytes: E[q] = lo + step * floor(256 f) / 256, so the
-    bias is below step/256 and exactly zero at halfway values (50/50 split)."""
+def test_sr_mean_over_all_random_values_is_the_truncated_value():
+    """Averaging over all 2^16 random values: E[q] = lo + step * floor(2^16 f) / 2^16, so the
+    bias is below step / 2^16 and exactly zero at halfway values (a 50/50 split)."""
     rng = np.random.Generator(np.random.PCG64(24))
-    vals = np.concatenate([rng.uniform(0, 6, 300), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]])
-    for t in vals.astype(np.float32):
-        codes = oracle.e2m1_encode_sr(np.full(256, t, np.float32), np.arange(256))
+    vals = np.concatenate([rng.uniform(0, 6, 6), [0.25, 1.75, 5.0, 4.00390625]]).astype(np.float32)
+    u = np.arange(1 << 16)
+    for t in vals:
+        codes = oracle.e2m1_encode_sr(np.full(u.size, t, np.float32), u)
         mean = oracle.e2m1_decode(codes).astype(np.float64).mean()
         step = 0.5 if t < 2 else (1.0 if t < 4 else 2.0)
         lo = np.floor(t / step) * step
-        expect = lo + step * np.floor((t - lo) / step * 256) / 256
+        expect = lo + step * np.floor((t - lo) / step * 65536) / 65536
         assert mean == pytest.approx(expect, abs=1e-12)
-        assert abs(mean - t) < step / 256 + 1e-12
+        assert abs(mean - t) < step / 65536 + 1e-12
+
+
+def test_sr_random_values_of_a_word_are_uniform_per_element():
+    """Each element's 16-bit value is a bijection of 16 bits of the word: over words covering
+    those bits it takes every value once."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    for i in range(4):
+        base = int(rng.integers(0, 1 << 32))
+        keep = 0xFF00FF00 if i >= 2 else 0x00FF00FF
+        seen = set()
+        for v in range(1 << 16):
+            spread = (v & 0xFF) << (8 if i >= 2 else 0) | (v >> 8) << (24 if i >= 2 else 16)
+            w = (base & ~keep & 0xFFFFFFFF) | spread
+            seen.add(oracle.sr_random16(w, i))
+        assert len(seen) == 1 << 16
 
 
 def test_sr_at_most_one_step_from_rtne_with_same_sign():
     rng = np.random.Generator(np.random.PCG64(25))
     t = rng.uniform(-7, 7, 4000).astype(np.float32)
-    r8 = rng.integers(0, 256, t.size)
-    sr = oracle.e2m1_encode_sr(t, r8)
+    r16 = rng.integers(0, 1 << 16, t.size)
+    sr = oracle.e2m1_encode_sr(t, r16)
     rn = oracle.e2m1_encode_rn(t)
     assert np.all((sr & 8) == (rn & 8))
     assert np.all(np.abs((sr & 7).astype(int) - (rn & 7).astype(int)) <= 1)
