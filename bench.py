@@ -1,0 +1,397 @@
+"""Benchmark: NVFP4 quantize throughput (GB/s of BF16-in ideal bytes) on GB300.
+
+One step = the whole hot path on one batch of seeded synthetic input resident in HBM: the amax
+pass (nvfp4_amax) and the quantize pass (nvfp4_quantize with that amax), i.e. every kernel a
+caller runs to turn a BF16 tensor into NVFP4 codes, E4M3 scales and FP32 global scales.
+Ideal bytes per step = one BF16 read + code writes + scale writes (the metric's roofline
+bytes). L2 is flushed (a 256 MiB write) before every timed step; device time comes from CUDA
+events on the launching stream. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--pipeline two_pass]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_block_scaled_quantize_gb300 import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "activation_8192x4096_rowcol_rtne"
+METRIC = "NVFP4 quantize GB/s (BF16 in) and fraction of GB300 HBM roofline, 1 GPU"
+FLUSH_BYTES = 256 << 20
+
+
+def ideal_bytes(w: workloads.Workload, rows=None, offsets=None) -> int:
+    """One BF16 read + codes (half a byte per element) + scales (1/16 byte per element) per
+    produced orientation. Grouped columnwise outputs count their padded tokens."""
+    M = w.rows if rows is None else rows
+    N = w.cols
+    b = 2 * M * N
+    if w.rowwise:
+        b += M * N // 2 + M * N // 16
+    if w.columnwise:
+        P = M
+        if w.grouped and offsets is not None:
+            P = int(sum((int(c) + 15) // 16 * 16 for c in np.diff(np.concatenate([[0], offsets]))))
+        b += P * N // 2 + P * N // 16
+    return b
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and workload, valid
+    only while the kernel source is unchanged (its sha256 is recorded in the summary)."""
+    summary = os.path.join(ROOT, "profiles", "quantize_tiles_%s.txt" % workload)
+    src = os.path.join(ROOT, "nvfp4_block_scaled_quantize_gb300", "csrc", kernel_file)
+    if not (os.path.exists(summary) and os.path.exists(src)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    fields = {}
+    for line in open(summary):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha256_16") != digest:
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value):
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def quant_kwargs(w, inp):
+    return dict(rowwise=w.rowwise, columnwise=w.columnwise, block2d=w.block2d,
+                rht_col=w.rht_col, sign_mask=inp["sign_mask"], seed=inp["seed"],
+                round_row="sr" if w.round_row_sr else "rn",
+                round_col="sr" if w.round_col_sr else "rn")
+
+
+def _oracle_run(w, inp, rows):
+    """The oracle, as it stands, on the first `rows` rows of the workload (amax + outputs)."""
+    import oracle
+    xb = oracle.as_bf16_bits(inp["x"])[:rows]
+    t0 = time.perf_counter()
+    if w.grouped:
+        off = np.minimum(inp["offsets"], rows).astype(np.int32)
+        oracle.quantize_grouped(xb, off, rowwise=w.rowwise, columnwise=w.columnwise,
+                                round_row_sr=w.round_row_sr, round_col_sr=w.round_col_sr,
+                                rht_col=w.rht_col, sign_mask=inp["sign_mask"], seed=inp["seed"])
+    else:
+        oracle.quantize(xb, oracle.Config(rowwise=w.rowwise, columnwise=w.columnwise,
+                                          block2d=w.block2d, round_row_sr=w.round_row_sr,
+                                          round_col_sr=w.round_col_sr, rht_col=w.rht_col,
+                                          sign_mask=inp["sign_mask"], seed=inp["seed"]))
+    return time.perf_counter() - t0
+
+
+def cpu_sample_rows(w, inp, budget_s):
+    """Rows (a multiple of 64) of the workload the oracle processes in about budget_s."""
+    rows = 64
+    dt = _oracle_run(w, inp, rows)
+    while dt < budget_s / 8 and rows < w.rows:
+        rows = min(w.rows, rows * 4)
+        dt = _oracle_run(w, inp, rows)
+    rows = int(min(w.rows, max(64, rows * budget_s / max(dt, 1e-6) // 64 * 64)))
+    return rows
+
+
+def cpu_baseline(w, inp, budget_s=15.0):
+    """Oracle throughput on a bounded sample, in the metric's unit (ideal bytes / s)."""
+    rows = cpu_sample_rows(w, inp, budget_s)
+    dt = _oracle_run(w, inp, rows)
+    off = np.minimum(inp["offsets"], rows) if w.grouped else None
+    b = ideal_bytes(w, rows, off)
+    return {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d rows of %s (amax + every output), %.2f s on 1 core"
+                      % (rows, w.rows, w.name, dt)}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the oracle on the host cores, rank 0 only (the other ranks exit)."""
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_input(w)
+    budget = min(10.0, 150.0 / (args.steps + args.warmup))
+    rows = cpu_sample_rows(w, inp, budget)
+    off = np.minimum(inp["offsets"], rows) if w.grouped else None
+    b = ideal_bytes(w, rows, off)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = _oracle_run(w, inp, rows)
+        if i >= args.warmup:
+            times.append(dt)
+    value = b * len(times) / sum(times) / 1e9
+    sample = "first %d of %d rows of %s per step (amax + every output), 1 core" % (
+        rows, w.rows, w.name)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "sample_rows": rows},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    from nvfp4_block_scaled_quantize_gb300 import api, _lib
+    _lib.load()
+    dev = torch.device("cuda", local)
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_input(w)
+    x = inp["x"].to(dev)
+    kw = quant_kwargs(w, inp)
+    ideal = ideal_bytes(w, offsets=inp.get("offsets"))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    if w.grouped:
+        offsets = torch.from_numpy(inp["offsets"]).to(dev)
+        cap = int(sum((int(c) + 15) // 16 * 16 for c in np.diff(np.concatenate([[0], inp["offsets"]]))))
+        out = api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise, col_ld=cap,
+                                groups=w.experts)
+
+        def step(ev=None):
+            if ev:
+                ev[0].record(stream)
+            api.nvfp4_quantize_grouped(x, offsets, col_capacity=cap, out=out,
+                                       **{k: v for k, v in kw.items() if k != "block2d"})
+            if ev:
+                ev[2].record(stream)
+        launches_per_step = 2
+        kernel_split = False
+    else:
+        out = api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise)
+        rht_amax = w.rht_col
+
+        def step(ev=None):
+            if ev:
+                ev[0].record(stream)
+            a_row, a_col = api.nvfp4_amax(x, rht_col=rht_amax, sign_mask=kw["sign_mask"])
+            if ev:
+                ev[1].record(stream)
+            api.nvfp4_quantize(x, amax_row=a_row, amax_col=a_col, out=out, **kw)
+            if ev:
+                ev[2].record(stream)
+        launches_per_step = 2
+        kernel_split = True
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    status, bits = api.nvfp4_get_status(dev)
+    if status != 0:
+        raise RuntimeError("device status %d (bits %#x) after warm-up" % (status, bits))
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        time.sleep(0.3)
+        for i in range(args.steps):
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize(dev)
+        time.sleep(0.2)
+    barrier(world)
+    step_ms = [e[0].elapsed_time(e[2]) for e in events]
+    quant_ms = [e[1].elapsed_time(e[2]) for e in events] if kernel_split else None
+    total_s = sum(step_ms) / 1e3
+    total_s = max_over_ranks(world, total_s)
+    value = ideal * args.steps * world / total_s / 1e9
+
+    # end to end through the public API: pinned host input -> device -> quantize -> pinned host
+    x_host = inp["x"].pin_memory()
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = x_host.numel() * 2
+    d2h = sum(v.numel() * v.element_size() for v in out.values())
+
+    def e2e_step():
+        xd = x_host.to(dev, non_blocking=True)
+        if w.grouped:
+            o = api.nvfp4_quantize_grouped(xd, offsets, col_capacity=cap,
+                                           **{k: v for k, v in kw.items() if k != "block2d"})
+        else:
+            o = api.nvfp4_quantize(xd, **kw)
+        for k, v in o.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(world, e0.elapsed_time(e1) / 1e3)
+    e2e_value = ideal * args.steps * world / e2e_s / 1e9
+
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": [w.rows, w.cols],
+                   "ideal_bytes_per_step": ideal,
+                   "pipeline": "amax pass + quantize pass (two launches)",
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+    }
+    if kernel_split:
+        qk = statistics.mean(quant_ms) / 1e3
+        achieved = ideal / qk / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                            "frac": achieved / hbm, "peak_kind": peak_kind,
+                            "kernel": "quantize_tiles_kernel",
+                            "kernel_us": qk * 1e6,
+                            "traffic": kernel_traffic("quantize_tiles.cu", w.name)}
+        amax_us = statistics.mean([e[0].elapsed_time(e[1]) for e in events]) * 1e3
+        line["amax_pass_us"] = amax_us
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4: NVFP4 block-scaled quantization of BF16 tensors on one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation is the one described on the page "[nvfp4_training] Optimize CuteDSL kernels
+ * for NVFP4 training" (pytorch/ao pull request #4798), cited below as [PR4798] with its
+ * section headings, and in the NVFP4 paragraph of the page "CuTeDSL at Perplexity":
+ *   - a per-tensor FP32 amax and global scale (S_enc = 2688 / amax, S_dec = 1 / S_enc; 2688 is
+ *     448, the largest E4M3 value, times 6, the largest E2M1 value; S_enc = 1 when amax = 0);
+ *   - one FP8-E4M3 scale per 16-element block, s = E4M3((block_amax / 6) * S_enc);
+ *   - every element multiplied by r = 1 / (float(s) * S_dec) (correctly rounded; r = 0 for a
+ *     zero scale) and rounded to E2M1 (FP4: 0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6), by
+ *     round-to-nearest-even or by stochastic rounding ([PR4798] "Optimization" items 1 and 3,
+ *     "Fast math": this library implements the exact mode);
+ *   - codes packed two per byte, the even element in the low nibble.
+ *
+ * Layouts (all row-major, all buffers owned and allocated by the caller):
+ *   x            BF16 [M][N]                          (2 bytes per element)
+ *   row codes    uint8 [M][N/2],  row scales  uint8 (E4M3) [M][N/16]
+ *   col codes    uint8 [N][M/2],  col scales  uint8 (E4M3) [N][M/16]   (the transposed tensor)
+ *   gscale       float [2] = {amax, S_dec}               (grouped: float [E][2])
+ * Columnwise blocks run along M (16 consecutive rows of one column); their outputs are the
+ * rowwise outputs of x transposed, optionally after a 16-point random Hadamard transform.
+ *
+ * Execution: every call is asynchronous on the caller's stream (a cudaStream_t passed as
+ * void*; NULL is the legacy default stream). Pointers marked (device) must be device (or
+ * managed) memory, 16-byte aligned. The return value reports argument checks and launch
+ * errors only; problems the device detects (bad grouped offsets, a bounded wait that gave up)
+ * are recorded in a per-device status word read by nvfp4_get_status. A call that returns an
+ * error status launched nothing and wrote nothing.
+ *
+ * Memory: the library allocates no memory on these calls except once per device, on the
+ * first call that needs it: a small workspace (status word, grid-barrier state and per-block
+ * partial maxima, under 16 KiB) allocated with cudaMalloc and kept until exit. Make that first
+ * call outside CUDA-graph capture.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,   /* NULL pointer where one is required, negative size, bad enum */
+  NVFP4_ERR_SHAPE = 2,         /* a dimension is not a multiple of 16 where blocks need it */
+  NVFP4_ERR_ALIGN = 3,         /* a pointer or row pitch is not 16-byte aligned */
+  NVFP4_ERR_UNSUPPORTED = 4,   /* an option combination the method does not define */
+  NVFP4_ERR_CUDA = 5,          /* a CUDA runtime call or a kernel launch failed */
+  NVFP4_ERR_DEVICE_STATUS = 6, /* the device flagged its input (nvfp4_get_status) */
+  NVFP4_ERR_TIMEOUT = 7        /* a bounded device-side wait gave up (nvfp4_get_status) */
+} nvfp4_status;
+
+typedef enum nvfp4_rounding {
+  NVFP4_ROUND_RN = 0,          /* round to nearest, ties to even */
+  NVFP4_ROUND_SR = 1           /* stochastic rounding driven by Philox4x32-10 */
+} nvfp4_rounding;
+
+/* Device status bits (nvfp4_get_status). */
+#define NVFP4_DEVICE_BAD_OFFSETS 0x1u  /* grouped offsets not non-decreasing within [0, T],
+                                          or padded token total above the column capacity */
+#define NVFP4_DEVICE_TIMEOUT     0x2u  /* a grid barrier or a copy wait passed its limit */
+
+/* Options of one quantization. Zero-initialise and set what is needed. */
+typedef struct nvfp4_config {
+  int32_t rowwise;        /* produce rowwise codes/scales (1x16 blocks along N) */
+  int32_t columnwise;     /* produce columnwise codes/scales (1x16 blocks along M, transposed) */
+  int32_t block2d;        /* one scale per 16x16 tile shared by both orientations, written
+                             replicated into both scale tensors ([PR4798] "Optimization"
+                             item 2, the 2D weight kernel); RTNE only, no RHT */
+  int32_t round_row;      /* nvfp4_rounding of the rowwise codes */
+  int32_t round_col;      /* nvfp4_rounding of the columnwise codes */
+  int32_t rht_col;        /* apply the 16-point random Hadamard transform to each columnwise
+                             block before quantizing: y = bf16(0.25 * H16 (d * v)), H16 the
+                             Sylvester Hadamard matrix, d the sign vector below ([PR4798]
+                             "Optimization" items 2 and 5, "Fast math": the accumulator is
+                             rounded through BF16 in exact mode) */
+  uint32_t rht_sign_mask; /* bit i set: d_i = -1 (bits 16..31 must be zero) */
+  uint32_t rng_offset;    /* Philox counter word 3 (advance it to draw a new stream) */
+  uint64_t rng_seed;      /* Philox key = (low 32 bits, high 32 bits) */
+  int32_t fused_amax;     /* when the amax inputs are NULL: 0 = amax pass + quantize pass,
+                             1 = one cooperative launch with a bounded grid barrier */
+  int32_t reserved;       /* must be zero */
+} nvfp4_config;
+
+/* Stochastic rounding ([PR4798] "Optimization" item 3 and "Correctness"): one Philox4x32-10
+ * draw per 16-element block with key (lo32 seed, hi32 seed) and counter (lo32 b, hi32 b, tag,
+ * rng_offset), b the block's linear index in its scale tensor ([M][N/16] rowwise, [N][M/16]
+ * columnwise; grouped columnwise: [H][capacity/16]), tag 0 rowwise and 1 columnwise. Word j
+ * of the draw is the random operand of the cvt.rs.satfinite.e2m1x4.f32 that converts elements
+ * 4j..4j+3 of the block. The stream is a pure function of (seed, offset, block position). */
+
+/* Text for a status code (static storage). */
+const char* nvfp4_status_string(nvfp4_status status);
+
+/* Per-tensor absolute maxima ([PR4798] "Optimization" item 5: the amax and RHT-amax kernels,
+ * "always exact").
+ *   x        (device) BF16 [M][N], 16-byte aligned; N % 16 == 0 (M % 16 == 0 with rht_col).
+ *   cfg      rht_col / rht_sign_mask select what amax_col measures.
+ *   amax_row (device) float[1] or NULL: receives max |x|.
+ *   amax_col (device) float[1] or NULL: receives max |y| over the RHT output y of every
+ *            16-row column block when cfg->rht_col, else max |x|.
+ * M == 0 or N == 0 writes 0. */
+nvfp4_status nvfp4_amax(const void* x, int64_t M, int64_t N, const nvfp4_config* cfg,
+                        float* amax_row, float* amax_col, void* stream);
+
+/* Quantize one BF16 tensor, rowwise and/or columnwise, from one read of x.
+ *   x                   (device) BF16 [M][N]; N % 16 == 0; M % 16 == 0 when columnwise or
+ *                       block2d.
+ *   amax_row, amax_col  (device) float[1] each, or NULL to compute them inside this call
+ *                       (amax_col is the RHT amax when cfg->rht_col). With block2d both
+ *                       orientations use amax_row.
+ *   row_codes [M][N/2], row_scales [M][N/16], row_gscale [2]: (device) outputs, required when
+ *                       cfg->rowwise (or block2d with rowwise), else ignored.
+ *   col_codes [N][M/2], col_scales [N][M/16], col_gscale [2]: (device) outputs, required when
+ *                       cfg->columnwise, else ignored.
+ * Errors: NVFP4_ERR_UNSUPPORTED for block2d with RHT or SR, or neither orientation selected;
+ * NVFP4_ERR_SHAPE / _ALIGN for the shape and alignment rules above. */
+nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N, const nvfp4_config* cfg,
+                            const float* amax_row, const float* amax_col,
+                            uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,
+                            uint8_t* col_codes, uint8_t* col_scales, float* col_gscale,
+                            void* stream);
+
+/* Grouped (MoE) quantization of a packed [T][H] tensor whose rows are split among E experts
+ * by device-side cumulative offsets ([PR4798] "Grouped allocation tail", "Config surface and
+ * AUTO": a packed tensor plus device-side offsets; rows past offsets[E-1] are not read or
+ * written).
+ *   offsets      (device) int32 [E], non-decreasing, offsets[E-1] <= T; expert e owns rows
+ *                [offsets[e-1], offsets[e]) with offsets[-1] = 0 (empty experts allowed).
+ *   E            1 <= E <= 256.
+ *   col_capacity columns of the columnwise outputs, a multiple of 16, >= sum_e pad16(n_e)
+ *                (pad16 rounds a token count up to a multiple of 16). Expert e's columnwise
+ *                block starts at column sum_{j<e} pad16(n_j); its last partial 16-token block
+ *                is zero-padded before the transform and stored in full.
+ *   Per expert: amax over its rows and global scale for the rowwise side; RHT amax (or amax)
+ *   over its zero-padded blocks for the columnwise side. Outputs:
+ *   row_codes [T][H/2], row_scales [T][H/16], row_gscale [E][2];
+ *   col_codes [H][col_capacity/2], col_scales [H][col_capacity/16], col_gscale [E][2].
+ * H % 16 == 0. block2d and fused_amax are not supported here. Offsets that break the rules
+ * above set NVFP4_DEVICE_BAD_OFFSETS and the kernels write no codes. */
+nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
+                                    const int32_t* offsets, int32_t E, int64_t col_capacity,
+                                    const nvfp4_config* cfg,
+                                    uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,
+                                    uint8_t* col_codes, uint8_t* col_scales, float* col_gscale,
+                                    void* stream);
+
+/* Dequantize codes back to FP32: out[r][c] = (e2m1(code) * e4m3(scale[r][c/16])) * S_dec,
+ * S_dec = gscale[1] (the check used by the reconstruction tests of [PR4798] "Correctness").
+ *   codes (device) [R][C/2], scales (device) [R][C/16], gscale (device) float[2],
+ *   out (device) float [R][C]; C % 16 == 0. Columnwise outputs dequantize with R = N, C = M. */
+nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
+                              int64_t R, int64_t C, float* out, void* stream);
+
+/* Synchronize `stream`, then read and clear the current device's status word into
+ * *device_status (NVFP4_DEVICE_* bits). Returns NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT
+ * when bits were set, NVFP4_OK otherwise. */
+nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

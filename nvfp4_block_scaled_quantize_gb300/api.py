@@ -1,0 +1,170 @@
+"""Python binding of the C ABI in include/nvfp4.h, with the same entry-point names.
+
+Argument marshalling only: torch supplies device memory and the current CUDA stream; every
+step of the computation runs in libnvfp4's kernels. Outputs are allocated here with
+torch.empty on the input's device and returned in a dict:
+
+    row_codes  uint8 [M, N/2]    row_scales  uint8 (E4M3 bits) [M, N/16]   row_gscale  float32 [2]
+    col_codes  uint8 [N, M/2]    col_scales  uint8 (E4M3 bits) [N, M/16]   col_gscale  float32 [2]
+
+(gscale = [amax, S_dec]; grouped: [E, 2]).
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import Config, NVFP4Error, ROUND_RN, ROUND_SR
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_x(x):
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise TypeError("x must be a 2-D torch.bfloat16 tensor")
+    if not x.is_cuda:
+        raise TypeError("x must live on a CUDA device (see quantize_from_host for host input)")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous (row-major)")
+
+
+def _round(v):
+    if v in ("rn", ROUND_RN, None):
+        return ROUND_RN
+    if v in ("sr", ROUND_SR):
+        return ROUND_SR
+    raise ValueError("rounding must be 'rn' or 'sr'")
+
+
+def make_config(rowwise=True, columnwise=False, block2d=False, round_row="rn", round_col="rn",
+                rht_col=False, sign_mask=0, seed=0, offset=0, fused_amax=False) -> Config:
+    return Config(rowwise=int(bool(rowwise)), columnwise=int(bool(columnwise)),
+                  block2d=int(bool(block2d)), round_row=_round(round_row),
+                  round_col=_round(round_col), rht_col=int(bool(rht_col)),
+                  rht_sign_mask=int(sign_mask), rng_offset=int(offset), rng_seed=int(seed),
+                  fused_amax=int(bool(fused_amax)), reserved=0)
+
+
+def _raise_if(status, where):
+    if status != _lib.NVFP4_OK:
+        raise NVFP4Error(status, where)
+
+
+def nvfp4_amax(x, rht_col=False, sign_mask=0):
+    """Per-tensor amax: returns (max |x|, max |RHT(x)| if rht_col else max |x|) as float32[1]
+    device tensors."""
+    _check_x(x)
+    L = _lib.load()
+    M, N = x.shape
+    cfg = make_config(rht_col=rht_col, sign_mask=sign_mask)
+    a_row = torch.empty(1, dtype=torch.float32, device=x.device)
+    a_col = torch.empty(1, dtype=torch.float32, device=x.device)
+    _raise_if(L.nvfp4_amax(_ptr(x), M, N, ctypes.byref(cfg), _ptr(a_row), _ptr(a_col),
+                           _stream(x.device)), "nvfp4_amax")
+    return a_row, a_col
+
+
+def alloc_outputs(M, N, device, rowwise=True, columnwise=False, col_ld=None, groups=None):
+    out = {}
+    g = () if groups is None else (groups,)
+    if rowwise:
+        out["row_codes"] = torch.empty((M, N // 2), dtype=torch.uint8, device=device)
+        out["row_scales"] = torch.empty((M, N // 16), dtype=torch.uint8, device=device)
+        out["row_gscale"] = torch.empty(g + (2,), dtype=torch.float32, device=device)
+    if columnwise:
+        ld = M if col_ld is None else col_ld
+        out["col_codes"] = torch.empty((N, ld // 2), dtype=torch.uint8, device=device)
+        out["col_scales"] = torch.empty((N, ld // 16), dtype=torch.uint8, device=device)
+        out["col_gscale"] = torch.empty(g + (2,), dtype=torch.float32, device=device)
+    return out
+
+
+def nvfp4_quantize(x, rowwise=True, columnwise=False, block2d=False, round_row="rn",
+                   round_col="rn", rht_col=False, sign_mask=0, seed=0, offset=0,
+                   fused_amax=False, amax_row=None, amax_col=None, out=None):
+    """Quantize a BF16 [M, N] CUDA tensor. amax_row / amax_col (float32[1] device tensors)
+    skip the amax pass; `out` reuses preallocated outputs (see alloc_outputs)."""
+    _check_x(x)
+    L = _lib.load()
+    M, N = x.shape
+    cfg = make_config(rowwise, columnwise, block2d, round_row, round_col, rht_col, sign_mask,
+                      seed, offset, fused_amax)
+    if out is None:
+        out = alloc_outputs(M, N, x.device, rowwise, columnwise)
+    g = out.get
+    status = L.nvfp4_quantize(_ptr(x), M, N, ctypes.byref(cfg), _ptr(amax_row), _ptr(amax_col),
+                              _ptr(g("row_codes")), _ptr(g("row_scales")), _ptr(g("row_gscale")),
+                              _ptr(g("col_codes")), _ptr(g("col_scales")), _ptr(g("col_gscale")),
+                              _stream(x.device))
+    _raise_if(status, "nvfp4_quantize")
+    return out
+
+
+def padded_capacity(counts) -> int:
+    return int(sum((int(c) + 15) // 16 * 16 for c in counts))
+
+
+def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwise=True,
+                           round_row="rn", round_col="rn", rht_col=False, sign_mask=0, seed=0,
+                           offset=0, out=None):
+    """Grouped quantization of a packed BF16 [T, H] tensor; `offsets` is an int32 [E] device
+    tensor of cumulative expert ends. col_capacity defaults to T + 16 * E (always enough)."""
+    _check_x(x)
+    L = _lib.load()
+    if offsets.dtype != torch.int32 or not offsets.is_cuda or offsets.dim() != 1:
+        raise TypeError("offsets must be a 1-D int32 CUDA tensor")
+    T, H = x.shape
+    E = offsets.shape[0]
+    if col_capacity is None:
+        col_capacity = (T + 15) // 16 * 16 + 16 * E
+    cfg = make_config(rowwise, columnwise, False, round_row, round_col, rht_col, sign_mask, seed,
+                      offset)
+    if out is None:
+        out = alloc_outputs(T, H, x.device, rowwise, columnwise, col_ld=col_capacity, groups=E)
+    g = out.get
+    status = L.nvfp4_quantize_grouped(
+        _ptr(x), T, H, _ptr(offsets), E, col_capacity, ctypes.byref(cfg),
+        _ptr(g("row_codes")), _ptr(g("row_scales")), _ptr(g("row_gscale")),
+        _ptr(g("col_codes")), _ptr(g("col_scales")), _ptr(g("col_gscale")), _stream(x.device))
+    _raise_if(status, "nvfp4_quantize_grouped")
+    return out
+
+
+def nvfp4_dequantize(codes, scales, gscale):
+    """FP32 [R, C] reconstruction of codes [R, C/2] with scales [R, C/16] and gscale [2]."""
+    L = _lib.load()
+    R, half = codes.shape
+    C = 2 * half
+    out = torch.empty((R, C), dtype=torch.float32, device=codes.device)
+    _raise_if(L.nvfp4_dequantize(_ptr(codes), _ptr(scales), _ptr(gscale), R, C, _ptr(out),
+                                 _stream(codes.device)), "nvfp4_dequantize")
+    return out
+
+
+def nvfp4_get_status(device=None):
+    """Synchronize the current stream and return (status, device status bits); clears them."""
+    L = _lib.load()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    bits = ctypes.c_uint32(0)
+    status = L.nvfp4_get_status(_stream(dev), ctypes.byref(bits))
+    return status, bits.value
+
+
+def quantize_from_host(x_host, pinned_out=None, **kw):
+    """End-to-end call for host data: copy a pinned host BF16 tensor to the device, quantize,
+    and copy every output back into pinned host tensors (all on the current stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = x_host.to(dev, non_blocking=True)
+    out = nvfp4_quantize(x, **kw)
+    if pinned_out is None:
+        pinned_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                      for k, v in out.items()}
+    for k, v in out.items():
+        pinned_out[k].copy_(v, non_blocking=True)
+    return pinned_out

@@ -1,0 +1,338 @@
+// C ABI of libnvfp4 (declared in include/nvfp4.h): argument checks, the per-device workspace,
+// TMA descriptors, and the launch sequence of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "nvfp4.h"
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+
+#define NVFP4_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kWorkspaceBytes = 16384;
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  uint32_t* workspace = nullptr;  // [0] status word
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+nvfp4_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    void* ws = nullptr;
+    if (cudaMalloc(&ws, kWorkspaceBytes) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaMemset(ws, 0, kWorkspaceBytes) != cudaSuccess) return NVFP4_ERR_CUDA;
+    st.workspace = static_cast<uint32_t*>(ws);
+    if (prepare_quantize_kernels() != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return NVFP4_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return NVFP4_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// TMA descriptor of a BF16 [rows][cols] row-major tensor, box {kTileN, kTileM}; reads outside
+// the tensor return zeros.
+nvfp4_status make_tensor_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTileN, (cuuint32_t)kTileM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status check_config(const nvfp4_config* cfg) {
+  if (cfg == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (cfg->reserved != 0) return NVFP4_ERR_INVALID_ARG;
+  if ((cfg->round_row != NVFP4_ROUND_RN && cfg->round_row != NVFP4_ROUND_SR) ||
+      (cfg->round_col != NVFP4_ROUND_RN && cfg->round_col != NVFP4_ROUND_SR))
+    return NVFP4_ERR_INVALID_ARG;
+  if (cfg->rht_sign_mask > 0xFFFFu) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
+// Writes {amax, S_dec} (amax = 0 when `amax` is null) into gscale[e][2] for e < n.
+__global__ void gscale_fill_kernel(const float* amax, float* gscale, int n) {
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    float a = amax ? amax[0] : 0.0f;
+    float enc, dec;
+    global_scale(a, enc, dec);
+    gscale[2 * e] = a;
+    gscale[2 * e + 1] = dec;
+  }
+}
+
+nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+int amax_grid(const DeviceState* st, int64_t work_items, int per_block) {
+  int64_t g = (work_items + per_block - 1) / per_block;
+  int64_t cap = (int64_t)st->sm_count * 8;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : (int)g;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+NVFP4_EXPORT const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_SHAPE: return "shape not a multiple of 16 where blocks need it";
+    case NVFP4_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+    case NVFP4_ERR_UNSUPPORTED: return "unsupported option combination";
+    case NVFP4_ERR_CUDA: return "CUDA error";
+    case NVFP4_ERR_DEVICE_STATUS: return "device flagged its input (bad grouped offsets)";
+    case NVFP4_ERR_TIMEOUT: return "a bounded device wait gave up";
+  }
+  return "unknown status";
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_amax(const void* x, int64_t M, int64_t N, const nvfp4_config* cfg,
+                                     float* amax_row, float* amax_col, void* stream) {
+  nvfp4_status st = check_config(cfg);
+  if (st != NVFP4_OK) return st;
+  if (M < 0 || N < 0 || (amax_row == nullptr && amax_col == nullptr)) return NVFP4_ERR_INVALID_ARG;
+  if (N % 16 != 0 || (cfg->rht_col && amax_col && M % 16 != 0)) return NVFP4_ERR_SHAPE;
+  if (M > INT32_MAX || N > INT32_MAX) return NVFP4_ERR_SHAPE;
+  if ((M * N > 0 && (x == nullptr || !aligned(x, 16))) || (amax_row && !aligned(amax_row, 4)) ||
+      (amax_col && !aligned(amax_col, 4)))
+    return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (amax_row && cudaMemsetAsync(amax_row, 0, 4, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (amax_col && cudaMemsetAsync(amax_col, 0, 4, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (M * N == 0) return NVFP4_OK;
+  if (cfg->rht_col && amax_col) {
+    AmaxArgs a{};
+    a.x = x; a.rows = M; a.cols = N; a.offsets = nullptr; a.segments = 1;
+    a.sign_mask = cfg->rht_sign_mask; a.amax_row = amax_row; a.amax_col = amax_col;
+    a.stride_row = 2; a.stride_col = 2; a.status = ds->workspace;
+    return cuda_status(launch_amax_blocks(true, a, amax_grid(ds, (M / 16) * (N / 4), 256), s));
+  }
+  return cuda_status(launch_amax_flat(x, M * N, amax_row, amax_col, amax_grid(ds, M * N / 8, 1024), s));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
+                                         const nvfp4_config* cfg, const float* amax_row,
+                                         const float* amax_col, uint8_t* row_codes,
+                                         uint8_t* row_scales, float* row_gscale,
+                                         uint8_t* col_codes, uint8_t* col_scales,
+                                         float* col_gscale, void* stream) {
+  nvfp4_status st = check_config(cfg);
+  if (st != NVFP4_OK) return st;
+  const bool two_d = cfg->block2d != 0;
+  const bool row = cfg->rowwise != 0;
+  const bool col = cfg->columnwise != 0;
+  const bool rht = cfg->rht_col != 0 && col;
+  if (!row && !col) return NVFP4_ERR_UNSUPPORTED;
+  if (two_d && (cfg->rht_col || cfg->round_row == NVFP4_ROUND_SR || cfg->round_col == NVFP4_ROUND_SR))
+    return NVFP4_ERR_UNSUPPORTED;
+  if (cfg->fused_amax) return NVFP4_ERR_UNSUPPORTED;
+  if (M < 0 || N < 0) return NVFP4_ERR_INVALID_ARG;
+  if (N % 16 != 0 || ((col || two_d) && M % 16 != 0)) return NVFP4_ERR_SHAPE;
+  if (M > INT32_MAX - kTileM || N > INT32_MAX - kTileN) return NVFP4_ERR_SHAPE;
+  const bool empty = M * N == 0;  // empty tensors: only the global scales are written
+  if (row && (row_gscale == nullptr || (!empty && (row_codes == nullptr || row_scales == nullptr))))
+    return NVFP4_ERR_INVALID_ARG;
+  if (col && (col_gscale == nullptr || (!empty && (col_codes == nullptr || col_scales == nullptr))))
+    return NVFP4_ERR_INVALID_ARG;
+  if ((!empty && (x == nullptr || !aligned(x, 16))) ||
+      (row && (!aligned(row_codes, 16) || !aligned(row_scales, 16) || !aligned(row_gscale, 4))) ||
+      (col && (!aligned(col_codes, 16) || !aligned(col_scales, 16) || !aligned(col_gscale, 4))) ||
+      (amax_row && !aligned(amax_row, 4)) || (amax_col && !aligned(amax_col, 4)))
+    return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (M * N == 0) {
+    if (row) gscale_fill_kernel<<<1, 32, 0, s>>>(amax_row, row_gscale, 1);
+    if (col) gscale_fill_kernel<<<1, 32, 0, s>>>(two_d ? amax_row : amax_col, col_gscale, 1);
+    return cuda_status(cudaGetLastError());
+  }
+
+  // amax pass (two-pass pipeline) for whatever the caller did not supply; the maxima land in
+  // the gscale outputs' amax slots, which the tile kernel reads.
+  const bool need_row_amax = (row || two_d) && amax_row == nullptr;
+  const bool need_col_amax = col && !two_d && amax_col == nullptr;
+  float* row_amax_slot = row ? row_gscale : col_gscale;  // 2D column-only keeps it in col_gscale
+  if (need_row_amax || need_col_amax) {
+    if (need_row_amax && cudaMemsetAsync(row_amax_slot, 0, 8, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (need_col_amax && cudaMemsetAsync(col_gscale, 0, 8, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (need_col_amax && rht) {
+      AmaxArgs a{};
+      a.x = x; a.rows = M; a.cols = N; a.offsets = nullptr; a.segments = 1;
+      a.sign_mask = cfg->rht_sign_mask;
+      a.amax_row = need_row_amax ? row_amax_slot : nullptr;
+      a.amax_col = col_gscale;
+      a.stride_row = 2; a.stride_col = 2; a.status = ds->workspace;
+      if (launch_amax_blocks(true, a, amax_grid(ds, (M / 16) * (N / 4), 256), s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    } else {
+      if (launch_amax_flat(x, M * N, need_row_amax ? row_amax_slot : nullptr,
+                           need_col_amax ? col_gscale : nullptr, amax_grid(ds, M * N / 8, 1024),
+                           s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    }
+  }
+
+  QuantArgs q;
+  std::memset(&q, 0, sizeof q);
+  if ((st = make_tensor_map(&q.tmap, x, M, N)) != NVFP4_OK) return st;
+  q.rows = M; q.cols = N; q.offsets = nullptr; q.segments = 1;
+  q.sr_row = cfg->round_row == NVFP4_ROUND_SR; q.sr_col = cfg->round_col == NVFP4_ROUND_SR;
+  q.sign_mask = cfg->rht_sign_mask; q.col_ld = M;
+  q.amax_row = amax_row ? amax_row : row_amax_slot;
+  q.amax_col = amax_col ? amax_col : col_gscale;
+  q.amax_row_stride = 2; q.amax_col_stride = 2;
+  q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
+  q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
+  q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
+  QuantVariant v;
+  if (two_d) v = row && col ? k2dRowCol : (row ? k2dRow : k2dCol);
+  else if (row && col) v = rht ? kRowColRht : kRowCol;
+  else if (row) v = kRow;
+  else v = rht ? kColRht : kCol;
+  const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
+  const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
+  return cuda_status(launch_quantize(v, q, grid, s));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
+                                                 const int32_t* offsets, int32_t E,
+                                                 int64_t col_capacity, const nvfp4_config* cfg,
+                                                 uint8_t* row_codes, uint8_t* row_scales,
+                                                 float* row_gscale, uint8_t* col_codes,
+                                                 uint8_t* col_scales, float* col_gscale,
+                                                 void* stream) {
+  nvfp4_status st = check_config(cfg);
+  if (st != NVFP4_OK) return st;
+  const bool row = cfg->rowwise != 0;
+  const bool col = cfg->columnwise != 0;
+  const bool rht = cfg->rht_col != 0 && col;
+  if (!row && !col) return NVFP4_ERR_UNSUPPORTED;
+  if (cfg->block2d || cfg->fused_amax) return NVFP4_ERR_UNSUPPORTED;
+  if (T < 0 || H < 0 || E < 1 || E > kMaxSegments || offsets == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (H % 16 != 0 || (col && (col_capacity < 0 || col_capacity % 16 != 0))) return NVFP4_ERR_SHAPE;
+  if (T > INT32_MAX - kTileM || H > INT32_MAX - kTileN || col_capacity > INT32_MAX)
+    return NVFP4_ERR_SHAPE;
+  const bool empty = T * H == 0;  // empty tensors: only the global scales are written
+  if (row && (row_gscale == nullptr || (!empty && (row_codes == nullptr || row_scales == nullptr))))
+    return NVFP4_ERR_INVALID_ARG;
+  if (col && (col_gscale == nullptr || (!empty && (col_codes == nullptr || col_scales == nullptr))))
+    return NVFP4_ERR_INVALID_ARG;
+  if ((!empty && (x == nullptr || !aligned(x, 16))) || !aligned(offsets, 4) ||
+      (row && (!aligned(row_codes, 16) || !aligned(row_scales, 16) || !aligned(row_gscale, 4))) ||
+      (col && (!aligned(col_codes, 16) || !aligned(col_scales, 16) || !aligned(col_gscale, 4))))
+    return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (T * H == 0) {
+    if (row) gscale_fill_kernel<<<1, 256, 0, s>>>(nullptr, row_gscale, E);
+    if (col) gscale_fill_kernel<<<1, 256, 0, s>>>(nullptr, col_gscale, E);
+    return cuda_status(cudaGetLastError());
+  }
+  // per-expert amax (and RHT amax) from one read, into the gscale outputs' amax slots
+  if (row && cudaMemsetAsync(row_gscale, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (col && cudaMemsetAsync(col_gscale, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  AmaxArgs a{};
+  a.x = x; a.rows = T; a.cols = H; a.offsets = offsets; a.segments = E;
+  a.sign_mask = cfg->rht_sign_mask;
+  a.amax_row = row ? row_gscale : nullptr;
+  a.amax_col = col ? col_gscale : nullptr;
+  a.stride_row = 2; a.stride_col = 2; a.status = ds->workspace;
+  if (launch_amax_blocks(rht, a, amax_grid(ds, (T / 16 + E) * (H / 4), 256), s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+
+  QuantArgs q;
+  std::memset(&q, 0, sizeof q);
+  if ((st = make_tensor_map(&q.tmap, x, T, H)) != NVFP4_OK) return st;
+  q.rows = T; q.cols = H; q.offsets = offsets; q.segments = E;
+  q.sr_row = cfg->round_row == NVFP4_ROUND_SR; q.sr_col = cfg->round_col == NVFP4_ROUND_SR;
+  q.sign_mask = cfg->rht_sign_mask; q.col_ld = col ? col_capacity : 0;
+  q.amax_row = row_gscale; q.amax_col = col_gscale;
+  q.amax_row_stride = 2; q.amax_col_stride = 2;
+  q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
+  q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
+  q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
+  QuantVariant v = (row && col) ? (rht ? kRowColRht : kRowCol) : (row ? kRow : (rht ? kColRht : kCol));
+  const int64_t tiles = ((T + kTileM - 1) / kTileM + E) * ((H + kTileN - 1) / kTileN);
+  const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
+  return cuda_status(launch_quantize(v, q, grid, s));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales,
+                                           const float* gscale, int64_t R, int64_t C, float* out,
+                                           void* stream) {
+  if (R < 0 || C < 0) return NVFP4_ERR_INVALID_ARG;
+  if (C % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (R * C == 0) return NVFP4_OK;
+  if (codes == nullptr || scales == nullptr || gscale == nullptr || out == nullptr)
+    return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(codes, 8) || !aligned(gscale, 4) || !aligned(out, 16)) return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  return cuda_status(launch_dequantize(codes, scales, gscale, R, C, out,
+                                       amax_grid(ds, R * (C / 16), 256),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status) {
+  if (device_status == nullptr) return NVFP4_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, ds->workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaMemset(ds->workspace, 0, 4) != cudaSuccess) return NVFP4_ERR_CUDA;
+  *device_status = v;
+  if (v & NVFP4_DEVICE_TIMEOUT) return NVFP4_ERR_TIMEOUT;
+  if (v) return NVFP4_ERR_DEVICE_STATUS;
+  return NVFP4_OK;
+}

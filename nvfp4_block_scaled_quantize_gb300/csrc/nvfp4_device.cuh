@@ -1,0 +1,323 @@
+// Device primitives of the NVFP4 quantizer (sm_103a): BF16 unpacking, block maxima, the
+// two-level scale arithmetic, E2M1 conversion with round-to-nearest-even or stochastic
+// rounding, Philox4x32-10, the 16-point Hadamard butterflies, and TMA/mbarrier plumbing.
+//
+// Page cited: "[nvfp4_training] Optimize CuteDSL kernels for NVFP4 training" (pytorch/ao pull
+// request #4798), by section. Every float operation is an explicit IEEE round-to-nearest
+// intrinsic or PTX instruction, so that no multiply-add is contracted and the results equal
+// the scalar binary32 statement of the method bit for bit.
+#pragma once
+
+#include <cfloat>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// ------------------------------------------------------------------------------------------
+// BF16 pairs. A 32-bit word holds two BF16 values: the lower-addressed (even) element in the
+// low half. BF16 is the upper half of a binary32, so widening is a shift or a mask
+// ([PR4798] "Optimization" item 6).
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Magnitudes of both halves (sign bits cleared). As unsigned 16-bit integers, BF16
+// magnitudes order exactly like the values they encode (finite inputs).
+__device__ __forceinline__ uint32_t abs2(uint32_t w) { return w & 0x7FFF7FFFu; }
+__device__ __forceinline__ uint32_t vmax2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+// Larger of the two magnitudes of a packed pair, as a float.
+__device__ __forceinline__ float pair_max(uint32_t m) {
+  return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+}
+__device__ __forceinline__ float mag_lo(uint32_t m) { return __uint_as_float(m << 16); }
+__device__ __forceinline__ float mag_hi(uint32_t m) { return __uint_as_float(m & 0xFFFF0000u); }
+
+// ------------------------------------------------------------------------------------------
+// Packed binary32 pairs (f32x2). One instruction handles both lanes of a 64-bit register
+// pair, each lane rounded to nearest-even exactly as the scalar instruction
+// ([PR4798] "Optimization" item 1: packed mul.f32x2).
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t d) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+  return make_float2(lo, hi);
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// A packed BF16 pair widened to a packed binary32 pair (low half -> low lane).
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) {
+  return f2_pack(bf16_lo(w), bf16_hi(w));
+}
+
+// ------------------------------------------------------------------------------------------
+// Scales
+// ------------------------------------------------------------------------------------------
+
+// Per-tensor global scale: S_enc = 2688 / amax (448 * 6), 1 when amax == 0, FLT_MAX when the
+// quotient overflows; S_dec = 1 / S_enc ([PR4798] "Fast math": the per-tensor
+// global_decode_scale).
+__device__ __forceinline__ void global_scale(float amax, float& s_enc, float& s_dec) {
+  float enc = (amax == 0.0f) ? 1.0f : __fdiv_rn(2688.0f, amax);
+  enc = fminf(enc, FLT_MAX);
+  s_enc = enc;
+  s_dec = __frcp_rn(enc);
+}
+
+// x / 6 correctly rounded, for the finite BF16 magnitudes a block amax can take: the product
+// by the rounded reciprocal of 6, corrected by one remainder step (Markstein's correction for
+// a divisor known in advance; see Brisebarre, Muller and Raina, "Accelerating correctly
+// rounded floating-point division when the divisor is known in advance", IEEE Trans.
+// Computers 53(8), 2004). Equal to IEEE division on all 32,640 finite BF16 magnitudes.
+__device__ __forceinline__ float div6(float x) {
+  const float c = 0.16666667163372039794921875f;  // binary32 nearest to 1/6
+  float q = __fmul_rn(x, c);
+  float r = __fmaf_rn(-q, 6.0f, x);
+  return __fmaf_rn(r, c, q);
+}
+
+// Two E4M3 block scales from two block maxima: s = E4M3_rn_satfinite((bamax / 6) * S_enc).
+// Returns the pair as a 16-bit word, `lo` in the low byte.
+__device__ __forceinline__ uint16_t block_scales2(float bamax_lo, float bamax_hi, float s_enc) {
+  float s_lo = __fmul_rn(div6(bamax_lo), s_enc);
+  float s_hi = __fmul_rn(div6(bamax_hi), s_enc);
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(s_hi), "f"(s_lo));
+  return d;
+}
+
+// E4M3 pair -> two floats (exact): .x from the low byte, .y from the high byte.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t s) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(s));
+  return make_float2(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))),
+                     __half2float(__ushort_as_half((unsigned short)(h2 >> 16))));
+}
+
+// Element multiplier r = 1 / (float(s) * S_dec), correctly rounded; 0 when the product is 0;
+// FLT_MAX when the reciprocal overflows ([PR4798] "Fast math": exact mode takes div_rn of
+// pvscale_fp8 * global_decode_scale).
+__device__ __forceinline__ float element_multiplier(float s, float s_dec) {
+  float p = __fmul_rn(s, s_dec);
+  float r = fminf(__frcp_rn(p), FLT_MAX);
+  return (p == 0.0f) ? 0.0f : r;
+}
+
+// ------------------------------------------------------------------------------------------
+// E2M1 conversion. Codes are packed two per byte with the even element in the low nibble.
+// ------------------------------------------------------------------------------------------
+
+// Eight scaled values -> eight codes, element 0 in bits 3:0 ([PR4798] "Optimization" item 1:
+// packed mul then cvt.rn.satfinite.e2m1x2.f32; that instruction puts its first operand in
+// the high nibble).
+__device__ __forceinline__ uint32_t e2m1x8_rn(uint64_t t01, uint64_t t23, uint64_t t45,
+                                              uint64_t t67) {
+  float2 a = f2_unpack(t01), b = f2_unpack(t23), c = f2_unpack(t45), d = f2_unpack(t67);
+  uint32_t out;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(out)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+  return out;
+}
+
+// Eight scaled values -> eight codes by stochastic rounding: elements 0..3 with random word
+// w0 and 4..7 with w1, each group one cvt.rs.satfinite.e2m1x4.f32 whose operands (a, b, e, f)
+// are elements (3, 2, 1, 0) so that element 0 lands in the low nibble ([PR4798]
+// "Optimization" item 3: the SR multiply and clamp fused into the convert).
+__device__ __forceinline__ uint32_t e2m1x8_rs(uint64_t t01, uint64_t t23, uint64_t t45,
+                                              uint64_t t67, uint32_t w0, uint32_t w1) {
+  float2 a = f2_unpack(t01), b = f2_unpack(t23), c = f2_unpack(t45), d = f2_unpack(t67);
+  uint16_t lo, hi;
+  asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+      : "=h"(lo) : "f"(b.y), "f"(b.x), "f"(a.y), "f"(a.x), "r"(w0));
+  asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+      : "=h"(hi) : "f"(d.y), "f"(d.x), "f"(c.y), "f"(c.x), "r"(w1));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Eight elements given as four packed BF16 pairs, times r, to codes. sr selects stochastic
+// rounding with words (w0, w1).
+__device__ __forceinline__ uint32_t quantize8(uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3,
+                                              float r, bool sr, uint32_t w0, uint32_t w1) {
+  uint64_t rr = f2_pack(r, r);
+  uint64_t t01 = f2_mul(f2_from_bf16x2(p0), rr);
+  uint64_t t23 = f2_mul(f2_from_bf16x2(p1), rr);
+  uint64_t t45 = f2_mul(f2_from_bf16x2(p2), rr);
+  uint64_t t67 = f2_mul(f2_from_bf16x2(p3), rr);
+  return sr ? e2m1x8_rs(t01, t23, t45, t67, w0, w1) : e2m1x8_rn(t01, t23, t45, t67);
+}
+
+// One column of eight elements taken from the low (hi = false) or high halves of eight
+// packed words, times r, to codes.
+__device__ __forceinline__ uint32_t quantize8_column(const uint32_t* w, bool hi, float r,
+                                                     bool sr, uint32_t w0, uint32_t w1) {
+  uint64_t rr = f2_pack(r, r);
+  uint64_t t[4];
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    float e0 = hi ? bf16_hi(w[2 * k]) : bf16_lo(w[2 * k]);
+    float e1 = hi ? bf16_hi(w[2 * k + 1]) : bf16_lo(w[2 * k + 1]);
+    t[k] = f2_mul(f2_pack(e0, e1), rr);
+  }
+  return sr ? e2m1x8_rs(t[0], t[1], t[2], t[3], w0, w1) : e2m1x8_rn(t[0], t[1], t[2], t[3]);
+}
+
+// ------------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11). One draw per 16-element block, all four words used ([PR4798] "Optimization" item 3;
+// the counter is the block's position, so results do not depend on the visit order).
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; round++) {
+    uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// The four words of block b: key (lo32 seed, hi32 seed), counter (lo32 b, hi32 b, tag, offset).
+__device__ __forceinline__ uint4 block_random(uint64_t seed, uint32_t offset, uint32_t tag,
+                                              uint64_t b) {
+  return philox4x32_10(make_uint4((uint32_t)b, (uint32_t)(b >> 32), tag, offset),
+                       (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// ------------------------------------------------------------------------------------------
+// 16-point random Hadamard transform of two adjacent columns at once ([PR4798] "Optimization"
+// items 2 and 5; "Fast math": an FP32 accumulator rounded through BF16 in exact mode).
+// w[i] holds rows i of the two columns as a BF16 pair. In place: w[i] <- bf16(0.25 * (H16 (d .
+// v))_i) for each column, H16 the natural-order Sylvester matrix computed by butterflies in
+// stages 1, 2, 4, 8 ((a, b) -> (a + b, a - b), a the lower index), d_i = -1 where bit i of
+// sign_mask is set.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void rht16_pair(uint32_t (&w)[16], uint32_t sign_mask) {
+  uint64_t x[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    uint32_t flip = ((sign_mask >> i) & 1u) ? 0x80008000u : 0u;
+    x[i] = f2_from_bf16x2(w[i] ^ flip);
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      if ((i & h) == 0) {
+        uint64_t a = x[i], b = x[i + h];
+        x[i] = f2_add(a, b);
+        x[i + h] = f2_sub(a, b);
+      }
+    }
+  }
+  const uint64_t quarter = f2_pack(0.25f, 0.25f);
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    float2 y = f2_unpack(f2_mul(x[i], quarter));
+    uint32_t packed;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(y.y), "f"(y.x));
+    w[i] = packed;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Shared memory, mbarriers and TMA
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns` nanoseconds of
+// global time. Returns false on a timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) return false;
+  }
+}
+
+// 2D tiled TMA load of the box at (x = innermost element index, y = row) into shared memory,
+// completing on `bar`. Out-of-range rows and columns are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tensor_map, int32_t x,
+                                            int32_t y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(tensor_map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* tensor_map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tensor_map) : "memory");
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,96 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry point the header
+declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from nvfp4_block_scaled_quantize_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "nvfp4.h")
+FAKE = 0x10000  # a 16-byte-aligned address never dereferenced: argument checks come first
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_library_agree(L):
+    declared = declared_functions()
+    assert declared == sorted(_lib.EXPORTED)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_config_struct_layout():
+    # int32 x 6, uint32 x 2, uint64, int32 x 2 -> 48 bytes, rng_seed at offset 32
+    assert ctypes.sizeof(_lib.Config) == 48
+    assert _lib.Config.rng_seed.offset == 32
+
+
+def test_status_strings(L):
+    for code in range(8):
+        assert L.nvfp4_status_string(code)
+
+
+def _cfg(**kw):
+    c = _lib.Config(rowwise=1)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _quant(L, M, N, cfg, x=FAKE, outs=FAKE):
+    p = ctypes.c_void_p
+    return L.nvfp4_quantize(p(x), M, N, ctypes.byref(cfg), None, None, p(outs), p(outs), p(outs),
+                            p(outs), p(outs), p(outs), None)
+
+
+def test_argument_checks_return_before_any_launch(L):
+    assert _quant(L, 32, 24, _cfg()) == 2                       # N % 16
+    assert _quant(L, 24, 32, _cfg(columnwise=1)) == 2           # M % 16 with columnwise
+    assert _quant(L, 24, 32, _cfg(rowwise=1, block2d=1)) == 2   # 2D needs both
+    assert _quant(L, 32, 32, _cfg(rowwise=0)) == 4              # nothing selected
+    assert _quant(L, 32, 32, _cfg(block2d=1, rht_col=1, columnwise=1)) == 4
+    assert _quant(L, 32, 32, _cfg(block2d=1, round_row=1)) == 4
+    assert _quant(L, 32, 32, _cfg(round_row=2)) == 1
+    assert _quant(L, 32, 32, _cfg(reserved=1)) == 1
+    assert _quant(L, 32, 32, _cfg(rht_sign_mask=1 << 16)) == 1
+    assert _quant(L, -1, 32, _cfg()) == 1
+    assert _quant(L, 32, 32, _cfg(), x=FAKE + 8) == 3           # misaligned input
+    assert _quant(L, 32, 32, _cfg(), outs=FAKE + 4) == 3        # misaligned outputs
+    p = ctypes.c_void_p
+    assert L.nvfp4_quantize(p(FAKE), 32, 32, ctypes.byref(_cfg()), None, None, None, None, None,
+                            None, None, None, None) == 1       # missing rowwise outputs
+    assert L.nvfp4_quantize(p(FAKE), 32, 32, None, None, None, p(FAKE), p(FAKE), p(FAKE), None,
+                            None, None, None) == 1             # missing config
+
+
+def test_grouped_and_dequant_argument_checks(L):
+    p = ctypes.c_void_p
+    cfg = _cfg(columnwise=1)
+
+    def grouped(T, H, offs, E, cap, c=cfg):
+        return L.nvfp4_quantize_grouped(p(FAKE), T, H, offs, E, cap, ctypes.byref(c), p(FAKE),
+                                        p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None)
+    assert grouped(64, 32, p(FAKE), 0, 64) == 1     # no experts
+    assert grouped(64, 32, p(FAKE), 257, 64) == 1   # too many experts
+    assert grouped(64, 32, None, 2, 64) == 1        # no offsets
+    assert grouped(64, 24, p(FAKE), 2, 64) == 2     # H % 16
+    assert grouped(64, 32, p(FAKE), 2, 40) == 2     # capacity % 16
+    assert grouped(64, 32, p(FAKE + 2), 2, 64) == 3
+    assert grouped(64, 32, p(FAKE), 2, 64, _cfg(columnwise=1, block2d=1)) == 4
+    assert L.nvfp4_dequantize(p(FAKE), p(FAKE), p(FAKE), 4, 24, p(FAKE), None) == 2
+    assert L.nvfp4_dequantize(p(FAKE), p(FAKE), p(FAKE), 4, 32, p(FAKE + 4), None) == 3
+    assert L.nvfp4_amax(p(FAKE), 16, 32, ctypes.byref(cfg), None, None, None) == 1
+    assert L.nvfp4_get_status(None, None) == 1
