@@ -14,8 +14,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libnvfp4.so")
-SOURCES = ["quantize_tiles.cu", "amax_dequant.cu", "nvfp4_api.cu"]
-HEADERS = ["nvfp4_device.cuh", "nvfp4_internal.h"]
+SOURCES = ["quantize_row.cu", "quantize_col.cu", "quantize_rowcol.cu", "quantize_rowcol_rht.cu",
+           "quantize_2d.cu", "amax_dequant.cu", "nvfp4_api.cu"]
+HEADERS = ["nvfp4_device.cuh", "nvfp4_internal.h", "quantize_kernel.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

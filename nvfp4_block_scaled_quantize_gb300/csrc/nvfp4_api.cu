@@ -99,6 +99,28 @@ __global__ void gscale_fill_kernel(const float* amax, float* gscale, int n) {
   }
 }
 
+}  // namespace
+
+cudaError_t launch_quantize(const QuantMode& m, const QuantArgs& args, int grid, cudaStream_t s) {
+  if (m.two_d) return launch_quantize_2d(m, args, grid, s);
+  if (m.row && m.col) return m.rht ? launch_quantize_rowcol_rht(m, args, grid, s)
+                                   : launch_quantize_rowcol(m, args, grid, s);
+  if (m.row) return launch_quantize_row(m, args, grid, s);
+  return launch_quantize_col(m, args, grid, s);
+}
+
+cudaError_t prepare_quantize_kernels() {
+  cudaError_t e = cudaSuccess, r;
+  if ((r = prepare_quantize_row()) != cudaSuccess) e = r;
+  if ((r = prepare_quantize_col()) != cudaSuccess) e = r;
+  if ((r = prepare_quantize_rowcol()) != cudaSuccess) e = r;
+  if ((r = prepare_quantize_rowcol_rht()) != cudaSuccess) e = r;
+  if ((r = prepare_quantize_2d()) != cudaSuccess) e = r;
+  return e;
+}
+
+namespace {
+
 nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
 int amax_grid(const DeviceState* st, int64_t work_items, int per_block) {
@@ -221,7 +243,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   std::memset(&q, 0, sizeof q);
   if ((st = make_tensor_map(&q.tmap, x, M, N)) != NVFP4_OK) return st;
   q.rows = M; q.cols = N; q.offsets = nullptr; q.segments = 1;
-  q.sr_row = cfg->round_row == NVFP4_ROUND_SR; q.sr_col = cfg->round_col == NVFP4_ROUND_SR;
+  const int sr_row = cfg->round_row == NVFP4_ROUND_SR, sr_col = cfg->round_col == NVFP4_ROUND_SR;
   q.sign_mask = cfg->rht_sign_mask; q.col_ld = M;
   q.amax_row = amax_row ? amax_row : row_amax_slot;
   q.amax_col = amax_col ? amax_col : col_gscale;
@@ -229,14 +251,10 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
   q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
-  QuantVariant v;
-  if (two_d) v = row && col ? k2dRowCol : (row ? k2dRow : k2dCol);
-  else if (row && col) v = rht ? kRowColRht : kRowCol;
-  else if (row) v = kRow;
-  else v = rht ? kColRht : kCol;
+  const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0};
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
-  return cuda_status(launch_quantize(v, q, grid, s));
+  return cuda_status(launch_quantize(mode, q, grid, s));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
@@ -291,17 +309,17 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   std::memset(&q, 0, sizeof q);
   if ((st = make_tensor_map(&q.tmap, x, T, H)) != NVFP4_OK) return st;
   q.rows = T; q.cols = H; q.offsets = offsets; q.segments = E;
-  q.sr_row = cfg->round_row == NVFP4_ROUND_SR; q.sr_col = cfg->round_col == NVFP4_ROUND_SR;
+  const int sr_row = cfg->round_row == NVFP4_ROUND_SR, sr_col = cfg->round_col == NVFP4_ROUND_SR;
   q.sign_mask = cfg->rht_sign_mask; q.col_ld = col ? col_capacity : 0;
   q.amax_row = row_gscale; q.amax_col = col_gscale;
   q.amax_row_stride = 2; q.amax_col_stride = 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
   q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
-  QuantVariant v = (row && col) ? (rht ? kRowColRht : kRowCol) : (row ? kRow : (rht ? kColRht : kCol));
+  const QuantMode mode{row, col, rht, false, sr_row != 0, sr_col != 0};
   const int64_t tiles = ((T + kTileM - 1) / kTileM + E) * ((H + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
-  return cuda_status(launch_quantize(v, q, grid, s));
+  return cuda_status(launch_quantize(mode, q, grid, s));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales,

@@ -64,6 +64,18 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// Per 16-bit half: max(|a|, |b|) of BF16 values, exact; the sign bits of the result are
+// meaningless (max.xorsign.abs) and are cleared once at the end of a chain.
+__device__ __forceinline__ uint32_t hmax_abs2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 // A packed BF16 pair widened to a packed binary32 pair (low half -> low lane).
 __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) {
   return f2_pack(bf16_lo(w), bf16_hi(w));
@@ -95,13 +107,17 @@ __device__ __forceinline__ float div6(float x) {
   return __fmaf_rn(r, c, q);
 }
 
-// Two E4M3 block scales from two block maxima: s = E4M3_rn_satfinite((bamax / 6) * S_enc).
-// Returns the pair as a 16-bit word, `lo` in the low byte.
+// Two E4M3 block scales from two block maxima: s = E4M3_rn_satfinite((bamax / 6) * S_enc),
+// with x / 6 as in div6 (packed). Returns the pair as a 16-bit word, `lo` in the low byte.
 __device__ __forceinline__ uint16_t block_scales2(float bamax_lo, float bamax_hi, float s_enc) {
-  float s_lo = __fmul_rn(div6(bamax_lo), s_enc);
-  float s_hi = __fmul_rn(div6(bamax_hi), s_enc);
+  const uint64_t c = f2_pack(0.16666667163372039794921875f, 0.16666667163372039794921875f);
+  const uint64_t neg6 = f2_pack(-6.0f, -6.0f);
+  const uint64_t x = f2_pack(bamax_lo, bamax_hi);
+  const uint64_t q = f2_mul(x, c);
+  const uint64_t r = f2_fma(q, neg6, x);
+  const float2 s = f2_unpack(f2_mul(f2_fma(r, c, q), f2_pack(s_enc, s_enc)));
   uint16_t d;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(s_hi), "f"(s_lo));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(s.y), "f"(s.x));
   return d;
 }
 
@@ -184,6 +200,25 @@ __device__ __forceinline__ uint32_t quantize8_column(const uint32_t* w, bool hi,
     t[k] = f2_mul(f2_pack(e0, e1), rr);
   }
   return sr ? e2m1x8_rs(t[0], t[1], t[2], t[3], w0, w1) : e2m1x8_rn(t[0], t[1], t[2], t[3]);
+}
+
+// Four scaled values -> four codes in 16 bits, element 0 in bits 3:0: round-to-nearest-even
+// (two cvt.rn.satfinite.e2m1x2.f32) or, with SR, one cvt.rs.satfinite.e2m1x4.f32 taking
+// random word w (operands a, b, e, f = elements 3, 2, 1, 0).
+template <bool SR>
+__device__ __forceinline__ uint32_t e2m1x4(float t0, float t1, float t2, float t3, uint32_t w) {
+  uint16_t d;
+  if (SR) {
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(d) : "f"(t3), "f"(t2), "f"(t1), "f"(t0), "r"(w));
+  } else {
+    asm("{\n\t.reg .b8 q0, q1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "mov.b16 %0, {q0, q1};\n\t}"
+        : "=h"(d) : "f"(t0), "f"(t1), "f"(t2), "f"(t3));
+  }
+  return (uint32_t)d;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -289,6 +324,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return done != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Barrier over `count` threads (a multiple of 32) on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 // Wait for phase `parity` of `bar` to complete, giving up after `limit_ns` nanoseconds of
 // global time. Returns false on a timeout.

@@ -7,41 +7,46 @@
 
 namespace nvfp4 {
 
-// Tile of the quantize kernels: kTileM rows x kTileN BF16 columns, one TMA box per stage.
+// ---- the quantize kernel's geometry ----
+// A tile is kTileM rows x kTileN BF16 columns (one TMA box, one pipeline stage). A warp owns
+// one 16-row slab of a tile; four warps (a group) share a tile; kGroups groups work on
+// different tiles at once, and each group refills the stage it has just drained, so kStages
+// tiles stay in flight.
 constexpr int kTileM = 64;
 constexpr int kTileN = 256;
 constexpr int kStages = 4;
-constexpr int kQuantThreads = 512;
+constexpr int kGroups = 3;
+constexpr int kWarpsPerGroup = kTileM / 16;
+constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
+constexpr int kQuantThreads = 32 * kConsumerWarps;
 constexpr int kStageBytes = kTileM * kTileN * 2;
 constexpr int kMaxSegments = 256;
+constexpr int kTableEntries = 128;  // E4M3 codes of non-negative scales
 
-// Shared-memory layout of the quantize kernels (byte offsets).
-constexpr int kColCodeStage = (kTileM / 16) * kTileN * 8;    // [4 row-blocks][256 cols][8 B]
-constexpr int kColScaleStage = (kTileM / 16) * kTileN;       // [4][256]
-constexpr int kRowScaleStage = kTileM * (kTileN / 16);       // [64 rows][16]
+// Shared-memory layout of the quantize kernel (byte offsets).
+constexpr int kColCodeStage = kWarpsPerGroup * kTileN * 8;   // [4 slabs][128 chunks][16 B]
+constexpr int kColScaleStage = kWarpsPerGroup * kTileN;      // [4 slabs][256 B]
 constexpr int kSmemStages = 0;
 constexpr int kSmemColCodes = kSmemStages + kStages * kStageBytes;
-constexpr int kSmemColScales = kSmemColCodes + 2 * kColCodeStage;
-constexpr int kSmemRowScales = kSmemColScales + 2 * kColScaleStage;
-constexpr int kSmemTileR = kSmemRowScales + 2 * kRowScaleStage;       // float [4][16]
-constexpr int kSmemTileS = kSmemTileR + 4 * 16 * 4;                   // uint8 [4][16]
-constexpr int kSmemSegStart = kSmemTileS + 64;                        // int32 [kMaxSegments]
+constexpr int kSmemColScales = kSmemColCodes + kGroups * kColCodeStage;
+constexpr int kSmemTables = kSmemColScales + kGroups * kColScaleStage;  // per warp: 2 x 128 f32
+constexpr int kSmemSegStart = kSmemTables + kConsumerWarps * 2 * kTableEntries * 4;
 constexpr int kSmemSegEnd = kSmemSegStart + 4 * kMaxSegments;
 constexpr int kSmemSegCol0 = kSmemSegEnd + 4 * kMaxSegments;
-constexpr int kSmemSegTile0 = kSmemSegCol0 + 4 * kMaxSegments;        // int32 [kMaxSegments + 1]
-constexpr int kSmemSegScale = kSmemSegTile0 + 4 * (kMaxSegments + 4); // float4 [kMaxSegments]
-constexpr int kSmemBars = kSmemSegScale + 16 * kMaxSegments;          // uint64 [kStages]
+constexpr int kSmemSegTile0 = kSmemSegCol0 + 4 * kMaxSegments;        // [kMaxSegments + 4]
+constexpr int kSmemCoords = kSmemSegTile0 + 4 * (kMaxSegments + 4);   // [kStages][8] int32
+constexpr int kSmemBars = kSmemCoords + 32 * kStages;                 // full[kStages]
 constexpr int kSmemFlags = kSmemBars + 8 * kStages;                   // int32 [4]
-constexpr int kQuantSmemBytes = kSmemFlags + 16;
+constexpr int kSmemLastIssued = kSmemFlags + 16;                      // int32 [kStages]
+constexpr int kQuantSmemBytes = kSmemLastIssued + 4 * kStages;
 
-// Arguments of the tile kernel: one BF16 tensor split into row segments (one segment for a
-// plain tensor, one per expert for the grouped case).
+// Arguments of the quantize kernel: one BF16 tensor split into row segments (one segment for
+// a plain tensor, one per expert for the grouped case).
 struct QuantArgs {
   CUtensorMap tmap;                 // x as BF16 [rows][cols], box {kTileN, kTileM}
   int64_t rows, cols;
   const int32_t* offsets;           // cumulative segment ends, or nullptr: one segment
   int32_t segments;
-  int32_t sr_row, sr_col;
   uint32_t sign_mask;
   int64_t col_ld;                   // columnwise output row length (elements)
   const float* amax_row;            // amax of segment e at amax_row[e * amax_row_stride]
@@ -58,9 +63,9 @@ struct QuantArgs {
   uint32_t* status;
 };
 
-// Kernel variants of the tile kernel.
-enum QuantVariant : int {
-  kRow = 0, kCol, kColRht, kRowCol, kRowColRht, k2dRow, k2dCol, k2dRowCol, kNumQuantVariants
+// What one quantize launch produces.
+struct QuantMode {
+  bool row, col, rht, two_d, sr_row, sr_col;
 };
 
 // Arguments of the amax kernels.
@@ -76,12 +81,25 @@ struct AmaxArgs {
   uint32_t* status;
 };
 
-cudaError_t launch_quantize(QuantVariant v, const QuantArgs& args, int grid, cudaStream_t s);
+cudaError_t launch_quantize(const QuantMode& m, const QuantArgs& args, int grid, cudaStream_t s);
+cudaError_t prepare_quantize_kernels();
+// per-translation-unit halves of the above
+cudaError_t launch_quantize_row(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_quantize_col(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_quantize_rowcol(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_quantize_rowcol_rht(const QuantMode& m, const QuantArgs& a, int grid,
+                                       cudaStream_t s);
+cudaError_t launch_quantize_2d(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
+cudaError_t prepare_quantize_row();
+cudaError_t prepare_quantize_col();
+cudaError_t prepare_quantize_rowcol();
+cudaError_t prepare_quantize_rowcol_rht();
+cudaError_t prepare_quantize_2d();
+
 cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float* out1, int grid,
                              cudaStream_t s);
 cudaError_t launch_amax_blocks(bool rht, const AmaxArgs& args, int grid, cudaStream_t s);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
                               int64_t R, int64_t C, float* out, int grid, cudaStream_t s);
-cudaError_t prepare_quantize_kernels();
 
 }  // namespace nvfp4

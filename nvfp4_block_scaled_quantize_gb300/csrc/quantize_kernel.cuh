@@ -1,0 +1,535 @@
+// The quantize kernel: rowwise, columnwise (optionally after the 16-point RHT, with RTNE or
+// stochastic rounding) and 16x16 2D NVFP4 quantization of BF16 tensors from ONE read of the
+// input, for plain tensors and for grouped (MoE) tensors split into row segments.
+//
+// Page cited: "[nvfp4_training] Optimize CuteDSL kernels for NVFP4 training" (pytorch/ao pull
+// request #4798). Its "linear fused" / "grouped fused" row+col kernels and its 2D weight
+// kernel are the prior art; this is a design for sm_103a:
+//   * one persistent CTA per SM keeps kStages 64 x 256 BF16 tiles in flight with TMA
+//     (cp.async.bulk.tensor) completing on mbarriers; kGroups groups of four warps each take a
+//     whole tile, one warp per 16-row slab, and refill the stage as soon as the four slabs sit
+//     in registers (12 warps: three per SM sub-partition, so up to 168 registers each);
+//   * each lane holds a 16-row x 8-column piece of its slab, so every element is widened
+//     from BF16 once and feeds both orientations: a rowwise 1x16 block is a lane pair
+//     ("Optimization" item 7: a warp covers several tokens x hidden blocks), a columnwise block
+//     is one lane's column (thread-local maximum, RHT butterflies and conversion);
+//   * scale reciprocals come from a per-warp 128-entry table indexed by the E4M3 code, built
+//     once per segment with the exact (div_rn) reciprocal ("Fast math");
+//   * columnwise codes/scales of the four slabs are staged in shared memory (XOR-swizzled,
+//     conflict-free) and leave as whole 32-byte column runs ("Optimization" item 5);
+//   * stochastic rounding uses one Philox4x32-10 draw per 16-element block, all four words
+//     consumed by cvt.rs.satfinite.e2m1x4 ("Optimization" item 3).
+// Every wait on an mbarrier gives up after a time limit; the kernel then records
+// NVFP4_DEVICE_TIMEOUT and leaves after the loads it issued have landed (bounded too).
+#pragma once
+
+#include "nvfp4_device.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+namespace qk {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: no TMA load takes this long
+
+struct Coord {
+  int32_t row0;    // first row of the tile in x
+  int32_t nrows;   // rows of the tile inside its segment (<= kTileM)
+  int32_t n0;      // first column
+  int32_t colpos;  // first column of the tile in the columnwise outputs
+  int32_t seg;
+  int32_t tile;    // the tile these coordinates belong to (checked by the consumers)
+  int32_t pad1, pad2;
+};
+
+// XOR swizzle of 16-byte chunks inside each 128-byte row of the columnwise code staging.
+__device__ __forceinline__ int swz(int chunk) { return (chunk & ~7) | ((chunk ^ (chunk >> 3)) & 7); }
+
+__device__ __forceinline__ uint32_t comp(const uint4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+// Packed magnitude of the two halves, merged across two rows: returns (max row a, max row b)
+// as a pair of 16-bit magnitudes, each the max over the four words of its row.
+__device__ __forceinline__ uint32_t row_pair_max(const uint4& a, const uint4& b) {
+  const uint32_t ma = hmax_abs2(hmax_abs2(a.x, a.y), hmax_abs2(a.z, a.w));
+  const uint32_t mb = hmax_abs2(hmax_abs2(b.x, b.y), hmax_abs2(b.z, b.w));
+  return hmax_abs2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632)) & 0x7FFF7FFFu;
+}
+
+// max |w| over 16 packed BF16 pairs, per half, as a balanced tree; sign bits cleared.
+__device__ __forceinline__ uint32_t tree_max16(const uint32_t (&w)[16]) {
+  uint32_t a[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) a[i] = hmax_abs2(w[2 * i], w[2 * i + 1]);
+  const uint32_t b0 = hmax_abs2(a[0], a[1]), b1 = hmax_abs2(a[2], a[3]);
+  const uint32_t b2 = hmax_abs2(a[4], a[5]), b3 = hmax_abs2(a[6], a[7]);
+  return hmax_abs2(hmax_abs2(b0, b1), hmax_abs2(b2, b3)) & 0x7FFF7FFFu;
+}
+
+// Eight scaled values -> eight codes in 32 bits, element 0 in bits 3:0. RTNE: four
+// cvt.rn.satfinite.e2m1x2.f32 (first operand -> high nibble); SR: two
+// cvt.rs.satfinite.e2m1x4.f32 with random words w0 (elements 0..3) and w1 (4..7), operands
+// a, b, e, f = elements 3, 2, 1, 0 of each group.
+template <bool SR>
+__device__ __forceinline__ uint32_t e2m1x8(float t0, float t1, float t2, float t3, float t4,
+                                           float t5, float t6, float t7, uint32_t w0,
+                                           uint32_t w1) {
+  uint32_t d;
+  if (SR) {
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h0, {%4, %3, %2, %1}, %9;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 h1, {%8, %7, %6, %5}, %10;\n\t"
+        "mov.b32 %0, {h0, h1};\n\t}"
+        : "=r"(d)
+        : "f"(t0), "f"(t1), "f"(t2), "f"(t3), "f"(t4), "f"(t5), "f"(t6), "f"(t7), "r"(w0),
+          "r"(w1));
+  } else {
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+        : "=r"(d)
+        : "f"(t0), "f"(t1), "f"(t2), "f"(t3), "f"(t4), "f"(t5), "f"(t6), "f"(t7));
+  }
+  return d;
+}
+
+// Bounded wait until stage s has been given tile i (its monotonic last-issued index).
+__device__ __forceinline__ bool wait_issued(volatile int32_t* last_issued, int s, int i) {
+  if (last_issued[s] >= i) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (last_issued[s] < i) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > kWaitLimitNs) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
+__global__ void __launch_bounds__(kQuantThreads, 1)
+    quantize_tiles_kernel(const __grid_constant__ QuantArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+
+  int32_t* seg_start = reinterpret_cast<int32_t*>(smem + kSmemSegStart);
+  int32_t* seg_end = reinterpret_cast<int32_t*>(smem + kSmemSegEnd);
+  int32_t* seg_col0 = reinterpret_cast<int32_t*>(smem + kSmemSegCol0);
+  int32_t* seg_tile0 = reinterpret_cast<int32_t*>(smem + kSmemSegTile0);
+  Coord* coords = reinterpret_cast<Coord*>(smem + kSmemCoords);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBars);
+  volatile int32_t* flags = reinterpret_cast<volatile int32_t*>(smem + kSmemFlags);
+  volatile int32_t* last_issued = reinterpret_cast<volatile int32_t*>(smem + kSmemLastIssued);
+
+  const int E = a.segments;
+  const int tiles_n = (int)((a.cols + kTileN - 1) / kTileN);
+  const int64_t N = a.cols;
+
+  // ---- segment table: starts, ends, padded column starts, tile prefix sums ----
+  if (tid < 4) flags[tid] = 0;
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int32_t start = (a.offsets == nullptr || e == 0) ? 0 : a.offsets[e - 1];
+    const int32_t end = (a.offsets == nullptr) ? (int32_t)a.rows : a.offsets[e];
+    if (start < 0 || end < start || (int64_t)end > a.rows) flags[3] = 1;
+    seg_start[e] = start;
+    seg_end[e] = end;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int32_t tile_base = 0, col_base = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const int e = c0 + lane;
+      const int32_t n = (e < E && !flags[3]) ? seg_end[e] - seg_start[e] : 0;
+      const int32_t t0 = ((n + kTileM - 1) / kTileM) * tiles_n;
+      const int32_t p0 = ((n + 15) / 16) * 16;
+      int32_t t = t0, p = p0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int32_t tu = __shfl_up_sync(0xFFFFFFFFu, t, d);
+        const int32_t pu = __shfl_up_sync(0xFFFFFFFFu, p, d);
+        if (lane >= d) { t += tu; p += pu; }
+      }
+      if (e < E) {
+        seg_tile0[e] = tile_base + t - t0;
+        seg_col0[e] = col_base + p - p0;
+      }
+      tile_base += __shfl_sync(0xFFFFFFFFu, t, 31);
+      col_base += __shfl_sync(0xFFFFFFFFu, p, 31);
+    }
+    if (lane == 0) {
+      seg_tile0[E] = tile_base;
+      if (COL && (int64_t)col_base > a.col_ld) flags[3] = 1;
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&full[s], 1);
+      last_issued[s] = -1;
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (flags[3]) {
+    if (blockIdx.x == 0 && tid == 0) atomicOr(a.status, 1u);  // NVFP4_DEVICE_BAD_OFFSETS
+    return;
+  }
+  if (blockIdx.x == 0) {  // global scales {amax, S_dec} of every segment
+    for (int e = tid; e < E; e += blockDim.x) {
+      float enc, dec;
+      if (ROW || TWO_D) {
+        const float amax = a.amax_row[(int64_t)e * a.amax_row_stride];
+        global_scale(amax, enc, dec);
+        if (ROW) { a.row_gscale[2 * e] = amax; a.row_gscale[2 * e + 1] = dec; }
+        if (TWO_D && COL) { a.col_gscale[2 * e] = amax; a.col_gscale[2 * e + 1] = dec; }
+      }
+      if (COL && !TWO_D) {
+        const float amax = a.amax_col[(int64_t)e * a.amax_col_stride];
+        global_scale(amax, enc, dec);
+        a.col_gscale[2 * e] = amax;
+        a.col_gscale[2 * e + 1] = dec;
+      }
+    }
+  }
+  const int total = seg_tile0[E];
+  const int stride = gridDim.x;
+
+  // Load tile (local index) i of this CTA into stage i % kStages.
+  auto issue = [&](int i) {
+    const int tile = blockIdx.x + i * stride;
+    const int s = i % kStages;
+    int lo = 0, hi = E;  // segment: largest e with seg_tile0[e] <= tile
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (seg_tile0[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int local = tile - seg_tile0[lo];
+    const int mt = local / tiles_n;
+    Coord c;
+    c.n0 = (local - mt * tiles_n) * kTileN;
+    c.row0 = seg_start[lo] + mt * kTileM;
+    c.nrows = min(kTileM, seg_end[lo] - c.row0);
+    c.colpos = seg_col0[lo] + mt * kTileM;
+    c.seg = lo;
+    c.tile = tile;
+    c.pad1 = c.pad2 = 0;
+    coords[s] = c;
+    __threadfence_block();
+    last_issued[s] = i;  // stage s now serves tile i: its next mbarrier phase is tile i's
+    mbar_expect_tx(&full[s], kStageBytes);
+    tma_load_2d(smem + kSmemStages + s * kStageBytes, &a.tmap, c.n0, c.row0, &full[s]);
+  };
+  if (tid == 0) {
+    prefetch_tensormap(&a.tmap);
+    for (int i = 0; i < kStages && blockIdx.x + i * stride < total; i++) issue(i);
+  }
+
+  // =========================================================================================
+  // Groups of four warps, one tile at a time.
+  // =========================================================================================
+  const int g = warp / kWarpsPerGroup;   // group
+  const int rb = warp % kWarpsPerGroup;  // slab of the tile (rows 16 rb .. 16 rb + 15)
+  const int gt = tid - g * 32 * kWarpsPerGroup;  // thread index inside the group
+  const bool odd = (lane & 1) != 0;
+  const int kb = lane >> 1;              // rowwise block of the tile row (lane pair)
+  float* tab_row = reinterpret_cast<float*>(smem + kSmemTables) + warp * 2 * kTableEntries;
+  float* tab_col = tab_row + kTableEntries;
+  uint8_t* cc_stage = smem + kSmemColCodes + g * kColCodeStage;
+  uint8_t* cs_stage = smem + kSmemColScales + g * kColScaleStage;
+  const int64_t row_nb = N / 16;
+  const int64_t col_nb = a.col_ld / 16;
+  int cur_seg = -1;
+  float s_enc_r = 1.0f, s_enc_c = 1.0f;
+
+  for (int i = g;; i += kGroups) {
+    const int tile = blockIdx.x + i * stride;
+    if (tile >= total) break;
+    const int s = i % kStages;
+    // Three groups share four stages, so a group can reach tile i before the group that
+    // drains the stage's previous tile has issued it. Wait until tile i is the stage's
+    // current load; only then does the phase parity name tile i's phase unambiguously.
+    bool arrived = wait_issued(last_issued, s, i);
+    arrived = arrived && mbar_wait_bounded(&full[s], (uint32_t)(i / kStages) & 1u, kWaitLimitNs);
+    const Coord c = coords[s];
+    if (!arrived || c.tile != tile) {
+      // the data never arrived (or the stage holds another tile): record it; the loads below
+      // read stale shared memory and the group leaves at its next barrier without storing
+      flags[g] = 1;
+      if (lane == 0) atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
+    }
+    const int slab_rows = min(16, c.nrows - 16 * rb);
+    uint4 v[16];
+    if (slab_rows > 0) {
+      const uint32_t src = smem_u32(smem + kSmemStages + s * kStageBytes) +
+                           (16 * rb) * (kTileN * 2) + lane * 16;
+#pragma unroll
+      for (int r = 0; r < 16; r++) v[r] = lds128(src + r * (kTileN * 2));
+      if (slab_rows < 16) {  // rows past the segment's end are zero padding
+#pragma unroll
+        for (int r = 0; r < 16; r++)
+          if (r >= slab_rows) v[r] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    // All four slabs are in registers: the stage can be refilled, the group's staging is free
+    // (the previous tile was written out), and the group's abort flag is settled.
+    named_bar_sync(1 + g, 32 * kWarpsPerGroup);
+    if (flags[g]) break;
+    if (gt == 0 && blockIdx.x + (i + kStages) * stride < total) {
+      fence_proxy_async();
+      issue(i + kStages);
+    }
+
+    if (c.seg != cur_seg) {  // reciprocal tables of this segment's global scales
+      __syncwarp();
+      float dec_r = 1.0f, dec_c = 1.0f;
+      if (ROW || TWO_D) global_scale(a.amax_row[(int64_t)c.seg * a.amax_row_stride], s_enc_r, dec_r);
+      if (COL && !TWO_D) global_scale(a.amax_col[(int64_t)c.seg * a.amax_col_stride], s_enc_c, dec_c);
+      if (TWO_D) { s_enc_c = s_enc_r; dec_c = dec_r; }
+      for (int idx = lane; idx < kTableEntries; idx += 32) {
+        const float sv = e4m3x2_to_float2((uint16_t)idx).x;
+        tab_row[idx] = element_multiplier(sv, dec_r);
+        tab_col[idx] = element_multiplier(sv, dec_c);
+      }
+      __syncwarp();
+      cur_seg = c.seg;
+    }
+
+    const bool lane_cols = (int64_t)c.n0 + lane * 8 < N;  // all 8 of the lane's columns exist
+    // every row of the slab and every column of the tile exist (uniform across the warp)
+    const bool full_slab = slab_rows == 16 && (int64_t)c.n0 + kTileN <= N;
+    const int64_t row_g0 = (int64_t)c.row0 + 16 * rb;
+    if (slab_rows > 0) {
+      // ---------------- 2D: one scale per 16x16 tile (the lane pair's 16 columns) ----------------
+      float tile_r = 0.0f;
+      uint32_t tile_s = 0u;
+      if (TWO_D) {
+        uint32_t cm[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          uint32_t w[16];
+#pragma unroll
+          for (int r = 0; r < 16; r++) w[r] = comp(v[r], k);
+          cm[k] = tree_max16(w);
+        }
+        const uint32_t m = vmax2(vmax2(cm[0], cm[1]), vmax2(cm[2], cm[3]));
+        uint32_t tm = max(m & 0xFFFFu, m >> 16);
+        tm = max(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 1));
+        tile_s = block_scales2(__uint_as_float(tm << 16), 0.0f, s_enc_r) & 0xFFu;
+        tile_r = tab_row[tile_s];
+      }
+
+      // ---------------- rowwise: 1x16 blocks, a lane pair per block ----------------
+      if (ROW) {
+        // Rows 4q, 4q+1 belong to the even lane of the pair, 4q+2, 4q+3 to the odd lane: the
+        // owner computes their scales (and Philox draws) and shares the multipliers.
+        float rr[16];
+        uint32_t own_s[4];
+        if (TWO_D) {
+#pragma unroll
+          for (int r = 0; r < 16; r++) rr[r] = tile_r;
+#pragma unroll
+          for (int q = 0; q < 4; q++) own_s[q] = tile_s | (tile_s << 8);
+        } else {
+          uint32_t P[8];
+#pragma unroll
+          for (int j = 0; j < 8; j++) P[j] = row_pair_max(v[2 * j], v[2 * j + 1]);
+          uint32_t recv[4];
+#pragma unroll
+          for (int q = 0; q < 4; q++)
+            recv[q] = __shfl_xor_sync(0xFFFFFFFFu, odd ? P[2 * q] : P[2 * q + 1], 1);
+          float r_own[8];
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            const uint32_t bm = vmax2(odd ? P[2 * q + 1] : P[2 * q], recv[q]);
+            own_s[q] = block_scales2(mag_lo(bm), mag_hi(bm), s_enc_r);
+            r_own[2 * q] = tab_row[own_s[q] & 0xFFu];
+            r_own[2 * q + 1] = tab_row[own_s[q] >> 8];
+          }
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            const float o0 = __shfl_xor_sync(0xFFFFFFFFu, r_own[2 * q], 1);
+            const float o1 = __shfl_xor_sync(0xFFFFFFFFu, r_own[2 * q + 1], 1);
+            rr[4 * q] = odd ? o0 : r_own[2 * q];
+            rr[4 * q + 1] = odd ? o1 : r_own[2 * q + 1];
+            rr[4 * q + 2] = odd ? r_own[2 * q] : o0;
+            rr[4 * q + 3] = odd ? r_own[2 * q + 1] : o1;
+          }
+        }
+        uint32_t wr[16][2];  // random words of the lane's half of each row block
+        if (SR_ROW) {
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            const uint64_t b0 = (uint64_t)(row_g0 + 4 * q + (odd ? 2 : 0)) * (uint64_t)row_nb +
+                                (uint64_t)(c.n0 / 16 + kb);
+            const uint4 D0 = block_random(a.seed, a.rng_offset, 0u, b0);
+            const uint4 D1 = block_random(a.seed, a.rng_offset, 0u, b0 + (uint64_t)row_nb);
+            const uint32_t x0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? D0.x : D0.z, 1);
+            const uint32_t x1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? D0.y : D0.w, 1);
+            const uint32_t x2 = __shfl_xor_sync(0xFFFFFFFFu, odd ? D1.x : D1.z, 1);
+            const uint32_t x3 = __shfl_xor_sync(0xFFFFFFFFu, odd ? D1.y : D1.w, 1);
+            wr[4 * q][0] = odd ? x0 : D0.x;      wr[4 * q][1] = odd ? x1 : D0.y;
+            wr[4 * q + 1][0] = odd ? x2 : D1.x;  wr[4 * q + 1][1] = odd ? x3 : D1.y;
+            wr[4 * q + 2][0] = odd ? D0.z : x0;  wr[4 * q + 2][1] = odd ? D0.w : x1;
+            wr[4 * q + 3][0] = odd ? D1.z : x2;  wr[4 * q + 3][1] = odd ? D1.w : x3;
+          }
+        }
+        auto row_code = [&](int r) -> uint32_t {
+          const uint64_t rr2 = f2_pack(rr[r], rr[r]);
+          const float2 t0 = f2_unpack(f2_mul(f2_from_bf16x2(v[r].x), rr2));
+          const float2 t1 = f2_unpack(f2_mul(f2_from_bf16x2(v[r].y), rr2));
+          const float2 t2 = f2_unpack(f2_mul(f2_from_bf16x2(v[r].z), rr2));
+          const float2 t3 = f2_unpack(f2_mul(f2_from_bf16x2(v[r].w), rr2));
+          return e2m1x8<SR_ROW>(t0.x, t0.y, t1.x, t1.y, t2.x, t2.y, t3.x, t3.y,
+                                SR_ROW ? wr[r][0] : 0u, SR_ROW ? wr[r][1] : 0u);
+        };
+        uint8_t* rowp = a.row_codes + row_g0 * (N / 2) + c.n0 / 2 + lane * 4;
+        uint8_t* rsp = a.row_scales + row_g0 * row_nb + c.n0 / 16 + kb + (odd ? 2 : 0) * row_nb;
+        if (full_slab) {
+#pragma unroll
+          for (int r = 0; r < 16; r++)
+            *reinterpret_cast<uint32_t*>(rowp + (int64_t)r * (N / 2)) = row_code(r);
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            rsp[(int64_t)(4 * q) * row_nb] = (uint8_t)(own_s[q] & 0xFFu);
+            rsp[(int64_t)(4 * q + 1) * row_nb] = (uint8_t)(own_s[q] >> 8);
+          }
+        } else if (lane_cols) {
+#pragma unroll
+          for (int r = 0; r < 16; r++)
+            if (r < slab_rows) *reinterpret_cast<uint32_t*>(rowp + (int64_t)r * (N / 2)) = row_code(r);
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            const int r0 = 4 * q + (odd ? 2 : 0);
+            if (r0 < slab_rows) rsp[(int64_t)(4 * q) * row_nb] = (uint8_t)(own_s[q] & 0xFFu);
+            if (r0 + 1 < slab_rows) rsp[(int64_t)(4 * q + 1) * row_nb] = (uint8_t)(own_s[q] >> 8);
+          }
+        }
+      }
+
+      // ---------------- columnwise: one lane-local block per column, two columns at a time --------
+      if (COL) {
+        uint32_t csc[2] = {0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          uint32_t w[16];
+#pragma unroll
+          for (int r = 0; r < 16; r++) w[r] = comp(v[r], k);
+          if (RHT) rht16_pair(w, a.sign_mask);
+          uint32_t s2;
+          uint64_t rc2;
+          if (TWO_D) {
+            s2 = tile_s | (tile_s << 8);
+            rc2 = f2_pack(tile_r, tile_r);
+          } else {
+            const uint32_t m = tree_max16(w);
+            s2 = block_scales2(mag_lo(m), mag_hi(m), s_enc_c);
+            rc2 = f2_pack(tab_col[s2 & 0xFFu], tab_col[s2 >> 8]);
+          }
+          csc[k >> 1] |= s2 << (16 * (k & 1));
+          uint4 W0 = make_uint4(0u, 0u, 0u, 0u), W1 = W0;
+          if (SR_COL) {
+            const uint64_t b0 = (uint64_t)(c.n0 + lane * 8 + 2 * k) * (uint64_t)col_nb +
+                                (uint64_t)(c.colpos / 16 + rb);
+            W0 = block_random(a.seed, a.rng_offset, 1u, b0);
+            W1 = block_random(a.seed, a.rng_offset, 1u, b0 + (uint64_t)col_nb);
+          }
+          uint32_t code[2][2];  // [column of the pair][rows 0..7, 8..15]
+#pragma unroll
+          for (int o = 0; o < 2; o++) {
+            float2 t[8];
+#pragma unroll
+            for (int r = 0; r < 8; r++) t[r] = f2_unpack(f2_mul(f2_from_bf16x2(w[8 * o + r]), rc2));
+            code[0][o] = e2m1x8<SR_COL>(t[0].x, t[1].x, t[2].x, t[3].x, t[4].x, t[5].x, t[6].x,
+                                        t[7].x, comp(W0, 2 * o), comp(W0, 2 * o + 1));
+            code[1][o] = e2m1x8<SR_COL>(t[0].y, t[1].y, t[2].y, t[3].y, t[4].y, t[5].y, t[6].y,
+                                        t[7].y, comp(W1, 2 * o), comp(W1, 2 * o + 1));
+          }
+          *reinterpret_cast<uint4*>(cc_stage + rb * (kTileN * 8) + swz(4 * lane + k) * 16) =
+              make_uint4(code[0][0], code[0][1], code[1][0], code[1][1]);
+        }
+        *reinterpret_cast<uint2*>(cs_stage + rb * kTileN + lane * 8) = make_uint2(csc[0], csc[1]);
+      }
+    }
+
+    // ---- group write-out of the staged columnwise codes and scales ----
+    named_bar_sync(1 + g, 32 * kWarpsPerGroup);
+    if (COL) {
+      const int nrb = (c.nrows + 15) >> 4;
+      const int64_t col0 = (int64_t)c.n0 + 2 * gt;   // this thread's column pair
+      if (col0 < N) {
+        uint4 d[kWarpsPerGroup];
+#pragma unroll
+        for (int r = 0; r < kWarpsPerGroup; r++)
+          if (r < nrb) d[r] = *reinterpret_cast<const uint4*>(cc_stage + r * (kTileN * 8) + swz(gt) * 16);
+        uint8_t* dst0 = a.col_codes + col0 * (a.col_ld / 2) + c.colpos / 2;
+        uint8_t* dst1 = dst0 + a.col_ld / 2;
+        if (nrb == kWarpsPerGroup && ((reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1)) & 15) == 0) {
+          reinterpret_cast<uint4*>(dst0)[0] = make_uint4(d[0].x, d[0].y, d[1].x, d[1].y);
+          reinterpret_cast<uint4*>(dst0)[1] = make_uint4(d[2].x, d[2].y, d[3].x, d[3].y);
+          reinterpret_cast<uint4*>(dst1)[0] = make_uint4(d[0].z, d[0].w, d[1].z, d[1].w);
+          reinterpret_cast<uint4*>(dst1)[1] = make_uint4(d[2].z, d[2].w, d[3].z, d[3].w);
+        } else {
+#pragma unroll
+          for (int r = 0; r < kWarpsPerGroup; r++) {
+            if (r < nrb) {
+              *reinterpret_cast<uint2*>(dst0 + 8 * r) = make_uint2(d[r].x, d[r].y);
+              *reinterpret_cast<uint2*>(dst1 + 8 * r) = make_uint2(d[r].z, d[r].w);
+            }
+          }
+        }
+        uint32_t sc0 = 0, sc1 = 0;
+#pragma unroll
+        for (int r = 0; r < kWarpsPerGroup; r++) {
+          if (r < nrb) {
+            const uint32_t pr = *reinterpret_cast<const uint16_t*>(cs_stage + r * kTileN + 2 * gt);
+            sc0 |= (pr & 0xFFu) << (8 * r);
+            sc1 |= (pr >> 8) << (8 * r);
+          }
+        }
+        uint8_t* sd0 = a.col_scales + col0 * col_nb + c.colpos / 16;
+        uint8_t* sd1 = sd0 + col_nb;
+        if (nrb == kWarpsPerGroup && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
+          *reinterpret_cast<uint32_t*>(sd0) = sc0;
+          *reinterpret_cast<uint32_t*>(sd1) = sc1;
+        } else {
+          for (int r = 0; r < nrb; r++) {
+            sd0[r] = (uint8_t)(sc0 >> (8 * r));
+            sd1[r] = (uint8_t)(sc1 >> (8 * r));
+          }
+        }
+      }
+    }
+  }
+
+  // Every load issued into a stage is waited for by the group that owns its tile, unless that
+  // group gave up: let the last load of each stage land before the CTA leaves.
+  __syncthreads();
+  if (tid == 0) {
+    for (int s = 0; s < kStages; s++) {
+      const int i = last_issued[s];
+      if (i >= 0) mbar_wait_bounded(&full[s], (uint32_t)(i / kStages) & 1u, kWaitLimitNs);
+    }
+  }
+}
+
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
+cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
+  quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL>
+      <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
+  return cudaGetLastError();
+}
+
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
+cudaError_t prepare() {
+  return cudaFuncSetAttribute(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+}
+
+}  // namespace qk
+}  // namespace nvfp4

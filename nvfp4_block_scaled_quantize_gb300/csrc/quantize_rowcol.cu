@@ -1,0 +1,22 @@
+// Instantiations of the quantize kernel (quantize_kernel.cuh): rowwise + columnwise without the RHT.
+#include "quantize_kernel.cuh"
+
+namespace nvfp4 {
+
+cudaError_t launch_quantize_rowcol(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s) {
+  if (m.sr_row && m.sr_col) return qk::launch<true, true, false, false, true, true>(a, grid, s);
+  if (m.sr_row) return qk::launch<true, true, false, false, true, false>(a, grid, s);
+  if (m.sr_col) return qk::launch<true, true, false, false, false, true>(a, grid, s);
+  return qk::launch<true, true, false, false, false, false>(a, grid, s);
+}
+
+cudaError_t prepare_quantize_rowcol() {
+  cudaError_t e = cudaSuccess, r;
+  if ((r = qk::prepare<true, true, false, false, true, true>()) != cudaSuccess) e = r;
+  if ((r = qk::prepare<true, true, false, false, true, false>()) != cudaSuccess) e = r;
+  if ((r = qk::prepare<true, true, false, false, false, true>()) != cudaSuccess) e = r;
+  if ((r = qk::prepare<true, true, false, false, false, false>()) != cudaSuccess) e = r;
+  return e;
+}
+
+}  // namespace nvfp4
