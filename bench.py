@@ -1,14 +1,15 @@
 """Benchmark: NVFP4 quantize throughput (GB/s of BF16-in ideal bytes) on GB300.
 
-One step = the whole hot path on one batch of seeded synthetic input resident in HBM: the amax
-pass (nvfp4_amax) and the quantize pass (nvfp4_quantize with that amax), i.e. every kernel a
-caller runs to turn a BF16 tensor into NVFP4 codes, E4M3 scales and FP32 global scales.
+One step = the whole hot path on one batch of seeded synthetic input resident in HBM: every
+kernel a caller runs to turn a BF16 tensor into NVFP4 codes, E4M3 scales and FP32 global
+scales -- by default one nvfp4_quantize launch that computes the amax itself (fused_amax), or
+with --pipeline two_pass the amax kernel (nvfp4_amax) followed by the quantize kernel.
 Ideal bytes per step = one BF16 read + code writes + scale writes (the metric's roofline
 bytes). L2 is flushed (a 256 MiB write) before every timed step; device time comes from CUDA
 events on the launching stream. Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--pipeline two_pass]
+                  [--workload NAME] [--pipeline fused|two_pass]
 """
 import argparse
 import hashlib
@@ -274,16 +275,26 @@ def run_ours(args, world, rank, local):
         out = api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise)
         rht_amax = w.rht_col
 
-        def step(ev=None):
-            if ev:
-                ev[0].record(stream)
-            a_row, a_col = api.nvfp4_amax(x, rht_col=rht_amax, sign_mask=kw["sign_mask"])
-            if ev:
-                ev[1].record(stream)
-            api.nvfp4_quantize(x, amax_row=a_row, amax_col=a_col, out=out, **kw)
-            if ev:
-                ev[2].record(stream)
-        launches_per_step = 2
+        if args.pipeline == "fused":
+            def step(ev=None):
+                if ev:
+                    ev[0].record(stream)
+                    ev[1].record(stream)
+                api.nvfp4_quantize(x, out=out, fused_amax=True, **kw)
+                if ev:
+                    ev[2].record(stream)
+            launches_per_step = 1
+        else:
+            def step(ev=None):
+                if ev:
+                    ev[0].record(stream)
+                a_row, a_col = api.nvfp4_amax(x, rht_col=rht_amax, sign_mask=kw["sign_mask"])
+                if ev:
+                    ev[1].record(stream)
+                api.nvfp4_quantize(x, amax_row=a_row, amax_col=a_col, out=out, **kw)
+                if ev:
+                    ev[2].record(stream)
+            launches_per_step = 2
         kernel_split = True
 
     for _ in range(args.warmup):
@@ -323,7 +334,7 @@ def run_ours(args, world, rank, local):
             o = api.nvfp4_quantize_grouped(xd, offsets, col_capacity=cap,
                                            **{k: v for k, v in kw.items() if k != "block2d"})
         else:
-            o = api.nvfp4_quantize(xd, **kw)
+            o = api.nvfp4_quantize(xd, fused_amax=args.pipeline == "fused", **kw)
         for k, v in o.items():
             host_out[k].copy_(v, non_blocking=True)
 
@@ -349,7 +360,9 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": w.name, "shape": [w.rows, w.cols],
                    "ideal_bytes_per_step": ideal,
-                   "pipeline": "amax pass + quantize pass (two launches)",
+                   "pipeline": ("one launch: amax phase, grid barrier, quantize phase"
+                                if args.pipeline == "fused" and not w.grouped else
+                                "amax pass + quantize pass (two launches)"),
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": launches_per_step * args.steps,
@@ -380,6 +393,9 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--pipeline", choices=["fused", "two_pass"], default="fused",
+                   help="fused: amax and quantize in one launch; two_pass: amax kernel then "
+                        "quantize kernel")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

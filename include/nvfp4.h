@@ -82,7 +82,11 @@ typedef struct nvfp4_config {
   uint32_t rng_offset;    /* Philox counter word 3 (advance it to draw a new stream) */
   uint64_t rng_seed;      /* Philox key = (low 32 bits, high 32 bits) */
   int32_t fused_amax;     /* when the amax inputs are NULL: 0 = amax pass + quantize pass,
-                             1 = one cooperative launch with a bounded grid barrier */
+                             1 = one cooperative launch: every CTA reduces its share of the
+                             amax, they meet at a bounded grid barrier, then quantize (the
+                             re-read of x comes from L2 when x fits there). Fused calls share
+                             the device workspace's barrier: on one device they must not
+                             overlap in time (issue them on one stream). Plain tensors only. */
   int32_t reserved;       /* must be zero */
 } nvfp4_config;
 

@@ -18,6 +18,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kWorkspaceBytes = 16384;
+constexpr int kFuseWsOffset = 16;  // words: [0] status, [16 .. 16 + kFuseWsWords) fused barrier
+static_assert((kFuseWsOffset + kFuseWsWords) * 4 <= (int)kWorkspaceBytes, "workspace too small");
 
 struct DeviceState {
   bool ready = false;
@@ -190,7 +192,6 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   if (!row && !col) return NVFP4_ERR_UNSUPPORTED;
   if (two_d && (cfg->rht_col || cfg->round_row == NVFP4_ROUND_SR || cfg->round_col == NVFP4_ROUND_SR))
     return NVFP4_ERR_UNSUPPORTED;
-  if (cfg->fused_amax) return NVFP4_ERR_UNSUPPORTED;
   if (M < 0 || N < 0) return NVFP4_ERR_INVALID_ARG;
   if (N % 16 != 0 || ((col || two_d) && M % 16 != 0)) return NVFP4_ERR_SHAPE;
   if (M > INT32_MAX - kTileM || N > INT32_MAX - kTileN) return NVFP4_ERR_SHAPE;
@@ -218,8 +219,12 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   // the gscale outputs' amax slots, which the tile kernel reads.
   const bool need_row_amax = (row || two_d) && amax_row == nullptr;
   const bool need_col_amax = col && !two_d && amax_col == nullptr;
+  // fused_amax: the missing maxima are computed inside the quantize launch (grid barrier)
+  const bool fused = cfg->fused_amax != 0 && (need_row_amax || need_col_amax) &&
+                     (amax_row == nullptr || !(row || two_d)) &&
+                     (amax_col == nullptr || !(col && !two_d));
   float* row_amax_slot = row ? row_gscale : col_gscale;  // 2D column-only keeps it in col_gscale
-  if (need_row_amax || need_col_amax) {
+  if (!fused && (need_row_amax || need_col_amax)) {
     if (need_row_amax && cudaMemsetAsync(row_amax_slot, 0, 8, s) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (need_col_amax && cudaMemsetAsync(col_gscale, 0, 8, s) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (need_col_amax && rht) {
@@ -251,6 +256,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
   q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
+  q.x = x;
+  q.fused = fused ? 1 : 0;
+  q.fuse_ws = ds->workspace + kFuseWsOffset;
   const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0};
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);

@@ -38,12 +38,19 @@ constexpr int kSmemCoords = kSmemSegTile0 + 4 * (kMaxSegments + 4);   // [kStage
 constexpr int kSmemBars = kSmemCoords + 32 * kStages;                 // full[kStages]
 constexpr int kSmemFlags = kSmemBars + 8 * kStages;                   // int32 [4]
 constexpr int kSmemLastIssued = kSmemFlags + 16;                      // int32 [kStages]
-constexpr int kQuantSmemBytes = kSmemLastIssued + 4 * kStages;
+constexpr int kSmemFused = kSmemLastIssued + 4 * kStages;            // uint32 [32 + 4]
+constexpr int kQuantSmemBytes = kSmemFused + 4 * 36;
+
+// Workspace words used by the single-launch (fused amax) path: a self-resetting grid barrier
+// {arrivals, generation} followed by per-CTA partial maxima (rowwise, then columnwise).
+constexpr int kFuseMaxCtas = 1024;
+constexpr int kFuseWsWords = 2 + 2 * kFuseMaxCtas;
 
 // Arguments of the quantize kernel: one BF16 tensor split into row segments (one segment for
 // a plain tensor, one per expert for the grouped case).
 struct QuantArgs {
   CUtensorMap tmap;                 // x as BF16 [rows][cols], box {kTileN, kTileM}
+  const void* x;                    // the same tensor, for the fused amax phase
   int64_t rows, cols;
   const int32_t* offsets;           // cumulative segment ends, or nullptr: one segment
   int32_t segments;
@@ -61,6 +68,8 @@ struct QuantArgs {
   uint64_t seed;
   uint32_t rng_offset;
   uint32_t* status;
+  int32_t fused;                    // 1: compute the amax inside this launch (one segment)
+  uint32_t* fuse_ws;                // kFuseWsWords words of zero-initialised workspace
 };
 
 // What one quantize launch produces.

@@ -23,6 +23,7 @@
 // NVFP4_DEVICE_TIMEOUT and leaves after the loads it issued have landed (bounded too).
 #pragma once
 
+#include "fused_amax.cuh"
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 
@@ -180,23 +181,6 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     if (blockIdx.x == 0 && tid == 0) atomicOr(a.status, 1u);  // NVFP4_DEVICE_BAD_OFFSETS
     return;
   }
-  if (blockIdx.x == 0) {  // global scales {amax, S_dec} of every segment
-    for (int e = tid; e < E; e += blockDim.x) {
-      float enc, dec;
-      if (ROW || TWO_D) {
-        const float amax = a.amax_row[(int64_t)e * a.amax_row_stride];
-        global_scale(amax, enc, dec);
-        if (ROW) { a.row_gscale[2 * e] = amax; a.row_gscale[2 * e + 1] = dec; }
-        if (TWO_D && COL) { a.col_gscale[2 * e] = amax; a.col_gscale[2 * e + 1] = dec; }
-      }
-      if (COL && !TWO_D) {
-        const float amax = a.amax_col[(int64_t)e * a.amax_col_stride];
-        global_scale(amax, enc, dec);
-        a.col_gscale[2 * e] = amax;
-        a.col_gscale[2 * e + 1] = dec;
-      }
-    }
-  }
   const int total = seg_tile0[E];
   const int stride = gridDim.x;
 
@@ -228,6 +212,62 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   if (tid == 0) {
     prefetch_tensormap(&a.tmap);
     for (int i = 0; i < kStages && blockIdx.x + i * stride < total; i++) issue(i);
+  }
+
+  // ---- single-launch amax: reduce, meet at the grid barrier, read every CTA's partials ----
+  float* fused_amax = reinterpret_cast<float*>(smem + kSmemFused) + 32;  // [0] row, [1] col
+  if (a.fused) {
+    volatile uint32_t* red = reinterpret_cast<volatile uint32_t*>(smem + kSmemFused);
+    uint32_t mr, mc;
+    local_amax<COL && RHT>(a.x, a.rows, a.cols, a.sign_mask, mr, mc);
+    mr = cta_max(mr, red);
+    if (COL && RHT) mc = cta_max(mc, red); else mc = mr;
+    if (tid == 0) {
+      a.fuse_ws[2 + blockIdx.x] = mr;
+      a.fuse_ws[2 + kFuseMaxCtas + blockIdx.x] = mc;
+      if (!grid_sync(a.fuse_ws, gridDim.x)) {
+        flags[0] = flags[1] = flags[2] = 1;  // every group leaves without storing
+        atomicOr(a.status, 2u);              // NVFP4_DEVICE_TIMEOUT
+      }
+    }
+    __syncthreads();
+    uint32_t pr = 0, pc = 0;
+    const volatile uint32_t* ws = a.fuse_ws;
+    for (int b = tid; b < (int)gridDim.x; b += blockDim.x) {
+      pr = max(pr, ws[2 + b]);
+      pc = max(pc, ws[2 + kFuseMaxCtas + b]);
+    }
+    pr = cta_max(pr, red);
+    pc = cta_max(pc, red);
+    if (tid == 0) {
+      fused_amax[0] = __uint_as_float(pr << 16);
+      fused_amax[1] = __uint_as_float(pc << 16);
+    }
+    __syncthreads();
+  }
+  // amax of segment e (rowwise / columnwise side)
+  auto amax_row_of = [&](int e) -> float {
+    return a.fused ? fused_amax[0] : a.amax_row[(int64_t)e * a.amax_row_stride];
+  };
+  auto amax_col_of = [&](int e) -> float {
+    return a.fused ? fused_amax[1] : a.amax_col[(int64_t)e * a.amax_col_stride];
+  };
+  if (blockIdx.x == 0) {  // global scales {amax, S_dec} of every segment
+    for (int e = tid; e < E; e += blockDim.x) {
+      float enc, dec;
+      if (ROW || TWO_D) {
+        const float amax = amax_row_of(e);
+        global_scale(amax, enc, dec);
+        if (ROW) { a.row_gscale[2 * e] = amax; a.row_gscale[2 * e + 1] = dec; }
+        if (TWO_D && COL) { a.col_gscale[2 * e] = amax; a.col_gscale[2 * e + 1] = dec; }
+      }
+      if (COL && !TWO_D) {
+        const float amax = amax_col_of(e);
+        global_scale(amax, enc, dec);
+        a.col_gscale[2 * e] = amax;
+        a.col_gscale[2 * e + 1] = dec;
+      }
+    }
   }
 
   // =========================================================================================
@@ -288,8 +328,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     if (c.seg != cur_seg) {  // reciprocal tables of this segment's global scales
       __syncwarp();
       float dec_r = 1.0f, dec_c = 1.0f;
-      if (ROW || TWO_D) global_scale(a.amax_row[(int64_t)c.seg * a.amax_row_stride], s_enc_r, dec_r);
-      if (COL && !TWO_D) global_scale(a.amax_col[(int64_t)c.seg * a.amax_col_stride], s_enc_c, dec_c);
+      if (ROW || TWO_D) global_scale(amax_row_of(c.seg), s_enc_r, dec_r);
+      if (COL && !TWO_D) global_scale(amax_col_of(c.seg), s_enc_c, dec_c);
       if (TWO_D) { s_enc_c = s_enc_r; dec_c = dec_r; }
       for (int idx = lane; idx < kTableEntries; idx += 32) {
         const float sv = e4m3x2_to_float2((uint16_t)idx).x;
@@ -520,6 +560,20 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
 cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
+  if (args.fused) {  // the grid barrier needs every CTA resident: a cooperative launch
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kQuantThreads);
+    cfg.dynamicSmemBytes = kQuantSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL>,
+                              args);
+  }
   quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL>
       <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
   return cudaGetLastError();

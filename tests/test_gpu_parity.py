@@ -329,3 +329,43 @@ def test_full_size_workload_matches_oracle(name):
                    round_row="sr" if w.round_row_sr else "rn", seed=inp["seed"])
         out, ref = run_both(x, **cfg)
     assert_same(out, ref, name)
+
+
+# ------------------------------------------------------------------------------------------
+# Single-launch amax (fused_amax): same outputs as the two-pass pipeline and the oracle
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", sorted(MODES))
+@pytest.mark.parametrize("shape", [(16, 16), (80, 272), (320, 1040)], ids=lambda s: "%dx%d" % s)
+def test_fused_amax_matches_oracle(mode, shape):
+    M, N = shape
+    x = workloads.normal_with_outliers(M, N, seed=M * 31 + N, fraction=0.01, gain=50.0)
+    out, ref = run_both(x, fused_amax=True, **MODES[mode])
+    assert_same(out, ref, "fused %s %s" % (mode, shape))
+
+
+def test_fused_amax_repeated_calls_reuse_the_barrier():
+    """The grid barrier resets itself: many fused launches in a row stay correct."""
+    dev = _cuda()
+    for k in range(6):
+        x_cpu = workloads.laplace(64 * (k + 1), 512, 1e-2 * (k + 1), seed=70 + k)
+        x = x_cpu.to(dev)
+        out = api.nvfp4_quantize(x, rowwise=True, columnwise=True, rht_col=True, sign_mask=0x0FF0,
+                                 round_col="sr", seed=k, fused_amax=True)
+        ref = oracle.quantize(x_cpu, oracle.Config(rowwise=True, columnwise=True, rht_col=True,
+                                                   sign_mask=0x0FF0, round_col_sr=True, seed=k))
+        torch.cuda.synchronize()
+        assert_same(out, ref, "repeat %d" % k)
+    status, bits = api.nvfp4_get_status()
+    assert status == 0 and bits == 0
+
+
+@pytest.mark.parametrize("name", [n for n, w in workloads.WORKLOADS.items() if not w.grouped])
+def test_full_size_workload_fused_matches_oracle(name):
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_input(w)
+    cfg = dict(rowwise=w.rowwise, columnwise=w.columnwise, block2d=w.block2d, rht_col=w.rht_col,
+               sign_mask=inp["sign_mask"], round_col="sr" if w.round_col_sr else "rn",
+               round_row="sr" if w.round_row_sr else "rn", seed=inp["seed"], fused_amax=True)
+    out, ref = run_both(inp["x"], **cfg)
+    assert_same(out, ref, "fused " + name)
