@@ -160,6 +160,30 @@ nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
 nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
                               int64_t R, int64_t C, float* out, void* stream);
 
+/* nvfp4_quantize with fused_amax, for callers that cannot allocate device memory: code that
+ * runs inside a memory allocator's own callbacks, a latency-critical path that must never
+ * reach cudaMalloc (it can synchronize the whole device), or a host that gives this library a
+ * fixed memory budget. The pages have no counterpart of this entry point; it exists only so
+ * that such callers get the single-launch path.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its scratch
+ * -- the grid barrier's counters and the partial maxima of up to 1024 CTAs (one CTA per SM),
+ * about 8 KiB in all -- is a static device array that every GPU loading this library holds
+ * until exit. The caller still passes x and every output.
+ *   Arguments, layouts and shape rules as nvfp4_quantize with amax_row = amax_col = NULL and
+ *   cfg->fused_amax = 1 (cfg->fused_amax itself is ignored); M and N must be positive.
+ *   The first call on a device looks up the array's device address and prepares the kernels
+ *   (no allocation): make that first call before any stream capture.
+ *   A device whose launch would need more than 1024 CTAs is refused with
+ *   NVFP4_ERR_UNSUPPORTED (GB300 launches one CTA per SM, 152).
+ *   Every call on a device shares the array: calls that overlap on the GPU race (issue them on
+ *   one stream). Each call clears the barrier's arrival count before it launches; the partial
+ *   maxima are rewritten by every call. A wait that gives up is recorded in the array's own
+ *   status word, which nvfp4_get_status does not read. */
+nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const nvfp4_config* cfg,
+                                    uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,
+                                    uint8_t* col_codes, uint8_t* col_scales, float* col_gscale,
+                                    void* stream);
+
 /* Synchronize `stream`, then read and clear the current device's status word into
  * *device_status (NVFP4_DEVICE_* bits). Returns NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT
  * when bits were set, NVFP4_OK otherwise. */

@@ -20,7 +20,7 @@ DEVICE_BAD_OFFSETS = 0x1
 DEVICE_TIMEOUT = 0x2
 
 EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped",
-            "nvfp4_dequantize", "nvfp4_get_status"]
+            "nvfp4_dequantize", "nvfp4_get_status", "nvfp4_quantize_noalloc"]
 
 
 class Config(ctypes.Structure):
@@ -79,6 +79,8 @@ def load(build_if_missing: bool = False):
                                          vp, vp]
     L.nvfp4_dequantize.restype = ctypes.c_int
     L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+    L.nvfp4_quantize_noalloc.restype = ctypes.c_int
+    L.nvfp4_quantize_noalloc.argtypes = [vp, i64, i64, cfgp, vp, vp, vp, vp, vp, vp, vp]
     L.nvfp4_get_status.restype = ctypes.c_int
     L.nvfp4_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     _lib = L
