@@ -59,29 +59,41 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def kernel_traffic(kernel_file: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel and workload, valid
-    only while the kernel source is unchanged (its sha256 is recorded in the summary)."""
-    summary = os.path.join(ROOT, "profiles", "quantize_tiles_%s.txt" % workload)
-    src = os.path.join(ROOT, "nvfp4_block_scaled_quantize_gb300", "csrc", kernel_file)
-    if not (os.path.exists(summary) and os.path.exists(src)):
+KERNEL_SOURCES = ("quantize_kernel.cuh", "fused_amax.cuh", "nvfp4_device.cuh", "nvfp4_internal.h")
+
+
+def kernel_source_digest() -> str:
+    """sha256 (first 16 hex digits) over the tile kernel's sources, in a fixed order."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_quantize_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(workload: str, pipeline: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, workload and
+    pipeline, valid only while the kernel sources are unchanged (the summary records their
+    digest)."""
+    summary = os.path.join(ROOT, "profiles", "quantize_tiles_%s_%s.txt" % (workload, pipeline))
+    if not os.path.exists(summary):
         return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     fields = {}
     for line in open(summary):
-        if ":" in line:
+        if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("source_sha256_16") != digest:
+    if fields.get("source_sha256_16") != kernel_source_digest():
         return None
     try:
-        return int(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return int(fields["dram_bytes_per_launch"].split()[0])
+    except (KeyError, ValueError, IndexError):
         return None
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples of SM clock and throttle reasons; summary() keeps the samples that
+    arrived between mark_start() and mark_end() (the timed region)."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -90,12 +102,13 @@ class ClockSampler:
         self.idx = device_index
         self.proc = None
         self.lines = []
+        self.window = (0.0, float("inf"))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -105,7 +118,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_start(self):
+        self.window = (time.monotonic(), float("inf"))
+
+    def mark_end(self):
+        self.window = (self.window[0], time.monotonic())
 
     def __exit__(self, *exc):
         if self.proc:
@@ -118,7 +137,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if not self.window[0] <= t <= self.window[1]:
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -278,8 +299,7 @@ def run_ours(args, world, rank, local):
         if args.pipeline == "fused":
             def step(ev=None):
                 if ev:
-                    ev[0].record(stream)
-                    ev[1].record(stream)
+                    ev[0].record(stream)  # one launch: the step and the kernel are the same span
                 api.nvfp4_quantize(x, out=out, fused_amax=True, **kw)
                 if ev:
                     ev[2].record(stream)
@@ -297,27 +317,30 @@ def run_ours(args, world, rank, local):
             launches_per_step = 2
         kernel_split = True
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    status, bits = api.nvfp4_get_status(dev)
-    if status != 0:
-        raise RuntimeError("device status %d (bits %#x) after warm-up" % (status, bits))
-
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
-        time.sleep(0.3)
+        time.sleep(0.3)  # the sampler is up before the GPU work starts
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
+        status, bits = api.nvfp4_get_status(dev)
+        if status != 0:
+            raise RuntimeError("device status %d (bits %#x) after warm-up" % (status, bits))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        clocks.mark_start()
         for i in range(args.steps):
             flush.zero_()
             step(events[i])
         torch.cuda.synchronize(dev)
-        time.sleep(0.2)
+        clocks.mark_end()
+        time.sleep(0.05)
     barrier(world)
     step_ms = [e[0].elapsed_time(e[2]) for e in events]
-    quant_ms = [e[1].elapsed_time(e[2]) for e in events] if kernel_split else None
+    if kernel_split:
+        quant_ms = ([e[0].elapsed_time(e[2]) for e in events] if args.pipeline == "fused"
+                    else [e[1].elapsed_time(e[2]) for e in events])
     total_s = sum(step_ms) / 1e3
     total_s = max_over_ranks(world, total_s)
     value = ideal * args.steps * world / total_s / 1e9
@@ -370,6 +393,8 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
     }
+    line["step_us"] = {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
+                       "max": max(step_ms) * 1e3}
     if kernel_split:
         qk = statistics.mean(quant_ms) / 1e3
         achieved = ideal / qk / 1e9
@@ -377,9 +402,9 @@ def run_ours(args, world, rank, local):
                             "frac": achieved / hbm, "peak_kind": peak_kind,
                             "kernel": "quantize_tiles_kernel",
                             "kernel_us": qk * 1e6,
-                            "traffic": kernel_traffic("quantize_tiles.cu", w.name)}
-        amax_us = statistics.mean([e[0].elapsed_time(e[1]) for e in events]) * 1e3
-        line["amax_pass_us"] = amax_us
+                            "traffic": kernel_traffic(w.name, args.pipeline)}
+        if args.pipeline != "fused" or w.grouped:
+            line["amax_pass_us"] = statistics.mean([e[0].elapsed_time(e[1]) for e in events]) * 1e3
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(line), flush=True)
@@ -388,8 +413,8 @@ def run_ours(args, world, rank, local):
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -1,7 +1,7 @@
-// Single-launch amax for the quantize kernel: every CTA reduces its share of the tensor
-// (plain and, for the columnwise RHT, transformed maxima), the CTAs meet at a grid barrier,
-// and each reads the per-CTA partials back. The tensor is walked from its end to its start so
-// that the tiles the quantize phase reads first are the ones most recently pulled into L2.
+// Single-launch amax for the quantize kernel: every CTA reduces the tiles it is about to
+// quantize (plain and, for the columnwise RHT, transformed maxima), the CTAs meet at a grid
+// barrier, and each reads the per-CTA partials back. These are the reduction and barrier
+// pieces; the tile walk is in the quantize kernel.
 //
 // Page cited: "[nvfp4_training] Optimize CuteDSL kernels for NVFP4 training" (pytorch/ao pull
 // request #4798), "Performance": its pipelines are an amax kernel followed by a quantize
@@ -29,79 +29,41 @@ __device__ __forceinline__ uint32_t cta_max(uint32_t v, volatile uint32_t* red) 
   return r;
 }
 
-// This CTA's share of max |x| (mr) and, when rht, of max |bf16(RHT(x))| over 16-row column
-// blocks (mc), as 16-bit BF16 magnitudes. rows % 16 == 0 when rht.
-template <bool RHT>
-__device__ __forceinline__ void local_amax(const void* x, int64_t rows, int64_t cols,
-                                           uint32_t sign_mask, uint32_t& mr, uint32_t& mc) {
-  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t gstride = (int64_t)gridDim.x * blockDim.x;
-  uint32_t m = 0, mt = 0;
-  if (!RHT) {
-    const uint4* p = reinterpret_cast<const uint4*>(x);
-    const int64_t total = rows * cols / 8;  // 16-byte vectors
-    int64_t j = gtid;
-    for (; j + 3 * gstride < total; j += 4 * gstride) {
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; u++) v[u] = p[total - 1 - (j + u * gstride)];
-#pragma unroll
-      for (int u = 0; u < 4; u++)
-        m = vmax2(m, vmax2(vmax2(abs2(v[u].x), abs2(v[u].y)), vmax2(abs2(v[u].z), abs2(v[u].w))));
-    }
-    for (; j < total; j += gstride) {
-      const uint4 v = p[total - 1 - j];
-      m = vmax2(m, vmax2(vmax2(abs2(v.x), abs2(v.y)), vmax2(abs2(v.z), abs2(v.w))));
-    }
-  } else {
-    const uint2* p = reinterpret_cast<const uint2*>(x);
-    const int64_t chunks = cols / 4;               // 4-column pieces of a row
-    const int64_t items = (rows / 16) * chunks;    // 16-row x 4-column items
-    for (int64_t j = gtid; j < items; j += gstride) {
-      const int64_t it = items - 1 - j;
-      const int64_t rb = it / chunks, ch = it - rb * chunks;
-      uint32_t w0[16], w1[16];
-#pragma unroll
-      for (int i = 0; i < 16; i++) {
-        const uint2 v = p[(rb * 16 + i) * chunks + ch];
-        w0[i] = v.x;
-        w1[i] = v.y;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; i++) m = vmax2(m, vmax2(abs2(w0[i]), abs2(w1[i])));
-      rht16_pair(w0, sign_mask);
-      rht16_pair(w1, sign_mask);
-#pragma unroll
-      for (int i = 0; i < 16; i++) mt = vmax2(mt, vmax2(abs2(w0[i]), abs2(w1[i])));
-    }
-  }
-  mr = max(m & 0xFFFFu, m >> 16);
-  mc = RHT ? max(mt & 0xFFFFu, mt >> 16) : mr;
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
-// Grid barrier for a launch whose CTAs are all resident: one thread per CTA calls it.
-// ws[0] counts arrivals and is reset by the last one, ws[1] is a generation number that only
-// grows, so the barrier needs no clearing between launches on one stream. Returns false when
-// the wait passed its limit.
+// Grid barrier for a launch whose CTAs are all resident: one thread per CTA calls it, after
+// its own writes that the other CTAs read. ws[0] counts arrivals; the last arrival resets it
+// and publishes the release by bumping the generation ws[1], which only grows, so the
+// barrier needs no clearing between launches on one stream. Returns false when the wait
+// passed its limit.
 __device__ __forceinline__ bool grid_sync(uint32_t* ws, uint32_t nblocks) {
-  volatile uint32_t* gen = ws + 1;
-  const uint32_t g = *gen;
-  __threadfence();
-  const uint32_t old = atomicAdd(ws, 1u);
-  if (old == nblocks - 1) {
-    atomicExch(ws, 0u);
-    __threadfence();
-    atomicAdd(ws + 1, 1u);
+  const uint32_t g = ld_acquire_gpu(ws + 1);  // cannot change before this CTA arrives
+  if (atom_add_acq_rel_gpu(ws, 1u) == nblocks - 1) {
+    st_relaxed_gpu(ws, 0u);        // nobody else touches the count until the next launch
+    st_release_gpu(ws + 1, g + 1u);
     return true;
   }
   uint64_t t0, t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-  while (*gen == g) {
+  while (ld_acquire_gpu(ws + 1) == g) {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     if (t - t0 > kBarrierLimitNs) return false;
-    __nanosleep(128);
   }
-  __threadfence();
   return true;
 }
 

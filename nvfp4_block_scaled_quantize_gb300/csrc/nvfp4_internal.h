@@ -37,8 +37,8 @@ constexpr int kSmemSegTile0 = kSmemSegCol0 + 4 * kMaxSegments;        // [kMaxSe
 constexpr int kSmemCoords = kSmemSegTile0 + 4 * (kMaxSegments + 4);   // [kStages][8] int32
 constexpr int kSmemBars = kSmemCoords + 32 * kStages;                 // full[kStages]
 constexpr int kSmemFlags = kSmemBars + 8 * kStages;                   // int32 [4]
-constexpr int kSmemLastIssued = kSmemFlags + 16;                      // int32 [kStages]
-constexpr int kSmemFused = kSmemLastIssued + 4 * kStages;            // uint32 [32 + 4]
+constexpr int kSmemIssued = kSmemFlags + 16;                          // int32 [kStages]
+constexpr int kSmemFused = kSmemIssued + 4 * kStages;            // uint32 [32 + 4]
 constexpr int kQuantSmemBytes = kSmemFused + 4 * 36;
 
 // Workspace words used by the single-launch (fused amax) path: a self-resetting grid barrier

@@ -97,12 +97,14 @@ __device__ __forceinline__ uint32_t e2m1x8(float t0, float t1, float t2, float t
   return d;
 }
 
-// Bounded wait until stage s has been given tile i (its monotonic last-issued index).
-__device__ __forceinline__ bool wait_issued(volatile int32_t* last_issued, int s, int i) {
-  if (last_issued[s] >= i) return true;
+// Bounded wait until at least `count` loads have been issued into stage s (a monotonic
+// per-stage count). Only then does the mbarrier parity of load count - 1 name its phase
+// unambiguously: the previous load of the stage has been consumed, so its phase is complete.
+__device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int count) {
+  if (issued[s] >= count) return true;
   uint64_t t0;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-  while (last_issued[s] < i) {
+  while (issued[s] < count) {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     if (t - t0 > kWaitLimitNs) return false;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   Coord* coords = reinterpret_cast<Coord*>(smem + kSmemCoords);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBars);
   volatile int32_t* flags = reinterpret_cast<volatile int32_t*>(smem + kSmemFlags);
-  volatile int32_t* last_issued = reinterpret_cast<volatile int32_t*>(smem + kSmemLastIssued);
+  volatile int32_t* issued = reinterpret_cast<volatile int32_t*>(smem + kSmemIssued);
 
   const int E = a.segments;
   const int tiles_n = (int)((a.cols + kTileN - 1) / kTileN);
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
       mbar_init(&full[s], 1);
-      last_issued[s] = -1;
+      issued[s] = 0;
     }
     fence_barrier_init();
   }
@@ -183,11 +185,13 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   }
   const int total = seg_tile0[E];
   const int stride = gridDim.x;
+  // this CTA's tiles: blockIdx.x + i * stride for local index i < n_local
+  const int n_local = (int)blockIdx.x < total ? (total - (int)blockIdx.x + stride - 1) / stride : 0;
+  const bool fused = a.fused != 0;
 
-  // Load tile (local index) i of this CTA into stage i % kStages.
-  auto issue = [&](int i) {
+  // Load local tile i of this CTA into stage s.
+  auto issue = [&](int i, int s) {
     const int tile = blockIdx.x + i * stride;
-    const int s = i % kStages;
     int lo = 0, hi = E;  // segment: largest e with seg_tile0[e] <= tile
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -205,32 +209,82 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     c.pad1 = c.pad2 = 0;
     coords[s] = c;
     __threadfence_block();
-    last_issued[s] = i;  // stage s now serves tile i: its next mbarrier phase is tile i's
+    issued[s] = issued[s] + 1;  // the stage's next mbarrier phase is this load's
     mbar_expect_tx(&full[s], kStageBytes);
     tma_load_2d(smem + kSmemStages + s * kStageBytes, &a.tmap, c.n0, c.row0, &full[s]);
   };
+  // The first kStages loads: the quantize phase's first tiles, or, with the single-launch
+  // amax, the amax phase's (it walks the local tiles from the last to the first, so that the
+  // quantize phase, walking forward, starts on the kStages tiles still in shared memory).
   if (tid == 0) {
     prefetch_tensormap(&a.tmap);
-    for (int i = 0; i < kStages && blockIdx.x + i * stride < total; i++) issue(i);
+    for (int k = 0; k < kStages && k < n_local; k++) issue(fused ? n_local - 1 - k : k, k);
   }
 
-  // ---- single-launch amax: reduce, meet at the grid barrier, read every CTA's partials ----
+  const int g = warp / kWarpsPerGroup;   // group
+  const int rb = warp % kWarpsPerGroup;  // slab of the tile (rows 16 rb .. 16 rb + 15)
+  const int gt = tid - g * 32 * kWarpsPerGroup;  // thread index inside the group
+
+  // ---- single-launch amax: stream the local tiles through the stage ring (last to first),
+  // reduce, meet at the grid barrier, read every CTA's partials ----
   float* fused_amax = reinterpret_cast<float*>(smem + kSmemFused) + 32;  // [0] row, [1] col
-  if (a.fused) {
+  if (fused) {
+    uint32_t m = 0u, mt = 0u;
+    bool ok = true;
+    for (int k = g; k < n_local; k += kGroups) {
+      const int s = k % kStages, p = k / kStages;  // load p of stage s
+      const int i = n_local - 1 - k;
+      bool arrived = wait_issued(issued, s, p + 1);
+      arrived = arrived && mbar_wait_bounded(&full[s], (uint32_t)p & 1u, kWaitLimitNs);
+      if (!arrived || coords[s].tile != (int)blockIdx.x + i * stride) ok = false;
+      // rows and columns outside the tensor arrive as zeros: no masking for a maximum
+      uint4 v[16];
+      const uint32_t src = smem_u32(smem + kSmemStages + s * kStageBytes) +
+                           (16 * rb) * (kTileN * 2) + lane * 16;
+#pragma unroll
+      for (int r = 0; r < 16; r++) v[r] = lds128(src + r * (kTileN * 2));
+      named_bar_sync(1 + g, 32 * kWarpsPerGroup);
+      if (gt == 0 && k + kStages < n_local) {
+        fence_proxy_async();
+        issue(n_local - 1 - (k + kStages), s);
+      }
+      // max.xorsign.abs: the magnitude is exact, the sign bit is cleared at the end (inputs
+      // are finite, so no NaN takes part)
+#pragma unroll
+      for (int r = 0; r < 16; r += 2)
+        m = hmax_abs2(m, hmax_abs2(hmax_abs2(hmax_abs2(v[r].x, v[r].y), hmax_abs2(v[r].z, v[r].w)),
+                                   hmax_abs2(hmax_abs2(v[r + 1].x, v[r + 1].y),
+                                             hmax_abs2(v[r + 1].z, v[r + 1].w))));
+      if (COL && RHT) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; c4++) {
+          uint32_t w[16];
+#pragma unroll
+          for (int r = 0; r < 16; r++) w[r] = comp(v[r], c4);
+          rht16_pair(w, a.sign_mask);
+          mt = vmax2(mt, tree_max16(w));  // both sign-cleared
+        }
+      }
+    }
+    if (!ok) {
+      flags[3] = 1;  // this CTA stores nothing (below); the others still need its partials
+      if (lane == 0) atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
+    }
+    m &= 0x7FFF7FFFu;
     volatile uint32_t* red = reinterpret_cast<volatile uint32_t*>(smem + kSmemFused);
-    uint32_t mr, mc;
-    local_amax<COL && RHT>(a.x, a.rows, a.cols, a.sign_mask, mr, mc);
-    mr = cta_max(mr, red);
-    if (COL && RHT) mc = cta_max(mc, red); else mc = mr;
+    uint32_t mr = cta_max(max(m & 0xFFFFu, m >> 16), red);
+    uint32_t mc = mr;
+    if (COL && RHT) mc = cta_max(max(mt & 0xFFFFu, mt >> 16), red);
     if (tid == 0) {
       a.fuse_ws[2 + blockIdx.x] = mr;
       a.fuse_ws[2 + kFuseMaxCtas + blockIdx.x] = mc;
       if (!grid_sync(a.fuse_ws, gridDim.x)) {
-        flags[0] = flags[1] = flags[2] = 1;  // every group leaves without storing
-        atomicOr(a.status, 2u);              // NVFP4_DEVICE_TIMEOUT
+        flags[3] = 1;
+        atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
       }
     }
     __syncthreads();
+    if (flags[3]) flags[0] = flags[1] = flags[2] = 1;  // every group leaves without storing
     uint32_t pr = 0, pc = 0;
     const volatile uint32_t* ws = a.fuse_ws;
     for (int b = tid; b < (int)gridDim.x; b += blockDim.x) {
@@ -273,9 +327,6 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   // =========================================================================================
   // Groups of four warps, one tile at a time.
   // =========================================================================================
-  const int g = warp / kWarpsPerGroup;   // group
-  const int rb = warp % kWarpsPerGroup;  // slab of the tile (rows 16 rb .. 16 rb + 15)
-  const int gt = tid - g * 32 * kWarpsPerGroup;  // thread index inside the group
   const bool odd = (lane & 1) != 0;
   const int kb = lane >> 1;              // rowwise block of the tile row (lane pair)
   float* tab_row = reinterpret_cast<float*>(smem + kSmemTables) + warp * 2 * kTableEntries;
@@ -287,15 +338,27 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   int cur_seg = -1;
   float s_enc_r = 1.0f, s_enc_c = 1.0f;
 
-  for (int i = g;; i += kGroups) {
+  for (int i = g; i < n_local; i += kGroups) {
     const int tile = blockIdx.x + i * stride;
-    if (tile >= total) break;
-    const int s = i % kStages;
+    // Stage and load number of local tile i. Plain: stage i % kStages, its load i / kStages.
+    // After the single-launch amax phase (loads a_s into stage s, last tiles first) the first
+    // kStages tiles are still in the stages; tile i >= kStages goes where tile i - kStages was.
+    int s, p;
+    bool resident = false;
+    if (fused) {
+      s = (n_local - 1 - i) % kStages;
+      const int a_s = n_local > s ? (n_local - 1 - s) / kStages + 1 : 0;
+      p = a_s + i / kStages - 1;
+      resident = i < kStages;
+    } else {
+      s = i % kStages;
+      p = i / kStages;
+    }
     // Three groups share four stages, so a group can reach tile i before the group that
-    // drains the stage's previous tile has issued it. Wait until tile i is the stage's
-    // current load; only then does the phase parity name tile i's phase unambiguously.
-    bool arrived = wait_issued(last_issued, s, i);
-    arrived = arrived && mbar_wait_bounded(&full[s], (uint32_t)(i / kStages) & 1u, kWaitLimitNs);
+    // drains the stage's previous tile has issued it. Wait until the load is issued; only
+    // then does the phase parity name its phase unambiguously.
+    bool arrived = resident || wait_issued(issued, s, p + 1);
+    arrived = arrived && (resident || mbar_wait_bounded(&full[s], (uint32_t)p & 1u, kWaitLimitNs));
     const Coord c = coords[s];
     if (!arrived || c.tile != tile) {
       // the data never arrived (or the stage holds another tile): record it; the loads below
@@ -320,9 +383,9 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     // (the previous tile was written out), and the group's abort flag is settled.
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     if (flags[g]) break;
-    if (gt == 0 && blockIdx.x + (i + kStages) * stride < total) {
+    if (gt == 0 && i + kStages < n_local) {
       fence_proxy_async();
-      issue(i + kStages);
+      issue(i + kStages, s);
     }
 
     if (c.seg != cur_seg) {  // reciprocal tables of this segment's global scales
@@ -552,8 +615,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   __syncthreads();
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
-      const int i = last_issued[s];
-      if (i >= 0) mbar_wait_bounded(&full[s], (uint32_t)(i / kStages) & 1u, kWaitLimitNs);
+      const int loads = issued[s];
+      if (loads > 0) mbar_wait_bounded(&full[s], (uint32_t)(loads - 1) & 1u, kWaitLimitNs);
     }
   }
 }
