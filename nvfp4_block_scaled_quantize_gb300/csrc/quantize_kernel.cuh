@@ -572,7 +572,12 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           if (r < nrb) d[r] = *reinterpret_cast<const uint4*>(cc_stage + r * (kTileN * 8) + swz(gt) * 16);
         uint8_t* dst0 = a.col_codes + col0 * (a.col_ld / 2) + c.colpos / 2;
         uint8_t* dst1 = dst0 + a.col_ld / 2;
-        if (nrb == kWarpsPerGroup && ((reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1)) & 15) == 0) {
+        const uintptr_t dbits = reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1);
+        if (nrb == kWarpsPerGroup && (dbits & 31) == 0) {
+          // each column's 64 codes are one full 32-byte sector: one store per column
+          stg256(dst0, make_uint4(d[0].x, d[0].y, d[1].x, d[1].y), make_uint4(d[2].x, d[2].y, d[3].x, d[3].y));
+          stg256(dst1, make_uint4(d[0].z, d[0].w, d[1].z, d[1].w), make_uint4(d[2].z, d[2].w, d[3].z, d[3].w));
+        } else if (nrb == kWarpsPerGroup && (dbits & 15) == 0) {
           reinterpret_cast<uint4*>(dst0)[0] = make_uint4(d[0].x, d[0].y, d[1].x, d[1].y);
           reinterpret_cast<uint4*>(dst0)[1] = make_uint4(d[2].x, d[2].y, d[3].x, d[3].y);
           reinterpret_cast<uint4*>(dst1)[0] = make_uint4(d[0].z, d[0].w, d[1].z, d[1].w);
