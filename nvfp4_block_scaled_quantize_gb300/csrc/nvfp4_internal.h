@@ -29,8 +29,8 @@ constexpr int kColScaleStage = kWarpsPerGroup * kTileN;      // [4 slabs][256 B]
 constexpr int kSmemStages = 0;
 constexpr int kSmemColCodes = kSmemStages + kStages * kStageBytes;
 constexpr int kSmemColScales = kSmemColCodes + kGroups * kColCodeStage;
-constexpr int kSmemTables = kSmemColScales + kGroups * kColScaleStage;  // per warp: 2 x 128 f32
-constexpr int kSmemSegStart = kSmemTables + kConsumerWarps * 2 * kTableEntries * 4;
+constexpr int kSmemTables = kSmemColScales + kGroups * kColScaleStage;  // per group: 2 x 128 f32
+constexpr int kSmemSegStart = kSmemTables + kGroups * 2 * kTableEntries * 4;
 constexpr int kSmemSegEnd = kSmemSegStart + 4 * kMaxSegments;
 constexpr int kSmemSegCol0 = kSmemSegEnd + 4 * kMaxSegments;
 constexpr int kSmemSegTile0 = kSmemSegCol0 + 4 * kMaxSegments;        // [kMaxSegments + 4]

@@ -134,60 +134,12 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int tiles_n = (int)((a.cols + kTileN - 1) / kTileN);
   const int64_t N = a.cols;
 
-  // ---- segment table: starts, ends, padded column starts, tile prefix sums ----
-  if (tid < 4) flags[tid] = 0;
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    const int32_t start = (a.offsets == nullptr || e == 0) ? 0 : a.offsets[e - 1];
-    const int32_t end = (a.offsets == nullptr) ? (int32_t)a.rows : a.offsets[e];
-    if (start < 0 || end < start || (int64_t)end > a.rows) flags[3] = 1;
-    seg_start[e] = start;
-    seg_end[e] = end;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int32_t tile_base = 0, col_base = 0;
-    for (int c0 = 0; c0 < E; c0 += 32) {
-      const int e = c0 + lane;
-      const int32_t n = (e < E && !flags[3]) ? seg_end[e] - seg_start[e] : 0;
-      const int32_t t0 = ((n + kTileM - 1) / kTileM) * tiles_n;
-      const int32_t p0 = ((n + 15) / 16) * 16;
-      int32_t t = t0, p = p0;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int32_t tu = __shfl_up_sync(0xFFFFFFFFu, t, d);
-        const int32_t pu = __shfl_up_sync(0xFFFFFFFFu, p, d);
-        if (lane >= d) { t += tu; p += pu; }
-      }
-      if (e < E) {
-        seg_tile0[e] = tile_base + t - t0;
-        seg_col0[e] = col_base + p - p0;
-      }
-      tile_base += __shfl_sync(0xFFFFFFFFu, t, 31);
-      col_base += __shfl_sync(0xFFFFFFFFu, p, 31);
-    }
-    if (lane == 0) {
-      seg_tile0[E] = tile_base;
-      if (COL && (int64_t)col_base > a.col_ld) flags[3] = 1;
-    }
-  }
-  if (tid == 0) {
-    for (int s = 0; s < kStages; s++) {
-      mbar_init(&full[s], 1);
-      issued[s] = 0;
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-  if (flags[3]) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(a.status, 1u);  // NVFP4_DEVICE_BAD_OFFSETS
-    return;
-  }
-  const int total = seg_tile0[E];
   const int stride = gridDim.x;
-  // this CTA's tiles: blockIdx.x + i * stride for local index i < n_local
-  const int n_local = (int)blockIdx.x < total ? (total - (int)blockIdx.x + stride - 1) / stride : 0;
   const bool fused = a.fused != 0;
+  // A plain tensor is one segment: the first loads leave at once, before anything else
+  // (the grouped path first needs the segment table below).
+  const bool plain = a.offsets == nullptr;
+  int total = 0, n_local = 0;
 
   // Load local tile i of this CTA into stage s.
   auto issue = [&](int i, int s) {
@@ -216,9 +168,77 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   // The first kStages loads: the quantize phase's first tiles, or, with the single-launch
   // amax, the amax phase's (it walks the local tiles from the last to the first, so that the
   // quantize phase, walking forward, starts on the kStages tiles still in shared memory).
-  if (tid == 0) {
+  auto first_loads = [&]() {
     prefetch_tensormap(&a.tmap);
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&full[s], 1);
+      issued[s] = 0;
+    }
+    fence_barrier_init();
     for (int k = 0; k < kStages && k < n_local; k++) issue(fused ? n_local - 1 - k : k, k);
+  };
+
+  if (plain) {
+    const int tiles_m = (int)((a.rows + kTileM - 1) / kTileM);
+    total = tiles_m * tiles_n;
+    n_local = (int)blockIdx.x < total ? (total - (int)blockIdx.x + stride - 1) / stride : 0;
+    if (tid == 0) {
+      flags[0] = flags[1] = flags[2] = flags[3] = 0;
+      seg_start[0] = 0;
+      seg_end[0] = (int32_t)a.rows;
+      seg_col0[0] = 0;
+      seg_tile0[0] = 0;
+      seg_tile0[1] = total;
+      first_loads();
+    }
+    __syncthreads();
+  } else {
+    // ---- segment table: starts, ends, padded column starts, tile prefix sums ----
+    if (tid < 4) flags[tid] = 0;
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int32_t start = e == 0 ? 0 : a.offsets[e - 1];
+      const int32_t end = a.offsets[e];
+      if (start < 0 || end < start || (int64_t)end > a.rows) flags[3] = 1;
+      seg_start[e] = start;
+      seg_end[e] = end;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int32_t tile_base = 0, col_base = 0;
+      for (int c0 = 0; c0 < E; c0 += 32) {
+        const int e = c0 + lane;
+        const int32_t n = (e < E && !flags[3]) ? seg_end[e] - seg_start[e] : 0;
+        const int32_t t0 = ((n + kTileM - 1) / kTileM) * tiles_n;
+        const int32_t p0 = ((n + 15) / 16) * 16;
+        int32_t t = t0, p = p0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int32_t tu = __shfl_up_sync(0xFFFFFFFFu, t, d);
+          const int32_t pu = __shfl_up_sync(0xFFFFFFFFu, p, d);
+          if (lane >= d) { t += tu; p += pu; }
+        }
+        if (e < E) {
+          seg_tile0[e] = tile_base + t - t0;
+          seg_col0[e] = col_base + p - p0;
+        }
+        tile_base += __shfl_sync(0xFFFFFFFFu, t, 31);
+        col_base += __shfl_sync(0xFFFFFFFFu, p, 31);
+      }
+      if (lane == 0) {
+        seg_tile0[E] = tile_base;
+        if (COL && (int64_t)col_base > a.col_ld) flags[3] = 1;
+      }
+    }
+    __syncthreads();
+    if (flags[3]) {
+      if (blockIdx.x == 0 && tid == 0) atomicOr(a.status, 1u);  // NVFP4_DEVICE_BAD_OFFSETS
+      return;
+    }
+    total = seg_tile0[E];
+    n_local = (int)blockIdx.x < total ? (total - (int)blockIdx.x + stride - 1) / stride : 0;
+    if (tid == 0) first_loads();
+    __syncthreads();
   }
 
   const int g = warp / kWarpsPerGroup;   // group
@@ -329,7 +349,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   // =========================================================================================
   const bool odd = (lane & 1) != 0;
   const int kb = lane >> 1;              // rowwise block of the tile row (lane pair)
-  float* tab_row = reinterpret_cast<float*>(smem + kSmemTables) + warp * 2 * kTableEntries;
+  float* tab_row = reinterpret_cast<float*>(smem + kSmemTables) + g * 2 * kTableEntries;
   float* tab_col = tab_row + kTableEntries;
   uint8_t* cc_stage = smem + kSmemColCodes + g * kColCodeStage;
   uint8_t* cs_stage = smem + kSmemColScales + g * kColScaleStage;
@@ -337,6 +357,22 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int64_t col_nb = a.col_ld / 16;
   int cur_seg = -1;
   float s_enc_r = 1.0f, s_enc_c = 1.0f;
+  // Global scales of segment e and the group's reciprocal tables for them: one entry of each
+  // table per thread of the group. Called by the whole group, between tiles (no warp of the
+  // group is still reading the previous tables).
+  auto set_segment = [&](int e) {
+    float dec_r = 1.0f, dec_c = 1.0f;
+    if (ROW || TWO_D) global_scale(amax_row_of(e), s_enc_r, dec_r);
+    if (COL && !TWO_D) global_scale(amax_col_of(e), s_enc_c, dec_c);
+    if (TWO_D) { s_enc_c = s_enc_r; dec_c = dec_r; }
+    static_assert(kTableEntries == 32 * kWarpsPerGroup, "one table entry per group thread");
+    const float sv = e4m3x2_to_float2((uint16_t)gt).x;
+    tab_row[gt] = element_multiplier(sv, dec_r);
+    tab_col[gt] = element_multiplier(sv, dec_c);
+    named_bar_sync(1 + g, 32 * kWarpsPerGroup);
+    cur_seg = e;
+  };
+  if (plain && n_local > g) set_segment(0);  // overlaps the first loads (or follows the amax)
 
   for (int i = g; i < n_local; i += kGroups) {
     const int tile = blockIdx.x + i * stride;
@@ -388,20 +424,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       issue(i + kStages, s);
     }
 
-    if (c.seg != cur_seg) {  // reciprocal tables of this segment's global scales
-      __syncwarp();
-      float dec_r = 1.0f, dec_c = 1.0f;
-      if (ROW || TWO_D) global_scale(amax_row_of(c.seg), s_enc_r, dec_r);
-      if (COL && !TWO_D) global_scale(amax_col_of(c.seg), s_enc_c, dec_c);
-      if (TWO_D) { s_enc_c = s_enc_r; dec_c = dec_r; }
-      for (int idx = lane; idx < kTableEntries; idx += 32) {
-        const float sv = e4m3x2_to_float2((uint16_t)idx).x;
-        tab_row[idx] = element_multiplier(sv, dec_r);
-        tab_col[idx] = element_multiplier(sv, dec_c);
-      }
-      __syncwarp();
-      cur_seg = c.seg;
-    }
+    if (c.seg != cur_seg) set_segment(c.seg);  // uniform across the group
 
     const bool lane_cols = (int64_t)c.n0 + lane * 8 < N;  // all 8 of the lane's columns exist
     // every row of the slab and every column of the tile exist (uniform across the warp)
