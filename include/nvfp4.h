@@ -82,11 +82,13 @@ typedef struct nvfp4_config {
   uint32_t rng_offset;    /* Philox counter word 3 (advance it to draw a new stream) */
   uint64_t rng_seed;      /* Philox key = (low 32 bits, high 32 bits) */
   int32_t fused_amax;     /* when the amax inputs are NULL: 0 = amax pass + quantize pass,
-                             1 = one cooperative launch: every CTA reduces its share of the
-                             amax, they meet at a bounded grid barrier, then quantize (the
-                             re-read of x comes from L2 when x fits there). Fused calls share
-                             the device workspace's barrier: on one device they must not
-                             overlap in time (issue them on one stream). Plain tensors only. */
+                             1 = one cooperative launch: every CTA reduces the tiles it will
+                             quantize, folds its maxima into the workspace with an atomic max,
+                             counts its arrival and waits (bounded) for all CTAs, then
+                             quantizes (the re-read of x comes from L2 when x fits there).
+                             Fused calls share the device workspace's count and maxima: on one
+                             device they must not overlap in time (issue them on one stream).
+                             Plain tensors only. */
   int32_t reserved;       /* must be zero */
 } nvfp4_config;
 
@@ -166,9 +168,9 @@ nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const
  * fixed memory budget. The pages have no counterpart of this entry point; it exists only so
  * that such callers get the single-launch path.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its scratch
- * -- the grid barrier's counters and the partial maxima of up to 1024 CTAs (one CTA per SM),
- * about 8 KiB in all -- is a static device array that every GPU loading this library holds
- * until exit. The caller still passes x and every output.
+ * -- a status word, the CTAs' arrival count and two maxima words, 256 bytes in all -- is a
+ * static device array that every GPU loading this library holds until exit. The caller still
+ * passes x and every output.
  *   Arguments, layouts and shape rules as nvfp4_quantize with amax_row = amax_col = NULL and
  *   cfg->fused_amax = 1 (cfg->fused_amax itself is ignored); M and N must be positive.
  *   The first call on a device looks up the array's device address and prepares the kernels
@@ -176,8 +178,9 @@ nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const
  *   A device whose launch would need more than 1024 CTAs is refused with
  *   NVFP4_ERR_UNSUPPORTED (GB300 launches one CTA per SM, 152).
  *   Every call on a device shares the array: calls that overlap on the GPU race (issue them on
- *   one stream). Each call clears the barrier's arrival count before it launches; the partial
- *   maxima are rewritten by every call. A wait that gives up is recorded in the array's own
+ *   one stream). The array is zero when the library loads; each call tags its maxima with a
+ *   larger epoch than the last call's and knows the arrival count its CTAs must reach, so
+ *   nothing needs clearing between calls. A wait that gives up is recorded in the array's own
  *   status word, which nvfp4_get_status does not read. */
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const nvfp4_config* cfg,
                                     uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,

@@ -1,7 +1,8 @@
 // Single-launch amax for the quantize kernel: every CTA reduces the tiles it is about to
-// quantize (plain and, for the columnwise RHT, transformed maxima), the CTAs meet at a grid
-// barrier, and each reads the per-CTA partials back. These are the reduction and barrier
-// pieces; the tile walk is in the quantize kernel.
+// quantize (plain and, for the columnwise RHT, transformed maxima), folds them into two
+// launch-tagged maxima words with an atomic max, counts its arrival, and waits until every
+// CTA has arrived (a grid barrier that carries the result). These are the reduction and
+// exchange pieces; the tile walk is in the quantize kernel.
 //
 // Page cited: "[nvfp4_training] Optimize CuteDSL kernels for NVFP4 training" (pytorch/ao pull
 // request #4798), "Performance": its pipelines are an amax kernel followed by a quantize
@@ -29,41 +30,39 @@ __device__ __forceinline__ uint32_t cta_max(uint32_t v, volatile uint32_t* red) 
   return r;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
+// Arrival of this CTA (one thread): fold its maxima (16-bit magnitudes) into the launch's two
+// maxima words, then count itself; the release orders the maxima before the count.
+__device__ __forceinline__ void fuse_arrive(uint32_t* ws, uint64_t epoch, uint32_t mr,
+                                            uint32_t mc) {
+  unsigned long long* mx = reinterpret_cast<unsigned long long*>(ws + 2);
+  const unsigned long long vr = (epoch << 16) | mr, vc = (epoch << 16) | mc;
+  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(mx), "l"(vr) : "memory");
+  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(mx + 1), "l"(vc) : "memory");
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws) : "memory");
 }
 
-// Grid barrier for a launch whose CTAs are all resident: one thread per CTA calls it, after
-// its own writes that the other CTAs read. ws[0] counts arrivals; the last arrival resets it
-// and publishes the release by bumping the generation ws[1], which only grows, so the
-// barrier needs no clearing between launches on one stream. Returns false when the wait
-// passed its limit.
-__device__ __forceinline__ bool grid_sync(uint32_t* ws, uint32_t nblocks) {
-  const uint32_t g = ld_acquire_gpu(ws + 1);  // cannot change before this CTA arrives
-  if (atom_add_acq_rel_gpu(ws, 1u) == nblocks - 1) {
-    st_relaxed_gpu(ws, 0u);        // nobody else touches the count until the next launch
-    st_release_gpu(ws + 1, g + 1u);
-    return true;
+// Wait (one thread, bounded) until the arrival count reaches `target`, then read the maxima
+// of every CTA. Returns false when the wait passed its limit or the maxima carry another epoch.
+__device__ __forceinline__ bool fuse_wait(uint32_t* ws, uint32_t target, uint64_t epoch,
+                                          uint32_t& mr, uint32_t& mc) {
+  uint32_t c;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(ws) : "memory");
+  if ((int32_t)(c - target) < 0) {
+    uint64_t t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > kBarrierLimitNs) return false;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(ws) : "memory");
+    } while ((int32_t)(c - target) < 0);
   }
-  uint64_t t0, t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-  while (ld_acquire_gpu(ws + 1) == g) {
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    if (t - t0 > kBarrierLimitNs) return false;
-  }
+  unsigned long long vr, vc;
+  const unsigned long long* mx = reinterpret_cast<const unsigned long long*>(ws + 2);
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(vr) : "l"(mx) : "memory");
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(vc) : "l"(mx + 1) : "memory");
+  if ((vr >> 16) != epoch || (vc >> 16) != epoch) return false;
+  mr = (uint32_t)vr & 0xFFFFu;
+  mc = (uint32_t)vc & 0xFFFFu;
   return true;
 }
 

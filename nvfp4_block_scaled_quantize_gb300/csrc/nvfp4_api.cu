@@ -25,6 +25,8 @@ struct DeviceState {
   bool ready = false;
   int sm_count = 0;
   uint32_t* workspace = nullptr;  // [0] status word
+  uint64_t fuse_epoch = 0;        // epoch of the last single-launch amax on this workspace
+  uint32_t fuse_count = 0;        // the workspace's arrival count after that launch
 };
 
 std::mutex g_mutex;
@@ -259,10 +261,19 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   q.x = x;
   q.fused = fused ? 1 : 0;
   q.fuse_ws = ds->workspace + kFuseWsOffset;
-  const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0};
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
-  return cuda_status(launch_quantize(mode, q, grid, s));
+  const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0};
+  if (!fused) return cuda_status(launch_quantize(mode, q, grid, s));
+  // every CTA adds one to the arrival count; the epoch orders this launch's maxima after all
+  // earlier ones (the workspace starts zeroed: epoch 0, count 0)
+  std::lock_guard<std::mutex> lock(g_mutex);
+  q.fuse_epoch = ds->fuse_epoch + 1;
+  q.fuse_target = ds->fuse_count + (uint32_t)grid;
+  if (launch_quantize(mode, q, grid, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  ds->fuse_epoch = q.fuse_epoch;
+  ds->fuse_count = q.fuse_target;
+  return NVFP4_OK;
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,

@@ -41,10 +41,12 @@ constexpr int kSmemIssued = kSmemFlags + 16;                          // int32 [
 constexpr int kSmemFused = kSmemIssued + 4 * kStages;            // uint32 [32 + 4]
 constexpr int kQuantSmemBytes = kSmemFused + 4 * 36;
 
-// Workspace words used by the single-launch (fused amax) path: a self-resetting grid barrier
-// {arrivals, generation} followed by per-CTA partial maxima (rowwise, then columnwise).
+// Workspace of the single-launch (fused amax) path, 8-byte aligned: word 0 counts CTA arrivals
+// (it only grows; the host knows the value each launch must reach), words 2-3 and 4-5 are the
+// rowwise and columnwise maxima as (launch epoch << 16) | 16-bit magnitude. Epochs increase
+// from launch to launch, so an atomic max needs no clearing in between.
 constexpr int kFuseMaxCtas = 1024;
-constexpr int kFuseWsWords = 2 + 2 * kFuseMaxCtas;
+constexpr int kFuseWsWords = 6;
 
 // Arguments of the quantize kernel: one BF16 tensor split into row segments (one segment for
 // a plain tensor, one per expert for the grouped case).
@@ -69,7 +71,9 @@ struct QuantArgs {
   uint32_t rng_offset;
   uint32_t* status;
   int32_t fused;                    // 1: compute the amax inside this launch (one segment)
-  uint32_t* fuse_ws;                // kFuseWsWords words of zero-initialised workspace
+  uint32_t fuse_target;             // fuse_ws[0] once every CTA of this launch has arrived
+  uint64_t fuse_epoch;              // larger than any earlier launch's on fuse_ws (< 2^48)
+  uint32_t* fuse_ws;                // kFuseWsWords words, 8-byte aligned
 };
 
 // What one quantize launch produces.

@@ -113,7 +113,9 @@ __device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int
   return true;
 }
 
-template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
+// FUSED: the amax is computed inside the launch (a.fused == 1; a cooperative launch of a
+// plain tensor). A template parameter, so that each path is compiled on its own.
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FUSED>
 __global__ void __launch_bounds__(kQuantThreads, 1)
     quantize_tiles_kernel(const __grid_constant__ QuantArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int64_t N = a.cols;
 
   const int stride = gridDim.x;
-  const bool fused = a.fused != 0;
+  constexpr bool fused = FUSED;
   // A plain tensor is one segment: the first loads leave at once, before anything else
   // (the grouped path first needs the segment table below).
   const bool plain = a.offsets == nullptr;
@@ -296,35 +298,24 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     uint32_t mc = mr;
     if (COL && RHT) mc = cta_max(max(mt & 0xFFFFu, mt >> 16), red);
     if (tid == 0) {
-      a.fuse_ws[2 + blockIdx.x] = mr;
-      a.fuse_ws[2 + kFuseMaxCtas + blockIdx.x] = mc;
-      if (!grid_sync(a.fuse_ws, gridDim.x)) {
+      fuse_arrive(a.fuse_ws, a.fuse_epoch, mr, mc);
+      uint32_t pr = 0u, pc = 0u;
+      if (!fuse_wait(a.fuse_ws, a.fuse_target, a.fuse_epoch, pr, pc)) {
         flags[3] = 1;
         atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
       }
-    }
-    __syncthreads();
-    if (flags[3]) flags[0] = flags[1] = flags[2] = 1;  // every group leaves without storing
-    uint32_t pr = 0, pc = 0;
-    const volatile uint32_t* ws = a.fuse_ws;
-    for (int b = tid; b < (int)gridDim.x; b += blockDim.x) {
-      pr = max(pr, ws[2 + b]);
-      pc = max(pc, ws[2 + kFuseMaxCtas + b]);
-    }
-    pr = cta_max(pr, red);
-    pc = cta_max(pc, red);
-    if (tid == 0) {
       fused_amax[0] = __uint_as_float(pr << 16);
       fused_amax[1] = __uint_as_float(pc << 16);
     }
     __syncthreads();
+    if (flags[3]) flags[0] = flags[1] = flags[2] = 1;  // every group leaves without storing
   }
   // amax of segment e (rowwise / columnwise side)
   auto amax_row_of = [&](int e) -> float {
-    return a.fused ? fused_amax[0] : a.amax_row[(int64_t)e * a.amax_row_stride];
+    return FUSED ? fused_amax[0] : a.amax_row[(int64_t)e * a.amax_row_stride];
   };
   auto amax_col_of = [&](int e) -> float {
-    return a.fused ? fused_amax[1] : a.amax_col[(int64_t)e * a.amax_col_stride];
+    return FUSED ? fused_amax[1] : a.amax_col[(int64_t)e * a.amax_col_stride];
   };
   if (blockIdx.x == 0) {  // global scales {amax, S_dec} of every segment
     for (int e = tid; e < E; e += blockDim.x) {
@@ -651,7 +642,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
 cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
-  if (args.fused) {  // the grid barrier needs every CTA resident: a cooperative launch
+  if (args.fused) {  // every CTA waits for all the others: a cooperative launch
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kQuantThreads);
@@ -662,17 +653,21 @@ cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL>,
-                              args);
+    return cudaLaunchKernelEx(
+        &cfg, quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true>, args);
   }
-  quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL>
+  quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false>
       <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
   return cudaGetLastError();
 }
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
 cudaError_t prepare() {
-  return cudaFuncSetAttribute(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL>,
+  cudaError_t e = cudaFuncSetAttribute(
+      quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
 }
 

@@ -2,9 +2,9 @@
 // allocate device memory -- e.g. code running inside a caching allocator's own callbacks, a
 // real-time path that must never reach cudaMalloc (which can synchronize the device), or a
 // host that hands this library a fixed memory budget. The regular entry points allocate a
-// small per-device workspace on their first call; this one keeps its scratch (the grid
-// barrier's counters, the per-CTA partial maxima and a status word) in a file-scope device
-// array instead, so it calls no cudaMalloc, cudaFree or other allocating routine.
+// small per-device workspace on their first call; this one keeps its scratch (a status word,
+// the CTAs' arrival count and the two launch-tagged maxima words) in a file-scope device array
+// instead, so it calls no cudaMalloc, cudaFree or other allocating routine.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -20,12 +20,14 @@
 namespace nvfp4 {
 namespace {
 
-// Scratch of every nvfp4_quantize_noalloc call on a device: word 0 the device status word,
-// words 4 .. 4 + kFuseWsWords the grid barrier {arrivals, generation} and the partial maxima
-// of up to kFuseMaxCtas CTAs (8 KiB in all). Loaded with the library and kept until exit.
+// Scratch of every nvfp4_quantize_noalloc call on a device (64 words, 256 bytes): word 0 the
+// device status word, words 4 .. 4 + kFuseWsWords the arrival count and the maxima words of
+// the single-launch amax. Zero when the library is loaded (epoch 0, count 0) and kept until
+// exit.
 constexpr int kScratchStatus = 0;
 constexpr int kScratchFuse = 4;
-constexpr int kScratchWords = kScratchFuse + kFuseWsWords;
+constexpr int kScratchWords = 64;
+static_assert(kScratchFuse + kFuseWsWords <= kScratchWords, "scratch too small");
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kScratchWords];
 
 constexpr int kMaxDevices = 64;
@@ -34,6 +36,8 @@ struct NoAllocDevice {
   bool ready = false;
   int sm_count = 0;
   uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  uint64_t epoch = 0;           // epoch of the last call on this device
+  uint32_t count = 0;           // the scratch's arrival count after that call
 };
 
 std::mutex g_mutex;
@@ -139,10 +143,15 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   q.status = d->scratch + kScratchStatus;
   q.fused = 1;
   q.fuse_ws = d->scratch + kScratchFuse;
-  // the barrier's arrival count must start at zero (a call that gave up may have left it set);
-  // clearing it is a memset of existing memory, not an allocation
-  if (cudaMemsetAsync(q.fuse_ws, 0, sizeof(uint32_t), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  // each CTA adds one to the arrival count and tags its maxima with a larger epoch than any
+  // earlier call's, so nothing has to be cleared before the launch
+  std::lock_guard<std::mutex> lock(g_mutex);
+  q.fuse_epoch = d->epoch + 1;
+  q.fuse_target = d->count + (uint32_t)grid;
   const QuantMode mode{row, col, rht, two_d, cfg->round_row == NVFP4_ROUND_SR,
                        cfg->round_col == NVFP4_ROUND_SR};
-  return launch_quantize(mode, q, grid, s) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+  if (launch_quantize(mode, q, grid, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  d->epoch = q.fuse_epoch;
+  d->count = q.fuse_target;
+  return NVFP4_OK;
 }
