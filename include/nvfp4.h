@@ -30,9 +30,10 @@
  * error status launched nothing and wrote nothing.
  *
  * Memory: the library allocates no memory on these calls except once per device, on the
- * first call that needs it: a small workspace (status word, grid-barrier state and per-block
- * partial maxima, under 16 KiB) allocated with cudaMalloc and kept until exit. Make that first
- * call outside CUDA-graph capture.
+ * first call that needs it: a small workspace (status word, the single-launch amax's arrival
+ * count and maxima words; 16 KiB) allocated with cudaMalloc and kept until exit. Make that
+ * first call outside CUDA-graph capture. The host pipeline (end of this file) allocates its
+ * device staging when it is created, and nothing when work is submitted.
  */
 #ifndef NVFP4_H
 #define NVFP4_H
@@ -191,6 +192,42 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const n
  * *device_status (NVFP4_DEVICE_* bits). Returns NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT
  * when bits were set, NVFP4_OK otherwise. */
 nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status);
+
+/* Host pipeline: quantization of tensors that live in host memory, with the copies of
+ * consecutive submissions overlapped (the input of one on the host-to-device link while the
+ * outputs of the previous one use the device-to-host direction). Runtime plumbing around
+ * nvfp4_quantize; the pages have no counterpart.
+ * A pipeline owns `depth` (1 to 4) slots of device staging (x and every output of one tensor
+ * of the shape given at creation), three CUDA streams (copy in, compute, copy out) and events.
+ * Submission i uses slot i % depth: copy x in once the slot's previous input has been read,
+ * quantize (nvfp4_quantize on the compute stream, with fused_amax as configured) once the
+ * copy landed and the slot's previous outputs have been copied out, copy the outputs out.
+ * Host buffers should be page-locked (cudaHostAlloc / torch pin_memory): pageable memory
+ * works, without overlap. Host outputs are written in submission order; the caller must not
+ * touch a submission's host buffers until a join has been waited for. One host thread drives
+ * a pipeline at a time. All submissions run on the device that was current at creation. */
+typedef struct nvfp4_host_pipeline nvfp4_host_pipeline;
+
+/* Create a pipeline for BF16 [M][N] tensors quantized with *cfg (copied; the rounding seed
+ * and offset stay fixed for every submission). Allocates the staging with cudaMalloc.
+ * Shape and option rules as nvfp4_quantize, with M, N > 0. *out receives the handle. */
+nvfp4_status nvfp4_host_pipeline_create(int64_t M, int64_t N, const nvfp4_config* cfg,
+                                        int32_t depth, nvfp4_host_pipeline** out);
+
+/* Enqueue one tensor: x_host (host) BF16 [M][N]; outputs (host) as nvfp4_quantize's, NULL for
+ * an orientation the configuration does not produce. The work starts after everything already
+ * enqueued on `stream` (the caller's stream at submission time). Returns without waiting. */
+nvfp4_status nvfp4_host_pipeline_submit(nvfp4_host_pipeline* p, const void* x_host,
+                                        uint8_t* row_codes, uint8_t* row_scales,
+                                        float* row_gscale, uint8_t* col_codes,
+                                        uint8_t* col_scales, float* col_gscale, void* stream);
+
+/* Make `stream` wait (on the device) until every submitted tensor's outputs are in host
+ * memory. Synchronize `stream` (or an event recorded after this call) before reading them. */
+nvfp4_status nvfp4_host_pipeline_join(nvfp4_host_pipeline* p, void* stream);
+
+/* Wait for all submitted work, then free the staging, streams and events. NULL is a no-op. */
+nvfp4_status nvfp4_host_pipeline_destroy(nvfp4_host_pipeline* p);
 
 #ifdef __cplusplus
 }

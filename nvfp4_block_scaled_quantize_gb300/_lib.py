@@ -20,7 +20,9 @@ DEVICE_BAD_OFFSETS = 0x1
 DEVICE_TIMEOUT = 0x2
 
 EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped",
-            "nvfp4_dequantize", "nvfp4_get_status", "nvfp4_quantize_noalloc"]
+            "nvfp4_dequantize", "nvfp4_get_status", "nvfp4_quantize_noalloc",
+            "nvfp4_host_pipeline_create", "nvfp4_host_pipeline_submit",
+            "nvfp4_host_pipeline_join", "nvfp4_host_pipeline_destroy"]
 
 
 class Config(ctypes.Structure):
@@ -81,6 +83,14 @@ def load(build_if_missing: bool = False):
     L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.nvfp4_quantize_noalloc.restype = ctypes.c_int
     L.nvfp4_quantize_noalloc.argtypes = [vp, i64, i64, cfgp, vp, vp, vp, vp, vp, vp, vp]
+    L.nvfp4_host_pipeline_create.restype = ctypes.c_int
+    L.nvfp4_host_pipeline_create.argtypes = [i64, i64, cfgp, i32, ctypes.POINTER(vp)]
+    L.nvfp4_host_pipeline_submit.restype = ctypes.c_int
+    L.nvfp4_host_pipeline_submit.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.nvfp4_host_pipeline_join.restype = ctypes.c_int
+    L.nvfp4_host_pipeline_join.argtypes = [vp, vp]
+    L.nvfp4_host_pipeline_destroy.restype = ctypes.c_int
+    L.nvfp4_host_pipeline_destroy.argtypes = [vp]
     L.nvfp4_get_status.restype = ctypes.c_int
     L.nvfp4_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     _lib = L

@@ -168,3 +168,63 @@ def quantize_from_host(x_host, pinned_out=None, **kw):
     for k, v in out.items():
         pinned_out[k].copy_(v, non_blocking=True)
     return pinned_out
+
+
+class HostPipeline:
+    """nvfp4_host_pipeline_*: quantization of host (pinned) BF16 [M, N] tensors with the copies
+    of consecutive submissions overlapped. The device staging is allocated once, here."""
+
+    def __init__(self, M, N, depth=2, **kw):
+        L = _lib.load()
+        self.M, self.N = M, N
+        self.cfg = make_config(fused_amax=kw.pop("fused_amax", True), **kw)
+        self.rowwise = bool(self.cfg.rowwise)
+        self.columnwise = bool(self.cfg.columnwise)
+        self.device = torch.device("cuda", torch.cuda.current_device())
+        handle = ctypes.c_void_p()
+        _raise_if(L.nvfp4_host_pipeline_create(M, N, ctypes.byref(self.cfg), depth,
+                                               ctypes.byref(handle)), "nvfp4_host_pipeline_create")
+        self._h = handle
+
+    def alloc_host_outputs(self):
+        """Pinned host tensors for one submission's outputs."""
+        out = {}
+        M, N = self.M, self.N
+        if self.rowwise:
+            out["row_codes"] = torch.empty((M, N // 2), dtype=torch.uint8, pin_memory=True)
+            out["row_scales"] = torch.empty((M, N // 16), dtype=torch.uint8, pin_memory=True)
+            out["row_gscale"] = torch.empty(2, dtype=torch.float32, pin_memory=True)
+        if self.columnwise:
+            out["col_codes"] = torch.empty((N, M // 2), dtype=torch.uint8, pin_memory=True)
+            out["col_scales"] = torch.empty((N, M // 16), dtype=torch.uint8, pin_memory=True)
+            out["col_gscale"] = torch.empty(2, dtype=torch.float32, pin_memory=True)
+        return out
+
+    def submit(self, x_host, out_host):
+        """Enqueue x_host (pinned BF16 [M, N]); outputs land in out_host (alloc_host_outputs)."""
+        if x_host.device.type != "cpu" or x_host.dtype != torch.bfloat16 or \
+                tuple(x_host.shape) != (self.M, self.N) or not x_host.is_contiguous():
+            raise ValueError("x_host must be a contiguous CPU bfloat16 [%d, %d] tensor"
+                             % (self.M, self.N))
+        L = _lib.load()
+        p = lambda k: ctypes.c_void_p(out_host[k].data_ptr()) if k in out_host else None
+        _raise_if(L.nvfp4_host_pipeline_submit(
+            self._h, ctypes.c_void_p(x_host.data_ptr()), p("row_codes"), p("row_scales"),
+            p("row_gscale"), p("col_codes"), p("col_scales"), p("col_gscale"),
+            _stream(self.device)), "nvfp4_host_pipeline_submit")
+
+    def join(self):
+        """Make the current stream wait until every submission's outputs are in host memory."""
+        _raise_if(_lib.load().nvfp4_host_pipeline_join(self._h, _stream(self.device)),
+                  "nvfp4_host_pipeline_join")
+
+    def close(self):
+        if self._h:
+            _lib.load().nvfp4_host_pipeline_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -94,3 +94,20 @@ def test_grouped_and_dequant_argument_checks(L):
     assert L.nvfp4_dequantize(p(FAKE), p(FAKE), p(FAKE), 4, 32, p(FAKE + 4), None) == 3
     assert L.nvfp4_amax(p(FAKE), 16, 32, ctypes.byref(cfg), None, None, None) == 1
     assert L.nvfp4_get_status(None, None) == 1
+
+
+def test_host_pipeline_argument_checks_return_before_any_cuda_call(L):
+    h = ctypes.c_void_p()
+    create = lambda M, N, c, depth: L.nvfp4_host_pipeline_create(M, N, ctypes.byref(c), depth,
+                                                                 ctypes.byref(h))
+    assert create(64, 64, _cfg(), 0) == 1                       # depth below 1
+    assert create(64, 64, _cfg(), 5) == 1                       # depth above 4
+    assert create(64, 64, _cfg(reserved=1), 2) == 1
+    assert create(64, 64, _cfg(rowwise=0), 2) == 4              # nothing selected
+    assert create(0, 64, _cfg(), 2) == 2                        # empty
+    assert create(64, 24, _cfg(), 2) == 2                       # N % 16
+    assert create(24, 64, _cfg(columnwise=1), 2) == 2           # M % 16 with columnwise
+    assert L.nvfp4_host_pipeline_create(64, 64, None, 2, ctypes.byref(h)) == 1
+    assert L.nvfp4_host_pipeline_submit(None, ctypes.c_void_p(FAKE), *([None] * 7)) == 1
+    assert L.nvfp4_host_pipeline_join(None, None) == 1
+    assert L.nvfp4_host_pipeline_destroy(None) == 0

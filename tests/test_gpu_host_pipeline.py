@@ -1,0 +1,84 @@
+"""nvfp4_host_pipeline_*: host tensors in, host outputs out, copies of consecutive submissions
+overlapped. Every submission's host outputs must equal nvfp4_quantize's on the device copy of
+the same input, bit for bit, whatever the depth and however the slots are reused."""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_block_scaled_quantize_gb300 import api, workloads
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [
+    ("rowcol_rtne", dict(rowwise=True, columnwise=True)),
+    ("row_rtne_col_rht_sr", dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x3C5A,
+                                 round_col="sr", seed=17)),
+    ("col_only_two_pass", dict(rowwise=False, columnwise=True, fused_amax=False)),
+]
+
+
+def _same(a, b, what):
+    a, b = a.cpu().numpy(), b.cpu().numpy()
+    if a.dtype == np.float32:
+        a, b = a.view(np.uint32), b.view(np.uint32)
+    assert np.array_equal(a, b), what
+
+
+@pytest.mark.parametrize("depth", [1, 2, 3])
+@pytest.mark.parametrize("name,kw", CONFIGS, ids=[c[0] for c in CONFIGS])
+def test_pipeline_outputs_match_device_quantize(depth, name, kw):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M, N = 320, 1040   # ragged against the 64 x 256 tiles
+    xs = [workloads.normal_with_outliers(M, N, seed=s, fraction=0.003, gain=30.0).pin_memory()
+          for s in (11, 12, 13)]
+    pipe = api.HostPipeline(M, N, depth=depth, **kw)
+    try:
+        outs = []
+        for i in range(5):   # more submissions than slots: every slot is reused
+            o = pipe.alloc_host_outputs()
+            for v in o.values():
+                v.fill_(0x77 if v.dtype == torch.uint8 else float("nan"))
+            pipe.submit(xs[i % 3], o)
+            outs.append(o)
+        pipe.join()
+        torch.cuda.synchronize()
+        dkw = dict(kw)
+        dkw.pop("fused_amax", None)
+        for i, o in enumerate(outs):
+            ref = api.nvfp4_quantize(xs[i % 3].cuda(), **dkw)
+            assert sorted(o) == sorted(ref)
+            for k in ref:
+                _same(o[k], ref[k], "%s depth %d submission %d %s" % (name, depth, i, k))
+    finally:
+        pipe.close()
+
+
+def test_pipeline_reused_host_buffers_hold_the_last_submission():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M, N = 256, 512
+    xs = [workloads.normal(M, N, 1.0, s).pin_memory() for s in (3, 4)]
+    pipe = api.HostPipeline(M, N, depth=2, rowwise=True, columnwise=True)
+    try:
+        o = pipe.alloc_host_outputs()
+        for i in range(7):
+            pipe.submit(xs[i % 2], o)
+        pipe.join()
+        torch.cuda.synchronize()
+        ref = api.nvfp4_quantize(xs[0].cuda(), rowwise=True, columnwise=True)
+        for k in ref:
+            _same(o[k], ref[k], k)
+    finally:
+        pipe.close()
+
+
+def test_pipeline_rejects_wrong_host_tensor():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pipe = api.HostPipeline(64, 64, depth=1, rowwise=True)
+    try:
+        with pytest.raises(ValueError):
+            pipe.submit(torch.zeros((64, 32), dtype=torch.bfloat16), pipe.alloc_host_outputs())
+    finally:
+        pipe.close()
