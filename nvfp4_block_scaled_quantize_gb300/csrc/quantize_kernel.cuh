@@ -33,13 +33,14 @@ namespace qk {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: no TMA load takes this long
 
 struct Coord {
-  int32_t row0;    // first row of the tile in x
-  int32_t nrows;   // rows of the tile inside its segment (<= kTileM)
+  int32_t row0;    // first row of the tile in x (negative rows read as zeros)
+  int32_t nrows;   // rows from row0 to the end of the tile's segment, at most kTileM
   int32_t n0;      // first column
-  int32_t colpos;  // first column of the tile in the columnwise outputs
+  int32_t colpos;  // first column of the tile in the columnwise outputs (a multiple of kTileM)
   int32_t seg;
   int32_t tile;    // the tile these coordinates belong to (checked by the consumers)
-  int32_t pad1, pad2;
+  int32_t skip;    // leading 16-row slabs that lie before the segment (its first tile only)
+  int32_t pad;
 };
 
 // XOR swizzle of 16-byte chunks inside each 128-byte row of the columnwise code staging.
@@ -153,14 +154,16 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     }
     const int local = tile - seg_tile0[lo];
     const int mt = local / tiles_n;
+    const int lead = COL ? (seg_col0[lo] & (kTileM - 1)) : 0;  // see the segment table
     Coord c;
     c.n0 = (local - mt * tiles_n) * kTileN;
-    c.row0 = seg_start[lo] + mt * kTileM;
+    c.row0 = seg_start[lo] - lead + mt * kTileM;
     c.nrows = min(kTileM, seg_end[lo] - c.row0);
-    c.colpos = seg_col0[lo] + mt * kTileM;
+    c.colpos = seg_col0[lo] - lead + mt * kTileM;
     c.seg = lo;
     c.tile = tile;
-    c.pad1 = c.pad2 = 0;
+    c.skip = mt == 0 ? lead / 16 : 0;
+    c.pad = 0;
     coords[s] = c;
     __threadfence_block();
     issued[s] = issued[s] + 1;  // the stage's next mbarrier phase is this load's
@@ -211,18 +214,28 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       for (int c0 = 0; c0 < E; c0 += 32) {
         const int e = c0 + lane;
         const int32_t n = (e < E && !flags[3]) ? seg_end[e] - seg_start[e] : 0;
-        const int32_t t0 = ((n + kTileM - 1) / kTileM) * tiles_n;
         const int32_t p0 = ((n + 15) / 16) * 16;
-        int32_t t = t0, p = p0;
+        int32_t p = p0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int32_t pu = __shfl_up_sync(0xFFFFFFFFu, p, d);
+          if (lane >= d) p += pu;
+        }
+        const int32_t col0 = col_base + p - p0;
+        // With columnwise outputs a segment's tiles start lead = col0 % kTileM rows before it,
+        // so that every tile's columnwise position is a multiple of kTileM (whole 32-byte
+        // column runs); the lead rows are whole slabs, skipped by the consumers.
+        const int32_t lead = COL ? (col0 & (kTileM - 1)) : 0;
+        const int32_t t0 = n > 0 ? ((n + lead + kTileM - 1) / kTileM) * tiles_n : 0;
+        int32_t t = t0;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
           const int32_t tu = __shfl_up_sync(0xFFFFFFFFu, t, d);
-          const int32_t pu = __shfl_up_sync(0xFFFFFFFFu, p, d);
-          if (lane >= d) { t += tu; p += pu; }
+          if (lane >= d) t += tu;
         }
         if (e < E) {
           seg_tile0[e] = tile_base + t - t0;
-          seg_col0[e] = col_base + p - p0;
+          seg_col0[e] = col0;
         }
         tile_base += __shfl_sync(0xFFFFFFFFu, t, 31);
         col_base += __shfl_sync(0xFFFFFFFFu, p, 31);
@@ -393,7 +406,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       flags[g] = 1;
       if (lane == 0) atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
     }
-    const int slab_rows = min(16, c.nrows - 16 * rb);
+    const int slab_rows = rb < c.skip ? 0 : min(16, c.nrows - 16 * rb);
     uint4 v[16];
     if (slab_rows > 0) {
       const uint32_t src = smem_u32(smem + kSmemStages + s * kStageBytes) +
@@ -587,11 +600,12 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         uint8_t* dst0 = a.col_codes + col0 * (a.col_ld / 2) + c.colpos / 2;
         uint8_t* dst1 = dst0 + a.col_ld / 2;
         const uintptr_t dbits = reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1);
-        if (nrb == kWarpsPerGroup && (dbits & 31) == 0) {
+        const bool whole = nrb == kWarpsPerGroup && c.skip == 0;  // all four slabs are ours
+        if (whole && (dbits & 31) == 0) {
           // each column's 64 codes are one full 32-byte sector: one store per column
           stg256(dst0, make_uint4(d[0].x, d[0].y, d[1].x, d[1].y), make_uint4(d[2].x, d[2].y, d[3].x, d[3].y));
           stg256(dst1, make_uint4(d[0].z, d[0].w, d[1].z, d[1].w), make_uint4(d[2].z, d[2].w, d[3].z, d[3].w));
-        } else if (nrb == kWarpsPerGroup && (dbits & 15) == 0) {
+        } else if (whole && (dbits & 15) == 0) {
           reinterpret_cast<uint4*>(dst0)[0] = make_uint4(d[0].x, d[0].y, d[1].x, d[1].y);
           reinterpret_cast<uint4*>(dst0)[1] = make_uint4(d[2].x, d[2].y, d[3].x, d[3].y);
           reinterpret_cast<uint4*>(dst1)[0] = make_uint4(d[0].z, d[0].w, d[1].z, d[1].w);
@@ -599,7 +613,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         } else {
 #pragma unroll
           for (int r = 0; r < kWarpsPerGroup; r++) {
-            if (r < nrb) {
+            if (r >= c.skip && r < nrb) {
               *reinterpret_cast<uint2*>(dst0 + 8 * r) = make_uint2(d[r].x, d[r].y);
               *reinterpret_cast<uint2*>(dst1 + 8 * r) = make_uint2(d[r].z, d[r].w);
             }
@@ -616,11 +630,11 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         }
         uint8_t* sd0 = a.col_scales + col0 * col_nb + c.colpos / 16;
         uint8_t* sd1 = sd0 + col_nb;
-        if (nrb == kWarpsPerGroup && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
+        if (whole && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
           *reinterpret_cast<uint32_t*>(sd0) = sc0;
           *reinterpret_cast<uint32_t*>(sd1) = sc1;
         } else {
-          for (int r = 0; r < nrb; r++) {
+          for (int r = c.skip; r < nrb; r++) {
             sd0[r] = (uint8_t)(sc0 >> (8 * r));
             sd1[r] = (uint8_t)(sc1 >> (8 * r));
           }
