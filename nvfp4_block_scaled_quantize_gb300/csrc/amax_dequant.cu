@@ -126,17 +126,19 @@ __global__ void __launch_bounds__(256, 2) amax_blocks_kernel(const AmaxArgs a) {
       w0[i] = v.x;
       w1[i] = v.y;
     }
-    uint32_t m = 0;
+    // max.xorsign.abs tree: exact magnitudes, sign bits cleared at the end (finite inputs)
+    uint32_t t[16];
 #pragma unroll
-    for (int i = 0; i < 16; i++) m = vmax2(m, vmax2(abs2(w0[i]), abs2(w1[i])));
+    for (int i = 0; i < 16; i++) t[i] = hmax_abs2(w0[i], w1[i]);
+#pragma unroll
+    for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+      for (int i = 0; i < h; i++) t[i] = hmax_abs2(t[i], t[i + h]);
+    const uint32_t m = t[0] & 0x7FFF7FFFu;
     const uint32_t mr = max(m & 0xFFFFu, m >> 16);
     uint32_t mc = mr;
     if (RHT) {
-      rht16_pair(w0, a.sign_mask);
-      rht16_pair(w1, a.sign_mask);
-      uint32_t mt = 0;
-#pragma unroll
-      for (int i = 0; i < 16; i++) mt = vmax2(mt, vmax2(abs2(w0[i]), abs2(w1[i])));
+      const uint32_t mt = vmax2(rht16_pair_absmax(w0, a.sign_mask), rht16_pair_absmax(w1, a.sign_mask));
       mc = max(mt & 0xFFFFu, mt >> 16);
     }
     if (mr) atomicMax(&seg_max_row[lo], mr);

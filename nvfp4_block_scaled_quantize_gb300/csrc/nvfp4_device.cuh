@@ -138,6 +138,43 @@ __device__ __forceinline__ float element_multiplier(float s, float s_dec) {
   return (p == 0.0f) ? 0.0f : r;
 }
 
+// Largest |bf16(0.25 * (H16 (d . v))_i)| over the 16 outputs of each of the two columns of w
+// (rht16_pair's outputs), as BF16 magnitude bits (column 0 in the low half). Scaling by 0.25
+// and rounding to BF16 are both monotone, so the maximum of the rounded outputs is the rounded
+// maximum of the unrounded ones: the maximum is taken in FP32 straight after the last
+// butterfly stage, and only it is scaled and rounded.
+__device__ __forceinline__ uint32_t rht16_pair_absmax(const uint32_t (&w)[16], uint32_t sign_mask) {
+  uint64_t x[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    uint32_t flip = ((sign_mask >> i) & 1u) ? 0x80008000u : 0u;
+    x[i] = f2_from_bf16x2(w[i] ^ flip);
+  }
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      if ((i & h) == 0) {
+        uint64_t a = x[i], b = x[i + h];
+        x[i] = f2_add(a, b);
+        x[i + h] = f2_sub(a, b);
+      }
+    }
+  }
+  float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const float2 s = f2_unpack(f2_add(x[i], x[i + 8]));
+    const float2 d = f2_unpack(f2_sub(x[i], x[i + 8]));
+    m0 = fmaxf(m0, fmaxf(fabsf(s.x), fabsf(d.x)));
+    m1 = fmaxf(m1, fmaxf(fabsf(s.y), fabsf(d.y)));
+  }
+  const float2 q = f2_unpack(f2_mul(f2_pack(m0, m1), f2_pack(0.25f, 0.25f)));
+  uint32_t packed;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(q.y), "f"(q.x));
+  return packed & 0x7FFF7FFFu;
+}
+
 // ------------------------------------------------------------------------------------------
 // E2M1 conversion. Codes are packed two per byte with the even element in the low nibble.
 // ------------------------------------------------------------------------------------------

@@ -296,8 +296,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           uint32_t w[16];
 #pragma unroll
           for (int r = 0; r < 16; r++) w[r] = comp(v[r], c4);
-          rht16_pair(w, a.sign_mask);
-          mt = vmax2(mt, tree_max16(w));  // both sign-cleared
+          mt = vmax2(mt, rht16_pair_absmax(w, a.sign_mask));  // both sign-cleared
         }
       }
     }
