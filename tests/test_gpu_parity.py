@@ -262,6 +262,9 @@ GROUPED_CASES = [
     ("odd_counts", 203, 272, [5, 5, 37, 37, 70, 150, 203]),
     ("zero_experts_and_tail", 300, 64, [0, 0, 17, 17, 129, 250]),
     ("many_small", 260, 32, list(np.cumsum([1, 2, 3, 15, 16, 17, 31, 33, 0, 64, 65, 13]))),
+    # column starts 16, 48, 96 (lead slabs of 16, 48, 32 rows before the next expert's tiles)
+    # followed by experts long enough for whole, aligned 64-row tiles
+    ("lead_slabs", 700, 512, list(np.cumsum([16, 200, 32, 150, 48, 200, 1, 53]))),
 ]
 
 
