@@ -45,18 +45,22 @@ __device__ __forceinline__ void block_max_out(uint32_t v, float* out0, float* ou
   }
 }
 
-// max |x| over a contiguous BF16 buffer of nvec 16-byte vectors.
-__global__ void __launch_bounds__(256) amax_flat_kernel(const uint4* __restrict__ x, int64_t nvec,
-                                                        float* out0, float* out1) {
+// max |x| over a contiguous BF16 buffer of nvec 16-byte vectors. Four CTAs of 256 threads per
+// SM, each thread with kFlatUnroll independent 16-byte loads in flight (128 KiB per SM).
+constexpr int kFlatUnroll = 8;
+__global__ void __launch_bounds__(256, 4) amax_flat_kernel(const uint4* __restrict__ x, int64_t nvec,
+                                                           float* out0, float* out1) {
   uint32_t m = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    const uint4 a = ldg_stream(x + i), b = ldg_stream(x + i + stride);
-    const uint4 c = ldg_stream(x + i + 2 * stride), d = ldg_stream(x + i + 3 * stride);
-    m = vmax2(m, vmax2(vmax2(max4(a), max4(b)), vmax2(max4(c), max4(d))));
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
+       i += kFlatUnroll * stride) {
+    uint4 v[kFlatUnroll];
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; u++)
+      v[u] = (i + u * stride < nvec) ? ldg_stream(x + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < kFlatUnroll; u++) m = vmax2(m, max4(v[u]));
   }
-  for (; i < nvec; i += stride) m = vmax2(m, max4(ldg_stream(x + i)));
   block_max_out(max(m & 0xFFFFu, m >> 16), out0, out1);
 }
 

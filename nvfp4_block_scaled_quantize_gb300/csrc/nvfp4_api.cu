@@ -127,6 +127,14 @@ namespace {
 
 nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
+// One wave of the flat amax kernel (four 256-thread CTAs per SM), fewer for small tensors.
+int amax_flat_grid(const DeviceState* st, int64_t nvec) {
+  int64_t g = (nvec + 2047) / 2048;
+  const int64_t cap = (int64_t)st->sm_count * 4;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : (int)g;
+}
+
 int amax_grid(const DeviceState* st, int64_t work_items, int per_block) {
   int64_t g = (work_items + per_block - 1) / per_block;
   int64_t cap = (int64_t)st->sm_count * 8;
@@ -176,7 +184,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_amax(const void* x, int64_t M, int64_t N, const 
     a.stride_row = 2; a.stride_col = 2; a.status = ds->workspace;
     return cuda_status(launch_amax_blocks(true, a, amax_grid(ds, (M / 16) * (N / 4), 256), s));
   }
-  return cuda_status(launch_amax_flat(x, M * N, amax_row, amax_col, amax_grid(ds, M * N / 8, 1024), s));
+  return cuda_status(launch_amax_flat(x, M * N, amax_row, amax_col, amax_flat_grid(ds, M * N / 8), s));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
@@ -240,7 +248,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
         return NVFP4_ERR_CUDA;
     } else {
       if (launch_amax_flat(x, M * N, need_row_amax ? row_amax_slot : nullptr,
-                           need_col_amax ? col_gscale : nullptr, amax_grid(ds, M * N / 8, 1024),
+                           need_col_amax ? col_gscale : nullptr, amax_flat_grid(ds, M * N / 8),
                            s) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     }
