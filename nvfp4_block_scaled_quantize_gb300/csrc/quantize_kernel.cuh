@@ -98,6 +98,32 @@ __device__ __forceinline__ uint32_t e2m1x8(float t0, float t1, float t2, float t
   return d;
 }
 
+// Transpose of an 8 x 8 block of 4-bit codes: on entry w[i] holds row i (nibble j = column
+// j), on exit w[j] holds column j (nibble i = row i). Swaps 4x4, then 2x2, then single-nibble
+// blocks (byte permutes, then masks).
+__device__ __forceinline__ void transpose_nibbles8(uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const uint32_t a = w[i], b = w[i + 4];
+    w[i] = __byte_perm(a, b, 0x5410);
+    w[i + 4] = __byte_perm(a, b, 0x7632);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    if ((i & 2) == 0) {
+      const uint32_t a = w[i], b = w[i + 2];
+      w[i] = __byte_perm(a, b, 0x6240);
+      w[i + 2] = __byte_perm(a, b, 0x7351);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const uint32_t a = w[i], b = w[i + 1];
+    w[i] = (a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u);
+    w[i + 1] = ((a >> 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u);
+  }
+}
+
 // Bounded wait until at least `count` loads have been issued into stage s (a monotonic
 // per-stage count). Only then does the mbarrier parity of load count - 1 name its phase
 // unambiguously: the previous load of the stage has been consumed, so its phase is complete.
@@ -120,6 +146,8 @@ template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bo
 __global__ void __launch_bounds__(kQuantThreads, 1)
     quantize_tiles_kernel(const __grid_constant__ QuantArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  // 2D with both orientations: the columnwise codes are the rowwise codes transposed
+  constexpr bool kRowCol2D = ROW && COL && TWO_D;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -453,6 +481,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         tile_r = tab_row[tile_s];
       }
 
+      uint32_t tcode[kRowCol2D ? 16 : 1];  // 2D row+col: the slab's row codes, then transposed
       // ---------------- rowwise: 1x16 blocks, a lane pair per block ----------------
       if (ROW) {
         // Rows 4q, 4q+1 belong to the even lane of the pair, 4q+2, 4q+3 to the odd lane: the
@@ -519,10 +548,16 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         };
         uint8_t* rowp = a.row_codes + row_g0 * (N / 2) + c.n0 / 2 + lane * 4;
         uint8_t* rsp = a.row_scales + row_g0 * row_nb + c.n0 / 16 + kb + (odd ? 2 : 0) * row_nb;
+        if (kRowCol2D) {
+          // 2D: the columnwise codes are these codes transposed (one multiplier per 16x16
+          // tile, the same in both orientations), so keep all 16 rows
+#pragma unroll
+          for (int r = 0; r < 16; r++) tcode[r] = row_code(r);
+        }
         if (full_slab) {
 #pragma unroll
           for (int r = 0; r < 16; r++)
-            *reinterpret_cast<uint32_t*>(rowp + (int64_t)r * (N / 2)) = row_code(r);
+            *reinterpret_cast<uint32_t*>(rowp + (int64_t)r * (N / 2)) = kRowCol2D ? tcode[r] : row_code(r);
 #pragma unroll
           for (int q = 0; q < 4; q++) {
             rsp[(int64_t)(4 * q) * row_nb] = (uint8_t)(own_s[q] & 0xFFu);
@@ -531,7 +566,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         } else if (lane_cols) {
 #pragma unroll
           for (int r = 0; r < 16; r++)
-            if (r < slab_rows) *reinterpret_cast<uint32_t*>(rowp + (int64_t)r * (N / 2)) = row_code(r);
+            if (r < slab_rows)
+              *reinterpret_cast<uint32_t*>(rowp + (int64_t)r * (N / 2)) = kRowCol2D ? tcode[r] : row_code(r);
 #pragma unroll
           for (int q = 0; q < 4; q++) {
             const int r0 = 4 * q + (odd ? 2 : 0);
@@ -542,7 +578,18 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       }
 
       // ---------------- columnwise: one lane-local block per column, two columns at a time --------
-      if (COL) {
+      if (COL && kRowCol2D) {
+        // rows 0..7 and 8..15 of the lane's 8 columns: two 8 x 8 nibble transposes
+        transpose_nibbles8(tcode);
+        transpose_nibbles8(tcode + 8);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          *reinterpret_cast<uint4*>(cc_stage + rb * (kTileN * 8) + swz(4 * lane + k) * 16) =
+              make_uint4(tcode[2 * k], tcode[8 + 2 * k], tcode[2 * k + 1], tcode[8 + 2 * k + 1]);
+        const uint32_t s4 = tile_s * 0x01010101u;  // the tile scale for all four column pairs
+        *reinterpret_cast<uint2*>(cs_stage + rb * kTileN + lane * 8) = make_uint2(s4, s4);
+      }
+      if (COL && !kRowCol2D) {
         uint32_t csc[2] = {0u, 0u};
 #pragma unroll
         for (int k = 0; k < 4; k++) {
