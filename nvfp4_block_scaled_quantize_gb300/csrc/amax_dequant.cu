@@ -1,4 +1,5 @@
-// Amax kernels and dequantization.
+// The flat amax kernel (plain tensors without the RHT) and dequantization. The per-segment
+// and RHT amax run through the tile kernel (amax_pass.cu).
 //
 // Page cited: "[nvfp4_training] Optimize CuteDSL kernels for NVFP4 training" (pytorch/ao pull
 // request #4798): the amax pre-pass ("Optimization" item 5: "Linear RHT amax"; "Performance":
@@ -14,12 +15,6 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint2 ldg_stream8(const uint2* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
 
@@ -64,101 +59,6 @@ __global__ void __launch_bounds__(256, 4) amax_flat_kernel(const uint4* __restri
   block_max_out(max(m & 0xFFFFu, m >> 16), out0, out1);
 }
 
-// Per-segment maxima over 16-row x 4-column items. Each item's 16 rows are one columnwise
-// block of its segment (zero-padded past the segment's end); with RHT the transformed block's
-// maximum goes to amax_col, the plain maximum to amax_row (and to amax_col without RHT).
-template <bool RHT>
-__global__ void __launch_bounds__(256, 2) amax_blocks_kernel(const AmaxArgs a) {
-  __shared__ int32_t seg_start[kMaxSegments], seg_end[kMaxSegments], seg_blk0[kMaxSegments + 1];
-  __shared__ uint32_t seg_max_row[kMaxSegments], seg_max_col[kMaxSegments];
-  __shared__ int bad;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int E = a.segments;
-  if (tid == 0) bad = 0;
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    int32_t start = (a.offsets == nullptr || e == 0) ? 0 : a.offsets[e - 1];
-    int32_t end = (a.offsets == nullptr) ? (int32_t)a.rows : a.offsets[e];
-    if (start < 0 || end < start || (int64_t)end > a.rows) bad = 1;
-    seg_start[e] = start;
-    seg_end[e] = end;
-    seg_max_row[e] = 0u;
-    seg_max_col[e] = 0u;
-  }
-  __syncthreads();
-  if (bad) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(a.status, 1u);  // NVFP4_DEVICE_BAD_OFFSETS
-    return;
-  }
-  if (tid < 32) {
-    int32_t base = 0;
-    for (int c0 = 0; c0 < E; c0 += 32) {
-      const int e = c0 + lane;
-      const int32_t nb = (e < E) ? (seg_end[e] - seg_start[e] + 15) / 16 : 0;
-      int32_t v = nb;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        int32_t u = __shfl_up_sync(0xFFFFFFFFu, v, d);
-        if (lane >= d) v += u;
-      }
-      if (e < E) seg_blk0[e] = base + v - nb;
-      base += __shfl_sync(0xFFFFFFFFu, v, 31);
-    }
-    if (lane == 0) seg_blk0[E] = base;
-  }
-  __syncthreads();
-
-  const int64_t chunks = a.cols / 4;
-  const int64_t items = (int64_t)seg_blk0[E] * chunks;
-  const uint2* x = reinterpret_cast<const uint2*>(a.x);
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + tid; it < items;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t blk = (int32_t)(it / chunks);
-    const int64_t ch = it - (int64_t)blk * chunks;
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (seg_blk0[mid] <= blk) lo = mid; else hi = mid;
-    }
-    const int64_t r0 = seg_start[lo] + 16 * (int64_t)(blk - seg_blk0[lo]);
-    const int64_t left = seg_end[lo] - r0;
-    const int valid = left < 16 ? (int)left : 16;
-    uint32_t w0[16], w1[16];
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-      const uint2 v = (i < valid) ? ldg_stream8(x + (r0 + i) * chunks + ch) : make_uint2(0, 0);
-      w0[i] = v.x;
-      w1[i] = v.y;
-    }
-    // max.xorsign.abs tree: exact magnitudes, sign bits cleared at the end (finite inputs)
-    uint32_t t[16];
-#pragma unroll
-    for (int i = 0; i < 16; i++) t[i] = hmax_abs2(w0[i], w1[i]);
-#pragma unroll
-    for (int h = 8; h >= 1; h >>= 1)
-#pragma unroll
-      for (int i = 0; i < h; i++) t[i] = hmax_abs2(t[i], t[i + h]);
-    const uint32_t m = t[0] & 0x7FFF7FFFu;
-    const uint32_t mr = max(m & 0xFFFFu, m >> 16);
-    uint32_t mc = mr;
-    if (RHT) {
-      const uint32_t mt = vmax2(rht16_pair_absmax(w0, a.sign_mask), rht16_pair_absmax(w1, a.sign_mask));
-      mc = max(mt & 0xFFFFu, mt >> 16);
-    }
-    if (mr) atomicMax(&seg_max_row[lo], mr);
-    if (mc) atomicMax(&seg_max_col[lo], mc);
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    if (a.amax_row && seg_max_row[e])
-      atomicMax(reinterpret_cast<unsigned int*>(a.amax_row + (int64_t)e * a.stride_row),
-                seg_max_row[e] << 16);
-    if (a.amax_col && seg_max_col[e])
-      atomicMax(reinterpret_cast<unsigned int*>(a.amax_col + (int64_t)e * a.stride_col),
-                seg_max_col[e] << 16);
-  }
-}
-
 // E2M1 code -> value (exact).
 __device__ __forceinline__ float e2m1_value(uint32_t nib) {
   const uint32_t c = nib & 7u;
@@ -198,12 +98,6 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint8_t* __restri
 cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float* out1, int grid,
                              cudaStream_t s) {
   amax_flat_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n_elems / 8, out0, out1);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_amax_blocks(bool rht, const AmaxArgs& args, int grid, cudaStream_t s) {
-  if (rht) amax_blocks_kernel<true><<<grid, 256, 0, s>>>(args);
-  else amax_blocks_kernel<false><<<grid, 256, 0, s>>>(args);
   return cudaGetLastError();
 }
 

@@ -120,6 +120,7 @@ cudaError_t prepare_quantize_kernels() {
   if ((r = prepare_quantize_rowcol()) != cudaSuccess) e = r;
   if ((r = prepare_quantize_rowcol_rht()) != cudaSuccess) e = r;
   if ((r = prepare_quantize_2d()) != cudaSuccess) e = r;
+  if ((r = prepare_amax_tiles()) != cudaSuccess) e = r;
   return e;
 }
 
@@ -140,6 +141,27 @@ int amax_grid(const DeviceState* st, int64_t work_items, int per_block) {
   int64_t cap = (int64_t)st->sm_count * 8;
   if (g > cap) g = cap;
   return g < 1 ? 1 : (int)g;
+}
+
+// The amax pass through the tile kernel: per segment (offsets, or one segment when null)
+// max |x| into amax_row[e * stride] and max |x| or the RHT amax into amax_col[e * stride],
+// both zeroed by the caller.
+nvfp4_status amax_tiles(const DeviceState* ds, const void* x, int64_t rows, int64_t cols,
+                        const int32_t* offsets, int32_t segments, uint32_t sign_mask, bool rht,
+                        float* amax_row, float* amax_col, int32_t stride, cudaStream_t s) {
+  QuantArgs q;
+  std::memset(&q, 0, sizeof q);
+  nvfp4_status st = make_tensor_map(&q.tmap, x, rows, cols);
+  if (st != NVFP4_OK) return st;
+  q.x = x; q.rows = rows; q.cols = cols; q.offsets = offsets; q.segments = segments;
+  q.sign_mask = sign_mask;
+  q.amax_row = amax_row; q.amax_col = amax_col;
+  q.amax_row_stride = stride; q.amax_col_stride = stride;
+  q.status = ds->workspace;
+  const int64_t tiles =
+      ((rows + kTileM - 1) / kTileM + (offsets ? segments : 0)) * ((cols + kTileN - 1) / kTileN);
+  const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
+  return cuda_status(launch_amax_tiles(rht, q, grid, s));
 }
 
 }  // namespace
@@ -177,13 +199,8 @@ NVFP4_EXPORT nvfp4_status nvfp4_amax(const void* x, int64_t M, int64_t N, const 
   if (amax_row && cudaMemsetAsync(amax_row, 0, 4, s) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (amax_col && cudaMemsetAsync(amax_col, 0, 4, s) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (M * N == 0) return NVFP4_OK;
-  if (cfg->rht_col && amax_col) {
-    AmaxArgs a{};
-    a.x = x; a.rows = M; a.cols = N; a.offsets = nullptr; a.segments = 1;
-    a.sign_mask = cfg->rht_sign_mask; a.amax_row = amax_row; a.amax_col = amax_col;
-    a.stride_row = 2; a.stride_col = 2; a.status = ds->workspace;
-    return cuda_status(launch_amax_blocks(true, a, amax_grid(ds, (M / 16) * (N / 4), 256), s));
-  }
+  if (cfg->rht_col && amax_col)
+    return amax_tiles(ds, x, M, N, nullptr, 1, cfg->rht_sign_mask, true, amax_row, amax_col, 1, s);
   return cuda_status(launch_amax_flat(x, M * N, amax_row, amax_col, amax_flat_grid(ds, M * N / 8), s));
 }
 
@@ -238,14 +255,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
     if (need_row_amax && cudaMemsetAsync(row_amax_slot, 0, 8, s) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (need_col_amax && cudaMemsetAsync(col_gscale, 0, 8, s) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (need_col_amax && rht) {
-      AmaxArgs a{};
-      a.x = x; a.rows = M; a.cols = N; a.offsets = nullptr; a.segments = 1;
-      a.sign_mask = cfg->rht_sign_mask;
-      a.amax_row = need_row_amax ? row_amax_slot : nullptr;
-      a.amax_col = col_gscale;
-      a.stride_row = 2; a.stride_col = 2; a.status = ds->workspace;
-      if (launch_amax_blocks(true, a, amax_grid(ds, (M / 16) * (N / 4), 256), s) != cudaSuccess)
-        return NVFP4_ERR_CUDA;
+      if ((st = amax_tiles(ds, x, M, N, nullptr, 1, cfg->rht_sign_mask, true,
+                           need_row_amax ? row_amax_slot : nullptr, col_gscale, 2, s)) != NVFP4_OK)
+        return st;
     } else {
       if (launch_amax_flat(x, M * N, need_row_amax ? row_amax_slot : nullptr,
                            need_col_amax ? col_gscale : nullptr, amax_flat_grid(ds, M * N / 8),
@@ -323,14 +335,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   // per-expert amax (and RHT amax) from one read, into the gscale outputs' amax slots
   if (row && cudaMemsetAsync(row_gscale, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (col && cudaMemsetAsync(col_gscale, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
-  AmaxArgs a{};
-  a.x = x; a.rows = T; a.cols = H; a.offsets = offsets; a.segments = E;
-  a.sign_mask = cfg->rht_sign_mask;
-  a.amax_row = row ? row_gscale : nullptr;
-  a.amax_col = col ? col_gscale : nullptr;
-  a.stride_row = 2; a.stride_col = 2; a.status = ds->workspace;
-  if (launch_amax_blocks(rht, a, amax_grid(ds, (T / 16 + E) * (H / 4), 256), s) != cudaSuccess)
-    return NVFP4_ERR_CUDA;
+  if ((st = amax_tiles(ds, x, T, H, offsets, E, cfg->rht_sign_mask, rht,
+                       row ? row_gscale : nullptr, col ? col_gscale : nullptr, 2, s)) != NVFP4_OK)
+    return st;
 
   QuantArgs q;
   std::memset(&q, 0, sizeof q);

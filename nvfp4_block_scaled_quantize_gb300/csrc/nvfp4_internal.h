@@ -81,21 +81,12 @@ struct QuantMode {
   bool row, col, rht, two_d, sr_row, sr_col;
 };
 
-// Arguments of the amax kernels.
-struct AmaxArgs {
-  const void* x;
-  int64_t rows, cols;
-  const int32_t* offsets;           // nullptr: one segment [0, rows)
-  int32_t segments;
-  uint32_t sign_mask;
-  float* amax_row;                  // max |x| per segment at amax_row[e * stride_row] (or null)
-  float* amax_col;                  // max |RHT(x)| (rht) or max |x| per segment (or null)
-  int32_t stride_row, stride_col;
-  uint32_t* status;
-};
-
 cudaError_t launch_quantize(const QuantMode& m, const QuantArgs& args, int grid, cudaStream_t s);
 cudaError_t prepare_quantize_kernels();
+// The amax pass alone through the tile kernel (per segment; RHT amax when rht): atomic maxima
+// into args.amax_row / args.amax_col, which the caller zeroes.
+cudaError_t launch_amax_tiles(bool rht, const QuantArgs& args, int grid, cudaStream_t s);
+cudaError_t prepare_amax_tiles();
 // per-translation-unit halves of the above
 cudaError_t launch_quantize_row(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_quantize_col(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
@@ -111,7 +102,6 @@ cudaError_t prepare_quantize_2d();
 
 cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float* out1, int grid,
                              cudaStream_t s);
-cudaError_t launch_amax_blocks(bool rht, const AmaxArgs& args, int grid, cudaStream_t s);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
                               int64_t R, int64_t C, float* out, int grid, cudaStream_t s);
 

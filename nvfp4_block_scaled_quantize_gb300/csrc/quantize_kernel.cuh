@@ -142,7 +142,12 @@ __device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int
 
 // FUSED: the amax is computed inside the launch (a.fused == 1; a cooperative launch of a
 // plain tensor). A template parameter, so that each path is compiled on its own.
-template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FUSED>
+// AMAX_ONLY: the amax pass alone, through the same stage ring: per segment max |x| and, with
+// RHT, max |bf16(RHT)| over its zero-padded 16-row column blocks, atomically maxed into
+// a.amax_row / a.amax_col (zeroed by the caller); no codes. Instantiated with ROW and !COL (no
+// lead rows: tiles start on the segments' 16-row blocks).
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FUSED,
+          bool AMAX_ONLY = false>
 __global__ void __launch_bounds__(kQuantThreads, 1)
     quantize_tiles_kernel(const __grid_constant__ QuantArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -284,6 +289,12 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     __syncthreads();
   }
 
+  // amax pass: per-segment maxima (16-bit magnitudes) in the otherwise unused staging area
+  uint32_t* seg_amax = reinterpret_cast<uint32_t*>(smem + kSmemColCodes);  // [2][kMaxSegments]
+  if (AMAX_ONLY) {
+    for (int e = tid; e < 2 * kMaxSegments; e += blockDim.x) seg_amax[e] = 0u;
+    __syncthreads();
+  }
   const int g = warp / kWarpsPerGroup;   // group
   const int rb = warp % kWarpsPerGroup;  // slab of the tile (rows 16 rb .. 16 rb + 15)
   const int gt = tid - g * 32 * kWarpsPerGroup;  // thread index inside the group
@@ -357,7 +368,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   auto amax_col_of = [&](int e) -> float {
     return FUSED ? fused_amax[1] : a.amax_col[(int64_t)e * a.amax_col_stride];
   };
-  if (blockIdx.x == 0) {  // global scales {amax, S_dec} of every segment
+  if (blockIdx.x == 0 && !AMAX_ONLY) {  // global scales {amax, S_dec} of every segment
     for (int e = tid; e < E; e += blockDim.x) {
       float enc, dec;
       if (ROW || TWO_D) {
@@ -403,7 +414,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     cur_seg = e;
   };
-  if (plain && n_local > g) set_segment(0);  // overlaps the first loads (or follows the amax)
+  if (!AMAX_ONLY && plain && n_local > g) set_segment(0);  // overlaps the first loads (or follows the amax)
 
   for (int i = g; i < n_local; i += kGroups) {
     const int tile = blockIdx.x + i * stride;
@@ -453,6 +464,39 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     if (gt == 0 && i + kStages < n_local) {
       fence_proxy_async();
       issue(i + kStages, s);
+    }
+
+    if constexpr (AMAX_ONLY) {
+      if (slab_rows > 0) {  // rows past the segment's end are zero (above)
+        uint32_t t[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++)
+          t[r] = hmax_abs2(hmax_abs2(v[r].x, v[r].y), hmax_abs2(v[r].z, v[r].w));
+#pragma unroll
+        for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+          for (int r = 0; r < h; r++) t[r] = hmax_abs2(t[r], t[r + h]);
+        const uint32_t m = t[0] & 0x7FFF7FFFu;
+        uint32_t mr = max(m & 0xFFFFu, m >> 16), mc = mr;
+        if (RHT) {
+          uint32_t mt = 0u;
+#pragma unroll
+          for (int k = 0; k < 4; k++) {
+            uint32_t w[16];
+#pragma unroll
+            for (int r = 0; r < 16; r++) w[r] = comp(v[r], k);
+            mt = vmax2(mt, rht16_pair_absmax(w, a.sign_mask));
+          }
+          mc = max(mt & 0xFFFFu, mt >> 16);
+        }
+        mr = __reduce_max_sync(0xFFFFFFFFu, mr);
+        mc = __reduce_max_sync(0xFFFFFFFFu, mc);
+        if (lane == 0) {
+          atomicMax(&seg_amax[c.seg], mr);
+          atomicMax(&seg_amax[kMaxSegments + c.seg], mc);
+        }
+      }
+      continue;
     }
 
     if (c.seg != cur_seg) set_segment(c.seg);  // uniform across the group
@@ -692,6 +736,15 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   // Every load issued into a stage is waited for by the group that owns its tile, unless that
   // group gave up: let the last load of each stage land before the CTA leaves.
   __syncthreads();
+  if (AMAX_ONLY) {  // this CTA's maxima into the per-segment results
+    for (int e = tid; e < E; e += blockDim.x) {
+      const uint32_t mr = seg_amax[e], mc = seg_amax[kMaxSegments + e];
+      if (a.amax_row && mr)
+        atomicMax(reinterpret_cast<unsigned int*>(const_cast<float*>(a.amax_row) + (int64_t)e * a.amax_row_stride), mr << 16);
+      if (a.amax_col && mc)
+        atomicMax(reinterpret_cast<unsigned int*>(const_cast<float*>(a.amax_col) + (int64_t)e * a.amax_col_stride), mc << 16);
+    }
+  }
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
       const int loads = issued[s];
@@ -719,6 +772,19 @@ cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
   quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false>
       <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
   return cudaGetLastError();
+}
+
+// The amax pass (AMAX_ONLY) of a plain or grouped tensor.
+template <bool RHT>
+cudaError_t launch_amax_pass(const QuantArgs& args, int grid, cudaStream_t s) {
+  quantize_tiles_kernel<true, false, RHT, false, false, false, false, true>
+      <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
+  return cudaGetLastError();
+}
+template <bool RHT>
+cudaError_t prepare_amax_pass() {
+  return cudaFuncSetAttribute(quantize_tiles_kernel<true, false, RHT, false, false, false, false, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
 }
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
