@@ -63,7 +63,8 @@ typedef enum nvfp4_rounding {
 /* Device status bits (nvfp4_get_status). */
 #define NVFP4_DEVICE_BAD_OFFSETS 0x1u  /* grouped offsets not non-decreasing within [0, T],
                                           or padded token total above the column capacity */
-#define NVFP4_DEVICE_TIMEOUT     0x2u  /* a grid barrier or a copy wait passed its limit */
+#define NVFP4_DEVICE_TIMEOUT     0x2u  /* the wait for every CTA's amax or a copy wait passed
+                                          its limit */
 
 /* Options of one quantization. Zero-initialise and set what is needed. */
 typedef struct nvfp4_config {

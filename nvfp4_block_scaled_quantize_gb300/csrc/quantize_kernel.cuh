@@ -9,16 +9,21 @@
 //     (cp.async.bulk.tensor) completing on mbarriers; kGroups groups of four warps each take a
 //     whole tile, one warp per 16-row slab, and refill the stage as soon as the four slabs sit
 //     in registers (12 warps: three per SM sub-partition, so up to 168 registers each);
-//   * each lane holds a 16-row x 8-column piece of its slab, so every element is widened
-//     from BF16 once and feeds both orientations: a rowwise 1x16 block is a lane pair
-//     ("Optimization" item 7: a warp covers several tokens x hidden blocks), a columnwise block
-//     is one lane's column (thread-local maximum, RHT butterflies and conversion);
-//   * scale reciprocals come from a per-warp 128-entry table indexed by the E4M3 code, built
+//   * each lane holds a 16-row x 8-column piece of its slab, read from shared memory once for
+//     both orientations: a rowwise 1x16 block is a lane pair ("Optimization" item 7: a warp
+//     covers several tokens x hidden blocks), a columnwise block is one lane's column
+//     (thread-local maximum, RHT butterflies and conversion);
+//   * scale reciprocals come from a per-group 128-entry table indexed by the E4M3 code, built
 //     once per segment with the exact (div_rn) reciprocal ("Fast math");
 //   * columnwise codes/scales of the four slabs are staged in shared memory (XOR-swizzled,
-//     conflict-free) and leave as whole 32-byte column runs ("Optimization" item 5);
+//     conflict-free) and leave as whole 32-byte column runs ("Optimization" item 5); grouped
+//     segments start their tiles on 64-row column boundaries so that this holds for them too;
+//   * 2D row+col: the columnwise codes are the rowwise codes transposed in registers;
 //   * stochastic rounding uses one Philox4x32-10 draw per 16-element block, all four words
 //     consumed by cvt.rs.satfinite.e2m1x4 ("Optimization" item 3).
+// Variants: FUSED adds the amax of a plain tensor inside the launch (an amax phase over the
+// same stage ring, then a wait for every CTA's arrival); AMAX_ONLY is that amax pass alone,
+// per segment (fused_amax.cuh, amax_pass.cu).
 // Every wait on an mbarrier gives up after a time limit; the kernel then records
 // NVFP4_DEVICE_TIMEOUT and leaves after the loads it issued have landed (bounded too).
 #pragma once
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int gt = tid - g * 32 * kWarpsPerGroup;  // thread index inside the group
 
   // ---- single-launch amax: stream the local tiles through the stage ring (last to first),
-  // reduce, meet at the grid barrier, read every CTA's partials ----
+  // reduce, fold into the workspace maxima, wait for every CTA's arrival ----
   float* fused_amax = reinterpret_cast<float*>(smem + kSmemFused) + 32;  // [0] row, [1] col
   if (fused) {
     uint32_t m = 0u, mt = 0u;

@@ -348,7 +348,8 @@ def test_fused_amax_matches_oracle(mode, shape):
 
 
 def test_fused_amax_repeated_calls_reuse_the_barrier():
-    """The grid barrier resets itself: many fused launches in a row stay correct."""
+    """The arrival count and the epoch-tagged maxima need no clearing: many fused launches in a
+    row stay correct."""
     dev = _cuda()
     for k in range(6):
         x_cpu = workloads.laplace(64 * (k + 1), 512, 1e-2 * (k + 1), seed=70 + k)
