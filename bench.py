@@ -13,6 +13,7 @@ events on the launching stream. Prints ONE JSON line (rank 0).
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -62,12 +63,20 @@ def peaks():
 KERNEL_SOURCES = ("quantize_kernel.cuh", "fused_amax.cuh", "nvfp4_device.cuh", "nvfp4_internal.h")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and whitespace (string literals in these files hold no
+    comment markers), so that only code changes change the digest."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_source_digest() -> str:
-    """sha256 (first 16 hex digits) over the tile kernel's sources, in a fixed order."""
+    """sha256 (first 16 hex digits) over the tile kernel's sources, code only, in a fixed order."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "nvfp4_block_scaled_quantize_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_quantize_gb300", "csrc", name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -83,7 +92,7 @@ def kernel_traffic(workload: str, pipeline: str):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("source_sha256_16") != kernel_source_digest():
+    if fields.get("source_sha256_16", "").split()[:1] != [kernel_source_digest()]:
         return None
     try:
         return int(fields["dram_bytes_per_launch"].split()[0])
