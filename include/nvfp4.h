@@ -189,6 +189,21 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const n
                                     uint8_t* col_codes, uint8_t* col_scales, float* col_gscale,
                                     void* stream);
 
+/* Scale bytes in the layout the tensor-core block-scaled (NVFP4) GEMMs read, e.g. cuBLASLt's
+ * ([PR4798] "Config surface and AUTO": the reference's columnwise scale store is hardwired to
+ * this swizzled layout; the layout is the 1D block-scaling-factor layout of the cuBLAS
+ * documentation).
+ *   scales (device) uint8 [R][C], row-major, as the quantize calls write them (rowwise:
+ *          R = M, C = N/16; columnwise: R = N, C = M/16).
+ *   out    (device) uint8 [ceil(R/128) * ceil(C/4) * 512], 16-byte aligned: 128 x 4 tiles of
+ *          the zero-padded matrix in row-major tile order, 512 bytes each; inside a tile the
+ *          scale of row r, column c is byte (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4).
+ * The codes need no change: [R][C*8] bytes, two E2M1 codes per byte, the even element in the
+ * low nibble, is the packed FP4 operand those GEMMs take (the global scales S_dec of both
+ * operands multiply the product). */
+nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, uint8_t* out,
+                                  void* stream);
+
 /* Synchronize `stream`, then read and clear the current device's status word into
  * *device_status (NVFP4_DEVICE_* bits). Returns NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT
  * when bits were set, NVFP4_OK otherwise. */

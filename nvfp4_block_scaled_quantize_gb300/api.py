@@ -147,6 +147,18 @@ def nvfp4_dequantize(codes, scales, gscale):
     return out
 
 
+def nvfp4_swizzle_scales(scales):
+    """uint8 [R, C] E4M3 scales -> the flat 128 x 4 tiled layout of the block-scaled GEMMs."""
+    L = _lib.load()
+    src = scales.contiguous()
+    R, C = src.shape
+    out = torch.empty(((R + 127) // 128) * ((C + 3) // 4) * 512, dtype=torch.uint8,
+                      device=src.device)
+    _raise_if(L.nvfp4_swizzle_scales(_ptr(src), R, C, _ptr(out), _stream(src.device)),
+              "nvfp4_swizzle_scales")
+    return out
+
+
 def nvfp4_get_status(device=None):
     """Synchronize the current stream and return (status, device status bits); clears them."""
     L = _lib.load()

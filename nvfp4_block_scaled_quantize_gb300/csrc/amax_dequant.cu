@@ -93,7 +93,45 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint8_t* __restri
   }
 }
 
+// Scale bytes [R][C] -> the 128 x 4 tiled layout of the tensor-core block-scaled GEMMs: one
+// thread per 16-byte chunk of the output; chunk q of tile (tr, tc) holds rows 128 tr + q +
+// 32 i (i = 0..3) of columns 4 tc .. 4 tc + 3, zero past R or C.
+__global__ void __launch_bounds__(256) swizzle_scales_kernel(const uint8_t* __restrict__ s,
+                                                             int64_t R, int64_t C,
+                                                             uint8_t* __restrict__ out) {
+  const int64_t tiles_c = (C + 3) / 4;
+  const int64_t nchunks = ((R + 127) / 128) * tiles_c * 32;
+  const bool words = (C & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 3) == 0;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < nchunks;
+       k += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = k >> 5, tr = t / tiles_c, tc = t - tr * tiles_c;
+    const int q = (int)(k & 31);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const int64_t r = 128 * tr + 32 * i + q;
+      w[i] = 0u;
+      if (r < R) {
+        if (words) {
+          w[i] = *reinterpret_cast<const uint32_t*>(s + r * C + 4 * tc);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; j++)
+            if (4 * tc + j < C) w[i] |= (uint32_t)s[r * C + 4 * tc + j] << (8 * j);
+        }
+      }
+    }
+    *reinterpret_cast<uint4*>(out + 16 * k) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, uint8_t* out,
+                                  int grid, cudaStream_t s) {
+  swizzle_scales_kernel<<<grid, 256, 0, s>>>(scales, R, C, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float* out1, int grid,
                              cudaStream_t s) {

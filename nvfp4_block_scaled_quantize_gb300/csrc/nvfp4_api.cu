@@ -373,6 +373,20 @@ NVFP4_EXPORT nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* 
                                        static_cast<cudaStream_t>(stream)));
 }
 
+NVFP4_EXPORT nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C,
+                                               uint8_t* out, void* stream) {
+  if (R < 0 || C < 0) return NVFP4_ERR_INVALID_ARG;
+  if (R * C == 0) return NVFP4_OK;
+  if (scales == nullptr || out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(out, 16)) return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  const int64_t chunks = ((R + 127) / 128) * ((C + 3) / 4) * 32;
+  return cuda_status(launch_swizzle_scales(scales, R, C, out, amax_grid(ds, chunks, 256),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 NVFP4_EXPORT nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status) {
   if (device_status == nullptr) return NVFP4_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;

@@ -102,6 +102,8 @@ cudaError_t prepare_quantize_2d();
 
 cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float* out1, int grid,
                              cudaStream_t s);
+cudaError_t launch_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, uint8_t* out,
+                                  int grid, cudaStream_t s);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
                               int64_t R, int64_t C, float* out, int grid, cudaStream_t s);
 

@@ -293,6 +293,26 @@ def dequantize(codes, scales, s_dec) -> np.ndarray:
     return out
 
 
+def swizzle_scales(scales) -> np.ndarray:
+    """E4M3 scale bytes [R, C] (row-major, as the quantize calls write them) rearranged into the
+    128 x 4 tiled layout that the tensor-core block-scaled GEMMs read ([PR4798] "Config surface
+    and AUTO": its columnwise scale store is hardwired to this swizzled layout; the layout is
+    the 1D block-scaling-factor layout of the cuBLAS documentation). The matrix is padded with
+    zeros to a multiple of 128 rows and 4 columns and cut into 128 x 4 tiles, stored one after
+    another in row-major tile order, 512 bytes each; inside a tile the scale of row r, column c
+    sits at byte (r mod 32) * 16 + ((r mod 128) div 32) * 4 + (c mod 4). Returns the flat byte
+    array."""
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    R, C = s.shape
+    tiles_c = (C + 3) // 4
+    out = np.zeros(((R + 127) // 128) * tiles_c * 512, dtype=np.uint8)
+    for r in range(R):
+        for c in range(C):
+            tile = (r // 128) * tiles_c + c // 4
+            out[tile * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4] = s[r, c]
+    return out
+
+
 @dataclass
 class Config:
     """The quantizer's options, named as in the C library's configuration."""

@@ -111,3 +111,11 @@ def test_host_pipeline_argument_checks_return_before_any_cuda_call(L):
     assert L.nvfp4_host_pipeline_submit(None, ctypes.c_void_p(FAKE), *([None] * 7)) == 1
     assert L.nvfp4_host_pipeline_join(None, None) == 1
     assert L.nvfp4_host_pipeline_destroy(None) == 0
+
+
+def test_swizzle_argument_checks_return_before_any_cuda_call(L):
+    p = ctypes.c_void_p
+    assert L.nvfp4_swizzle_scales(p(FAKE), -1, 4, p(FAKE), None) == 1
+    assert L.nvfp4_swizzle_scales(None, 0, 4, None, None) == 0           # empty: nothing to do
+    assert L.nvfp4_swizzle_scales(None, 4, 4, p(FAKE), None) == 1
+    assert L.nvfp4_swizzle_scales(p(FAKE), 4, 4, p(FAKE + 8), None) == 3  # misaligned output

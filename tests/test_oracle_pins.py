@@ -529,3 +529,19 @@ def test_grouped_rejects_bad_offsets():
         oracle.quantize_grouped(x, np.array([10, 40], dtype=np.int32))
     with pytest.raises(ValueError):
         oracle.quantize_grouped(x, np.array([10, 30], dtype=np.int32), cap=32)
+
+
+def test_swizzled_scales_are_a_permutation_padded_with_zeros():
+    """The 128 x 4 tiled layout moves every scale byte exactly once and fills the padding with
+    zeros: with all scales distinct and nonzero, each appears once in the output and every
+    other byte is zero. (Whether it is the layout the block-scaled GEMM reads is pinned on the
+    GPU by running cuBLASLt's NVFP4 GEMM on it.)"""
+    rng = np.random.Generator(np.random.PCG64(71))
+    for R, C in ((128, 1), (33, 3), (60, 4), (130, 1), (16, 15), (1, 5)):
+        s = rng.permutation(np.arange(1, R * C + 1)).astype(np.uint8).reshape(R, C)
+        out = oracle.swizzle_scales(s)
+        Rp, Cp = (R + 127) // 128 * 128, (C + 3) // 4 * 4
+        assert out.shape == (Rp * Cp,)
+        nz = out[out != 0]
+        assert len(nz) == R * C
+        assert np.array_equal(np.sort(nz), np.arange(1, R * C + 1, dtype=np.uint8))
