@@ -326,6 +326,7 @@ def run_ours(args, world, rank, local):
     inp = workloads.make_input(w)
     x = inp["x"].to(dev)
     kw = quant_kwargs(w, inp)
+    kw["fast_math"] = args.fast_math
     ideal = ideal_bytes(w, offsets=inp.get("offsets"))
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -452,6 +453,9 @@ def run_ours(args, world, rank, local):
                    "pipeline": ("one launch: amax phase, grid barrier, quantize phase"
                                 if args.pipeline == "fused" and not w.grouped else
                                 "amax pass + quantize pass (two launches)"),
+                   "math": "fast (rcp.approx multipliers%s)" % (
+                       ", FP32 RHT" if w.rht_col else "") if args.fast_math and not w.block2d
+                           else "exact",
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": launches_per_step * args.steps,
@@ -470,7 +474,8 @@ def run_ours(args, world, rank, local):
                             "frac": achieved / hbm, "peak_kind": peak_kind,
                             "kernel": "quantize_tiles_kernel",
                             "kernel_us": qk * 1e6,
-                            "traffic": kernel_traffic(w.name, args.pipeline)}
+                            "traffic": (None if args.fast_math
+                                        else kernel_traffic(w.name, args.pipeline))}
         if args.pipeline != "fused" or w.grouped:
             line["amax_pass_us"] = statistics.mean([e[0].elapsed_time(e[1]) for e in events]) * 1e3
     if world == 1 and not args.no_cpu_baseline:
@@ -489,6 +494,8 @@ def main():
     p.add_argument("--pipeline", choices=["fused", "two_pass"], default="fused",
                    help="fused: amax and quantize in one launch; two_pass: amax kernel then "
                         "quantize kernel")
+    p.add_argument("--fast-math", action="store_true",
+                   help="the fast-math variant (approximate reciprocal; FP32 RHT columnwise)")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

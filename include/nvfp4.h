@@ -91,7 +91,16 @@ typedef struct nvfp4_config {
                              Fused calls share the device workspace's count and maxima: on one
                              device they must not overlap in time (issue them on one stream).
                              Plain tensors only. */
-  int32_t reserved;       /* must be zero */
+  int32_t fast_math;      /* 0 = exact (default). 1 = the fast variant of [PR4798] "Fast math":
+                             the element multiplier is rcp.approx.ftz(float(s) * S_dec) instead
+                             of the correctly rounded reciprocal, and the columnwise RHT output
+                             is quantized from its FP32 value without the BF16 round-through.
+                             Not bit-defined (the approximate reciprocal is the hardware's);
+                             dequantized, it stays above 25 dB SQNR against the exact mode's
+                             output; with round-to-nearest a code moves by at most one E2M1
+                             step. The amax, the global scales and 2D (block2d) quantization
+                             stay exact. Other values:
+                             NVFP4_ERR_INVALID_ARG. */
 } nvfp4_config;
 
 /* Stochastic rounding ([PR4798] "Optimization" item 3 and "Correctness"): one Philox4x32-10

@@ -38,7 +38,7 @@ class Config(ctypes.Structure):
         ("rng_offset", ctypes.c_uint32),
         ("rng_seed", ctypes.c_uint64),
         ("fused_amax", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("fast_math", ctypes.c_int32),
     ]
 
 

@@ -43,12 +43,13 @@ def _round(v):
 
 
 def make_config(rowwise=True, columnwise=False, block2d=False, round_row="rn", round_col="rn",
-                rht_col=False, sign_mask=0, seed=0, offset=0, fused_amax=False) -> Config:
+                rht_col=False, sign_mask=0, seed=0, offset=0, fused_amax=False,
+                fast_math=False) -> Config:
     return Config(rowwise=int(bool(rowwise)), columnwise=int(bool(columnwise)),
                   block2d=int(bool(block2d)), round_row=_round(round_row),
                   round_col=_round(round_col), rht_col=int(bool(rht_col)),
                   rht_sign_mask=int(sign_mask), rng_offset=int(offset), rng_seed=int(seed),
-                  fused_amax=int(bool(fused_amax)), reserved=0)
+                  fused_amax=int(bool(fused_amax)), fast_math=int(bool(fast_math)))
 
 
 def _raise_if(status, where):
@@ -87,14 +88,15 @@ def alloc_outputs(M, N, device, rowwise=True, columnwise=False, col_ld=None, gro
 
 def nvfp4_quantize(x, rowwise=True, columnwise=False, block2d=False, round_row="rn",
                    round_col="rn", rht_col=False, sign_mask=0, seed=0, offset=0,
-                   fused_amax=False, amax_row=None, amax_col=None, out=None):
+                   fused_amax=False, amax_row=None, amax_col=None, out=None, fast_math=False):
     """Quantize a BF16 [M, N] CUDA tensor. amax_row / amax_col (float32[1] device tensors)
-    skip the amax pass; `out` reuses preallocated outputs (see alloc_outputs)."""
+    skip the amax pass; `out` reuses preallocated outputs (see alloc_outputs); fast_math
+    selects the approximate variant (see nvfp4_config.fast_math)."""
     _check_x(x)
     L = _lib.load()
     M, N = x.shape
     cfg = make_config(rowwise, columnwise, block2d, round_row, round_col, rht_col, sign_mask,
-                      seed, offset, fused_amax)
+                      seed, offset, fused_amax, fast_math)
     if out is None:
         out = alloc_outputs(M, N, x.device, rowwise, columnwise)
     g = out.get
@@ -112,7 +114,7 @@ def padded_capacity(counts) -> int:
 
 def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwise=True,
                            round_row="rn", round_col="rn", rht_col=False, sign_mask=0, seed=0,
-                           offset=0, out=None):
+                           offset=0, out=None, fast_math=False):
     """Grouped quantization of a packed BF16 [T, H] tensor; `offsets` is an int32 [E] device
     tensor of cumulative expert ends. col_capacity defaults to T + 16 * E (always enough)."""
     _check_x(x)
@@ -124,7 +126,7 @@ def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwi
     if col_capacity is None:
         col_capacity = (T + 15) // 16 * 16 + 16 * E
     cfg = make_config(rowwise, columnwise, False, round_row, round_col, rht_col, sign_mask, seed,
-                      offset)
+                      offset, fast_math=fast_math)
     if out is None:
         out = alloc_outputs(T, H, x.device, rowwise, columnwise, col_ld=col_capacity, groups=E)
     g = out.get

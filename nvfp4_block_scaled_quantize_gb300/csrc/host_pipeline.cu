@@ -95,7 +95,8 @@ bool alloc(T** out, size_t bytes) {
 NVFP4_EXPORT nvfp4_status nvfp4_host_pipeline_create(int64_t M, int64_t N,
                                                      const nvfp4_config* cfg, int32_t depth,
                                                      nvfp4_host_pipeline** out) {
-  if (out == nullptr || cfg == nullptr || cfg->reserved != 0) return NVFP4_ERR_INVALID_ARG;
+  if (out == nullptr || cfg == nullptr || (cfg->fast_math != 0 && cfg->fast_math != 1))
+    return NVFP4_ERR_INVALID_ARG;
   *out = nullptr;
   if (depth < 1 || depth > kMaxDepth) return NVFP4_ERR_INVALID_ARG;
   const bool row = cfg->rowwise != 0, col = cfg->columnwise != 0;

@@ -84,7 +84,7 @@ nvfp4_status make_tensor_map(CUtensorMap* map, const void* x, int64_t rows, int6
 
 nvfp4_status check_config(const nvfp4_config* cfg) {
   if (cfg == nullptr) return NVFP4_ERR_INVALID_ARG;
-  if (cfg->reserved != 0) return NVFP4_ERR_INVALID_ARG;
+  if (cfg->fast_math != 0 && cfg->fast_math != 1) return NVFP4_ERR_INVALID_ARG;
   if ((cfg->round_row != NVFP4_ROUND_RN && cfg->round_row != NVFP4_ROUND_SR) ||
       (cfg->round_col != NVFP4_ROUND_RN && cfg->round_col != NVFP4_ROUND_SR))
     return NVFP4_ERR_INVALID_ARG;
@@ -280,10 +280,11 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
   q.x = x;
   q.fused = fused ? 1 : 0;
+  q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
   q.fuse_ws = ds->workspace + kFuseWsOffset;
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
-  const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0};
+  const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};
   if (!fused) return cuda_status(launch_quantize(mode, q, grid, s));
   // every CTA adds one to the arrival count; the epoch orders this launch's maxima after all
   // earlier ones (the workspace starts zeroed: epoch 0, count 0)
@@ -350,7 +351,8 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
   q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
-  const QuantMode mode{row, col, rht, false, sr_row != 0, sr_col != 0};
+  q.fast = cfg->fast_math ? 1 : 0;
+  const QuantMode mode{row, col, rht, false, sr_row != 0, sr_col != 0, q.fast && rht};
   const int64_t tiles = ((T + kTileM - 1) / kTileM + E) * ((H + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
   return cuda_status(launch_quantize(mode, q, grid, s));

@@ -138,6 +138,40 @@ __device__ __forceinline__ float element_multiplier(float s, float s_dec) {
   return (p == 0.0f) ? 0.0f : r;
 }
 
+// rht16_pair without the BF16 round-through (the fast-math variant): x[i] receives the FP32
+// pair 0.25 * (H16 (d . v))_i of the two columns.
+__device__ __forceinline__ void rht16_pair_f32(const uint32_t (&w)[16], uint32_t sign_mask,
+                                               uint64_t (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    uint32_t flip = ((sign_mask >> i) & 1u) ? 0x80008000u : 0u;
+    x[i] = f2_from_bf16x2(w[i] ^ flip);
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      if ((i & h) == 0) {
+        uint64_t a = x[i], b = x[i + h];
+        x[i] = f2_add(a, b);
+        x[i + h] = f2_sub(a, b);
+      }
+    }
+  }
+  const uint64_t quarter = f2_pack(0.25f, 0.25f);
+#pragma unroll
+  for (int i = 0; i < 16; i++) x[i] = f2_mul(x[i], quarter);
+}
+
+// The fast-math element multiplier: the hardware's approximate reciprocal of s * S_dec (flush
+// to zero), 0 for a zero product, at most FLT_MAX ([PR4798] "Fast math": rcp.approx.ftz).
+__device__ __forceinline__ float element_multiplier_fast(float s, float s_dec) {
+  const float p = __fmul_rn(s, s_dec);
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(p));
+  return (p == 0.0f) ? 0.0f : fminf(r, FLT_MAX);
+}
+
 // Largest |bf16(0.25 * (H16 (d . v))_i)| over the 16 outputs of each of the two columns of w
 // (rht16_pair's outputs), as BF16 magnitude bits (column 0 in the low half). Scaling by 0.25
 // and rounding to BF16 are both monotone, so the maximum of the rounded outputs is the rounded

@@ -71,6 +71,7 @@ struct QuantArgs {
   uint32_t rng_offset;
   uint32_t* status;
   int32_t fused;                    // 1: compute the amax inside this launch (one segment)
+  int32_t fast;                     // 1: fast-math element multipliers (rcp.approx)
   uint32_t fuse_target;             // fuse_ws[0] once every CTA of this launch has arrived
   uint64_t fuse_epoch;              // larger than any earlier launch's on fuse_ws (< 2^48)
   uint32_t* fuse_ws;                // kFuseWsWords words, 8-byte aligned
@@ -79,6 +80,7 @@ struct QuantArgs {
 // What one quantize launch produces.
 struct QuantMode {
   bool row, col, rht, two_d, sr_row, sr_col;
+  bool fast;  // fast math with the RHT: the columnwise transform is not rounded through BF16
 };
 
 cudaError_t launch_quantize(const QuantMode& m, const QuantArgs& args, int grid, cudaStream_t s);

@@ -151,8 +151,10 @@ __device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int
 // RHT, max |bf16(RHT)| over its zero-padded 16-row column blocks, atomically maxed into
 // a.amax_row / a.amax_col (zeroed by the caller); no codes. Instantiated with ROW and !COL (no
 // lead rows: tiles start on the segments' 16-row blocks).
+// FAST_RHT: fast math with the RHT (columnwise codes from the FP32 transform, no BF16
+// round-through).
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FUSED,
-          bool AMAX_ONLY = false>
+          bool AMAX_ONLY = false, bool FAST_RHT = false>
 __global__ void __launch_bounds__(kQuantThreads, 1)
     quantize_tiles_kernel(const __grid_constant__ QuantArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -414,8 +416,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     if (TWO_D) { s_enc_c = s_enc_r; dec_c = dec_r; }
     static_assert(kTableEntries == 32 * kWarpsPerGroup, "one table entry per group thread");
     const float sv = e4m3x2_to_float2((uint16_t)gt).x;
-    tab_row[gt] = element_multiplier(sv, dec_r);
-    tab_col[gt] = element_multiplier(sv, dec_c);
+    tab_row[gt] = a.fast ? element_multiplier_fast(sv, dec_r) : element_multiplier(sv, dec_r);
+    tab_col[gt] = a.fast ? element_multiplier_fast(sv, dec_c) : element_multiplier(sv, dec_c);
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     cur_seg = e;
   };
@@ -645,10 +647,22 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           uint32_t w[16];
 #pragma unroll
           for (int r = 0; r < 16; r++) w[r] = comp(v[r], k);
-          if (RHT) rht16_pair(w, a.sign_mask);
+          uint64_t xs[16];  // fast math: the FP32 transform, not rounded (unused otherwise)
+          if (FAST_RHT) rht16_pair_f32(w, a.sign_mask, xs);
+          else if (RHT) rht16_pair(w, a.sign_mask);
           uint32_t s2;
           uint64_t rc2;
-          if (TWO_D) {
+          if (FAST_RHT) {
+            float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+              const float2 y = f2_unpack(xs[r]);
+              m0 = fmaxf(m0, fabsf(y.x));
+              m1 = fmaxf(m1, fabsf(y.y));
+            }
+            s2 = block_scales2(m0, m1, s_enc_c);
+            rc2 = f2_pack(tab_col[s2 & 0xFFu], tab_col[s2 >> 8]);
+          } else if (TWO_D) {
             s2 = tile_s | (tile_s << 8);
             rc2 = f2_pack(tile_r, tile_r);
           } else {
@@ -669,7 +683,9 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           for (int o = 0; o < 2; o++) {
             float2 t[8];
 #pragma unroll
-            for (int r = 0; r < 8; r++) t[r] = f2_unpack(f2_mul(f2_from_bf16x2(w[8 * o + r]), rc2));
+            for (int r = 0; r < 8; r++)
+              t[r] = f2_unpack(
+                  f2_mul(FAST_RHT ? xs[8 * o + r] : f2_from_bf16x2(w[8 * o + r]), rc2));
             code[0][o] = e2m1x8<SR_COL>(t[0].x, t[1].x, t[2].x, t[3].x, t[4].x, t[5].x, t[6].x,
                                         t[7].x, comp(W0, 2 * o), comp(W0, 2 * o + 1));
             code[1][o] = e2m1x8<SR_COL>(t[0].y, t[1].y, t[2].y, t[3].y, t[4].y, t[5].y, t[6].y,
@@ -758,7 +774,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   }
 }
 
-template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
 cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
   if (args.fused) {  // every CTA waits for all the others: a cooperative launch
     cudaLaunchConfig_t cfg = {};
@@ -772,9 +788,10 @@ cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(
-        &cfg, quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true>, args);
+        &cfg, quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT>,
+        args);
   }
-  quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false>
+  quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT>
       <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
   return cudaGetLastError();
 }
@@ -792,14 +809,15 @@ cudaError_t prepare_amax_pass() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
 }
 
-template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL>
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
 cudaError_t prepare() {
   cudaError_t e = cudaFuncSetAttribute(
-      quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false>,
+      quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT>,
       cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+  return cudaFuncSetAttribute(
+      quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
 }
 
 }  // namespace qk

@@ -91,7 +91,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
                                                  uint8_t* row_scales, float* row_gscale,
                                                  uint8_t* col_codes, uint8_t* col_scales,
                                                  float* col_gscale, void* stream) {
-  if (cfg == nullptr || cfg->reserved != 0) return NVFP4_ERR_INVALID_ARG;
+  if (cfg == nullptr || (cfg->fast_math != 0 && cfg->fast_math != 1)) return NVFP4_ERR_INVALID_ARG;
   if ((cfg->round_row != NVFP4_ROUND_RN && cfg->round_row != NVFP4_ROUND_SR) ||
       (cfg->round_col != NVFP4_ROUND_RN && cfg->round_col != NVFP4_ROUND_SR) ||
       cfg->rht_sign_mask > 0xFFFFu)
@@ -142,6 +142,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset;
   q.status = d->scratch + kScratchStatus;
   q.fused = 1;
+  q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
   q.fuse_ws = d->scratch + kScratchFuse;
   // each CTA adds one to the arrival count and tags its maxima with a larger epoch than any
   // earlier call's, so nothing has to be cleared before the launch
@@ -149,7 +150,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   q.fuse_epoch = d->epoch + 1;
   q.fuse_target = d->count + (uint32_t)grid;
   const QuantMode mode{row, col, rht, two_d, cfg->round_row == NVFP4_ROUND_SR,
-                       cfg->round_col == NVFP4_ROUND_SR};
+                       cfg->round_col == NVFP4_ROUND_SR, q.fast && rht};
   if (launch_quantize(mode, q, grid, s) != cudaSuccess) return NVFP4_ERR_CUDA;
   d->epoch = q.fuse_epoch;
   d->count = q.fuse_target;

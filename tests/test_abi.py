@@ -64,7 +64,7 @@ def test_argument_checks_return_before_any_launch(L):
     assert _quant(L, 32, 32, _cfg(block2d=1, rht_col=1, columnwise=1)) == 4
     assert _quant(L, 32, 32, _cfg(block2d=1, round_row=1)) == 4
     assert _quant(L, 32, 32, _cfg(round_row=2)) == 1
-    assert _quant(L, 32, 32, _cfg(reserved=1)) == 1
+    assert _quant(L, 32, 32, _cfg(fast_math=2)) == 1
     assert _quant(L, 32, 32, _cfg(rht_sign_mask=1 << 16)) == 1
     assert _quant(L, -1, 32, _cfg()) == 1
     assert _quant(L, 32, 32, _cfg(), x=FAKE + 8) == 3           # misaligned input
@@ -102,7 +102,7 @@ def test_host_pipeline_argument_checks_return_before_any_cuda_call(L):
                                                                  ctypes.byref(h))
     assert create(64, 64, _cfg(), 0) == 1                       # depth below 1
     assert create(64, 64, _cfg(), 5) == 1                       # depth above 4
-    assert create(64, 64, _cfg(reserved=1), 2) == 1
+    assert create(64, 64, _cfg(fast_math=-1), 2) == 1
     assert create(64, 64, _cfg(rowwise=0), 2) == 4              # nothing selected
     assert create(0, 64, _cfg(), 2) == 2                        # empty
     assert create(64, 24, _cfg(), 2) == 2                       # N % 16

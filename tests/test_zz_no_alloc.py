@@ -37,6 +37,8 @@ CASES = [
                                                sign_mask=0x5A3C, round_col="sr", seed=9)),
     ("weight_2d", (512, 1792), dict(rowwise=True, columnwise=True, block2d=True)),
     ("ragged_row_sr", (80, 272), dict(rowwise=True, round_row="sr", seed=3)),
+    ("row_col_rht_fast_math", (1024, 2048), dict(rowwise=True, columnwise=True, rht_col=True,
+                                                  sign_mask=0x3C5A, fast_math=True)),
 ]
 
 
