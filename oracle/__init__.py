@@ -6,6 +6,11 @@ no code with it; the arithmetic lives in ``nvfp4_oracle.c`` (plain scalar C, IEE
 each step cited there to the page "[nvfp4_training] Optimize CuteDSL kernels for NVFP4
 training", pytorch/ao pull request #4798).
 
+The MX formats (MXFP8 with E4M3 or E5M2 elements, MXFP4 with E2M1 elements; 32-element
+blocks, E8M0 power-of-two scales, no tensor scale) follow the same pattern; their readings
+(M1-M4 in ``nvfp4_oracle.c``) take the OCP Microscaling Formats v1.0 conversion, which the pages
+name but do not spell out.
+
 BF16 tensors are passed as their 16-bit patterns (``numpy.uint16``). Outputs follow the
 layouts of the C library: rowwise codes [M, N/2] and scales [M, N/16]; columnwise (transposed)
 codes [N, M/2] and scales [N, M/16]; global scales as ``[amax, S_dec]``.
@@ -70,6 +75,17 @@ def lib():
                                                        ctypes.c_uint64, ctypes.c_uint32,
                                                        _u8p, _u8p, _f32p, _u8p, _u8p, _f32p]),
             "oracle_dequantize": (None, [_u8p, _u8p, ctypes.c_float, _i64, _i64, _f32p]),
+            "oracle_e5m2_encode": (ctypes.c_uint8, [ctypes.c_float]),
+            "oracle_e5m2_decode": (ctypes.c_float, [ctypes.c_uint8]),
+            "oracle_e8m0_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "oracle_mx_scale": (ctypes.c_uint8, [ctypes.c_double, ctypes.c_int32]),
+            "oracle_mx_encode": (ctypes.c_uint8, [ctypes.c_double, ctypes.c_int32]),
+            "oracle_mx_decode": (ctypes.c_double, [ctypes.c_uint8, ctypes.c_int32]),
+            "oracle_mx_quantize_rowwise": (None, [_u16p, _i64, _i64, ctypes.c_int32, _u8p,
+                                                  _u8p]),
+            "oracle_mx_quantize_colwise": (None, [_u16p, _i64, _i64, ctypes.c_int32, _u8p,
+                                                  _u8p]),
+            "oracle_mx_dequantize": (None, [_u8p, _u8p, ctypes.c_int32, _i64, _i64, _f32p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -350,3 +366,89 @@ def quantize(x, cfg: Config):
         out.update(col_codes=cc, col_scales=cs, col_gscale=gs)
     return out
 
+
+
+# ----------------------------------------------------------------------------------------
+# MX formats (readings M1-M4 in nvfp4_oracle.c)
+# ----------------------------------------------------------------------------------------
+
+MX_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
+
+
+def mx_format(fmt) -> int:
+    return MX_FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def e5m2_encode(values) -> np.ndarray:
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib().oracle_e5m2_encode(float(f)) for f in v], dtype=np.uint8)
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib().oracle_e5m2_decode(int(b)) for b in c], dtype=np.float32)
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib().oracle_e8m0_decode(int(b)) for b in c], dtype=np.float64)
+
+
+def mx_scale(amax: float, fmt) -> int:
+    """E8M0 code of a 32-element block whose largest magnitude is amax (reading M1)."""
+    return lib().oracle_mx_scale(float(amax), mx_format(fmt))
+
+
+def mx_encode(values, fmt) -> np.ndarray:
+    """Element codes of already scaled values t = v / X (reading M2)."""
+    f = mx_format(fmt)
+    v = np.asarray(values, dtype=np.float64).ravel()
+    return np.array([lib().oracle_mx_encode(float(t), f) for t in v], dtype=np.uint8)
+
+
+def mx_decode(codes, fmt) -> np.ndarray:
+    f = mx_format(fmt)
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib().oracle_mx_decode(int(b), f) for b in c], dtype=np.float64)
+
+
+def _mx_outputs(rows, cols, fmt):
+    f = mx_format(fmt)
+    codes = np.zeros((rows, cols // 2 if f == 2 else cols), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 32), dtype=np.uint8)
+    return f, codes, scales
+
+
+def mx_quantize_rowwise(x, fmt):
+    """Rowwise MX codes [M, N] (FP8) or [M, N/2] (FP4) and E8M0 scales [M, N/32]."""
+    xb = as_bf16_bits(x)
+    M, N = xb.shape
+    assert N % 32 == 0
+    f, codes, scales = _mx_outputs(M, N, fmt)
+    lib().oracle_mx_quantize_rowwise(_ptr(xb, _u16p), M, N, f, _ptr(codes, _u8p),
+                                     _ptr(scales, _u8p))
+    return codes, scales
+
+
+def mx_quantize_colwise(x, fmt):
+    """Columnwise MX codes [N, M] (FP8) or [N, M/2] (FP4) and E8M0 scales [N, M/32]."""
+    xb = as_bf16_bits(x)
+    M, N = xb.shape
+    assert M % 32 == 0
+    f, codes, scales = _mx_outputs(N, M, fmt)
+    lib().oracle_mx_quantize_colwise(_ptr(xb, _u16p), M, N, f, _ptr(codes, _u8p),
+                                     _ptr(scales, _u8p))
+    return codes, scales
+
+
+def mx_dequantize(codes, scales, fmt) -> np.ndarray:
+    """FP32 [R, C] values of MX codes and E8M0 scales [R, C/32]."""
+    f = mx_format(fmt)
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    R = c.shape[0]
+    C = c.shape[1] * (2 if f == 2 else 1)
+    assert s.shape == (R, C // 32)
+    out = np.zeros((R, C), dtype=np.float32)
+    lib().oracle_mx_dequantize(_ptr(c, _u8p), _ptr(s, _u8p), f, R, C, _ptr(out, _f32p))
+    return out

@@ -565,3 +565,162 @@ ORACLE_API void oracle_dequantize(const uint8_t* codes, const uint8_t* scales, f
     }
   }
 }
+
+/* ========================================================================================== */
+/* MX formats: MXFP8 (E4M3 or E5M2 elements) and MXFP4 (E2M1 elements). Blocks of 32         */
+/* consecutive elements share one power-of-two scale stored as E8M0; there is no tensor-wide   */
+/* scale, so no amax pass. [Perplexity] names the formats and their 32-element block maxima;  */
+/* the pages give no formula, so the scale and rounding rules are the conversion the OCP      */
+/* Microscaling Formats (MX) v1.0 specification defines (readings M1-M4):                     */
+/*   M1 the block's shared exponent is floor(log2(max |v_i|)) - emax_elem, emax_elem being the */
+/*      exponent of the element format's largest normal (E4M3: 8, E5M2: 15, E2M1: 2), clamped */
+/*      to [-127, 127]; an all-zero block gets -127. The E8M0 code is the exponent + 127 (the  */
+/*      NaN code 0xFF is never produced: inputs are finite).                                   */
+/*   M2 each element is v_i / 2^exponent rounded to nearest-even onto the element format,     */
+/*      saturating at its largest finite magnitude (448, 57344, 6); the sign of a value that  */
+/*      rounds to zero is kept.                                                               */
+/*   M3 rowwise: codes [M][N] bytes (FP8) or [M][N/2] (FP4, even element in the low nibble),  */
+/*      scales [M][N/32]; columnwise: the same for the transposed tensor, codes [N][M] or     */
+/*      [N][M/2], scales [N][M/32] (as R9).                                                   */
+/*   M4 formats are numbered 0 = E4M3, 1 = E5M2, 2 = E2M1.                                    */
+/* ========================================================================================== */
+
+/* E5M2 (FP8, 1 sign / 5 exponent bits, bias 15 / 2 mantissa bits, infinities at 0x7C, largest
+ * finite 57344 = 1.75 * 2^15, subnormals 0.mm * 2^-14 down to 2^-16). */
+static uint8_t e5m2_encode_rn_satfinite(float v) {
+  uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  double a = fabs((double)v);
+  if (isnan(v)) return 0x7F;
+  if (a >= 57344.0) return (uint8_t)(sign | 0x7B); /* satfinite: clamp to the largest finite */
+  if (a < ldexp(1.0, -14)) {
+    /* subnormal range: an integer multiple of 2^-16; q == 4 is 2^-14 = code 0x04 */
+    double q = round_half_even(a * 65536.0);
+    return (uint8_t)(sign | (uint8_t)q);
+  }
+  int e2;
+  double m = frexp(a, &e2); /* a = m * 2^e2, m in [0.5, 1) */
+  int e = e2 - 1;
+  double mant = round_half_even((2.0 * m - 1.0) * 4.0);
+  if (mant == 4.0) { mant = 0.0; e += 1; }
+  int code = ((e + 15) << 2) | (int)mant;
+  if (code > 0x7B) code = 0x7B;
+  return (uint8_t)(sign | code);
+}
+
+static float e5m2_decode(uint8_t c) {
+  int exp_bits = (c >> 2) & 0x1F;
+  int man = c & 0x3;
+  double v;
+  if (exp_bits == 0x1F) return man ? NAN : ((c & 0x80) ? -INFINITY : INFINITY);
+  if (exp_bits == 0) v = ldexp((double)man, -16);
+  else v = ldexp(1.0 + man / 4.0, exp_bits - 15);
+  return (float)((c & 0x80) ? -v : v);
+}
+
+static double e8m0_decode(uint8_t c) { return ldexp(1.0, (int)c - 127); }
+
+static int mx_emax(int fmt) { return fmt == 0 ? 8 : (fmt == 1 ? 15 : 2); }
+
+/* Reading M1: the E8M0 code of a block with maximum magnitude amax. */
+static uint8_t mx_scale_code(double amax, int fmt) {
+  int exponent = -127;
+  if (amax > 0.0) {
+    int e2;
+    frexp(amax, &e2); /* amax = m * 2^e2 with m in [0.5, 1): floor(log2(amax)) = e2 - 1 */
+    exponent = (e2 - 1) - mx_emax(fmt);
+  }
+  if (exponent < -127) exponent = -127;
+  if (exponent > 127) exponent = 127;
+  return (uint8_t)(exponent + 127);
+}
+
+/* Reading M2: one element, t = v / X. The division by a power of two is exact in double; the
+ * cast to float is exact too unless t lies far below every format's smallest subnormal
+ * (2^-16), where it rounds to a float that encodes to zero all the same. */
+static uint8_t mx_encode(double t, int fmt) {
+  float f = (float)t;
+  if (fmt == 0) return e4m3_encode_rn_satfinite(f);
+  if (fmt == 1) return e5m2_encode_rn_satfinite(f);
+  return e2m1_encode_rn_satfinite(f);
+}
+
+static double mx_decode(uint8_t code, int fmt) {
+  if (fmt == 0) return e4m3_decode(code);
+  if (fmt == 1) return e5m2_decode(code);
+  return e2m1_decode(code);
+}
+
+/* One 32-element block: its E8M0 code and element codes (FP8: 32 bytes; FP4: 16 bytes). */
+static void mx_quantize_block32(const double v[32], int fmt, uint8_t* codes, uint8_t* scale) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; i++)
+    if (fabs(v[i]) > amax) amax = fabs(v[i]);
+  uint8_t s = mx_scale_code(amax, fmt);
+  double X = e8m0_decode(s);
+  *scale = s;
+  for (int i = 0; i < 32; i++) {
+    uint8_t q = mx_encode(v[i] / X, fmt);
+    if (fmt == 2) {
+      if (i % 2 == 0) codes[i / 2] = q;
+      else codes[i / 2] |= (uint8_t)(q << 4);
+    } else {
+      codes[i] = q;
+    }
+  }
+}
+
+ORACLE_API uint8_t oracle_e5m2_encode(float v) { return e5m2_encode_rn_satfinite(v); }
+ORACLE_API float oracle_e5m2_decode(uint8_t c) { return e5m2_decode(c); }
+ORACLE_API double oracle_e8m0_decode(uint8_t c) { return e8m0_decode(c); }
+ORACLE_API uint8_t oracle_mx_scale(double amax, int32_t fmt) { return mx_scale_code(amax, fmt); }
+ORACLE_API uint8_t oracle_mx_encode(double t, int32_t fmt) { return mx_encode(t, fmt); }
+ORACLE_API double oracle_mx_decode(uint8_t code, int32_t fmt) { return mx_decode(code, fmt); }
+
+/* Rowwise MX quantization of BF16 x [M][N] (N % 32 == 0). Reading M3. */
+ORACLE_API void oracle_mx_quantize_rowwise(const uint16_t* x, int64_t M, int64_t N, int32_t fmt,
+                                           uint8_t* codes, uint8_t* scales) {
+  const int64_t code_row = fmt == 2 ? N / 2 : N;
+  const int64_t bytes_per_block = fmt == 2 ? 16 : 32;
+  for (int64_t m = 0; m < M; m++) {
+    for (int64_t b = 0; b < N / 32; b++) {
+      double v[32];
+      for (int i = 0; i < 32; i++) v[i] = bf16_to_f32(x[m * N + 32 * b + i]);
+      mx_quantize_block32(v, fmt, codes + m * code_row + b * bytes_per_block,
+                          scales + m * (N / 32) + b);
+    }
+  }
+}
+
+/* Columnwise MX quantization: the blocks are 32 consecutive rows of one column (M % 32 == 0);
+ * column n's codes and scales form row n of the transposed outputs. Reading M3. */
+ORACLE_API void oracle_mx_quantize_colwise(const uint16_t* x, int64_t M, int64_t N, int32_t fmt,
+                                           uint8_t* codes, uint8_t* scales) {
+  const int64_t code_row = fmt == 2 ? M / 2 : M;
+  const int64_t bytes_per_block = fmt == 2 ? 16 : 32;
+  for (int64_t n = 0; n < N; n++) {
+    for (int64_t b = 0; b < M / 32; b++) {
+      double v[32];
+      for (int i = 0; i < 32; i++) v[i] = bf16_to_f32(x[(32 * b + i) * N + n]);
+      mx_quantize_block32(v, fmt, codes + n * code_row + b * bytes_per_block,
+                          scales + n * (M / 32) + b);
+    }
+  }
+}
+
+/* MX dequantization: x_hat = decode(q) * 2^(s - 127), exact in double, stored as float.
+ * codes [R][C] (FP8) or [R][C/2] (FP4), scales [R][C/32], out [R][C]. */
+ORACLE_API void oracle_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int32_t fmt,
+                                     int64_t R, int64_t C, float* out) {
+  for (int64_t r = 0; r < R; r++) {
+    for (int64_t c = 0; c < C; c++) {
+      uint8_t q;
+      if (fmt == 2) {
+        uint8_t byte = codes[r * (C / 2) + c / 2];
+        q = (c % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      } else {
+        q = codes[r * C + c];
+      }
+      out[r * C + c] = (float)(mx_decode(q, fmt) * e8m0_decode(scales[r * (C / 32) + c / 32]));
+    }
+  }
+}
