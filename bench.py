@@ -483,6 +483,150 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+MX_METRIC = "MX quantize GB/s (BF16 in) and fraction of GB300 HBM roofline, 1 GPU"
+
+
+def mx_ideal_bytes(w, fmt, rows=None) -> int:
+    """One BF16 read + codes (1 byte per element for FP8, half for FP4) + E8M0 scales (1/32
+    byte per element) per produced orientation."""
+    M = w.rows if rows is None else rows
+    n = M * w.cols
+    per = (n // 2 if fmt == "e2m1" else n) + n // 32
+    return 2 * n + per * (int(w.rowwise) + int(w.columnwise))
+
+
+def mx_cpu_baseline(w, inp, fmt, budget_s=15.0):
+    """The oracle's MX functions on a bounded row sample, threads over 64-row chunks (blocks
+    are independent: no amax)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    xb = oracle.as_bf16_bits(inp["x"])
+
+    def run(rows, threads):
+        chunks = [xb[r:r + 64] for r in range(0, rows, 64)]
+
+        def one(c):
+            if w.rowwise:
+                oracle.mx_quantize_rowwise(c, fmt)
+            if w.columnwise:
+                oracle.mx_quantize_colwise(c, fmt)
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(max_workers=threads) as pool:
+            list(pool.map(one, chunks))
+        return time.perf_counter() - t0
+    rows = 64
+    dt = run(rows, 1)
+    while dt < budget_s / 8 and rows < w.rows:
+        rows = min(w.rows, rows * 4)
+        dt = run(rows, 1)
+    cores = host_cores()
+    rows = int(min(w.rows, max(64, rows * budget_s * cores / max(dt, 1e-6) // 64 * 64)))
+    dtn = run(rows, cores)
+    b = mx_ideal_bytes(w, fmt, rows)
+    return {"value": b / dtn / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "first %d of %d rows of %s, MX %s (every output): %.2f s on %d cores "
+                      "(threads over 64-row chunks)" % (rows, w.rows, w.name, fmt, dtn, cores)}
+
+
+def run_mx(args, world, rank, local):
+    """--mx FMT: the MX quantizer on the workload's shape and orientations (one launch per
+    step, no amax)."""
+    from nvfp4_block_scaled_quantize_gb300 import api, _lib
+    _lib.load()
+    dev = torch.device("cuda", local)
+    w = workloads.WORKLOADS[args.workload]
+    if w.grouped or w.block2d:
+        raise SystemExit("--mx runs on plain 1D workloads")
+    fmt = args.mx
+    inp = workloads.make_input(w)
+    x = inp["x"].to(dev)
+    ideal = mx_ideal_bytes(w, fmt)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = api.alloc_mx_outputs(w.rows, w.cols, dev, fmt, w.rowwise, w.columnwise)
+
+    def step():
+        api.nvfp4_mx_quantize(x, fmt, w.rowwise, w.columnwise, out=out)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        time.sleep(0.3)
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
+        status, bits = api.nvfp4_get_status(dev)
+        if status != 0:
+            raise RuntimeError("device status %d (bits %#x) after warm-up" % (status, bits))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        clocks.mark_start()
+        for i in range(args.steps):
+            flush.zero_()
+            events[i][0].record(stream)
+            step()
+            events[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark_end()
+        time.sleep(0.05)
+    barrier(world)
+    step_ms = [e[0].elapsed_time(e[1]) for e in events]
+    total_s = max_over_ranks(world, sum(step_ms) / 1e3)
+    value = ideal * args.steps * world / total_s / 1e9
+
+    # end to end: pinned host input -> device -> quantize -> pinned host outputs, one stream
+    x_host = inp["x"].pin_memory()
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = x_host.numel() * 2
+    d2h = sum(v.numel() for v in out.values())
+
+    def e2e_step():
+        xd = x_host.to(dev, non_blocking=True)
+        o = api.nvfp4_mx_quantize(xd, fmt, w.rowwise, w.columnwise, out=out)
+        for k, v in o.items():
+            host_out[k].copy_(v, non_blocking=True)
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = min(args.steps, 100)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(world, e0.elapsed_time(e1) / 1e3)
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    kus = statistics.mean(step_ms) * 1e3
+    achieved = ideal / (kus / 1e6) / 1e9
+    line = {
+        "metric": MX_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": [w.rows, w.cols], "format": "MX" + fmt,
+                   "rowwise": w.rowwise, "columnwise": w.columnwise,
+                   "ideal_bytes_per_step": ideal, "pipeline": "one launch (no amax)",
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gpu_launches": args.steps,
+        "e2e": {"value": ideal * e2e_steps * world / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": "nvfp4_mx_quantize, copies on the current stream"},
+        "clocks": clocks.summary(),
+        "step_us": {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
+                    "max": max(step_ms) * 1e3},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_kind": peak_kind,
+                     "kernel": "mx_quantize_kernel", "kernel_us": kus, "traffic": None},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = mx_cpu_baseline(w, inp, fmt)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -494,6 +638,8 @@ def main():
     p.add_argument("--pipeline", choices=["fused", "two_pass"], default="fused",
                    help="fused: amax and quantize in one launch; two_pass: amax kernel then "
                         "quantize kernel")
+    p.add_argument("--mx", choices=["e4m3", "e5m2", "e2m1"], default=None,
+                   help="time the MX quantizer (MXFP8 E4M3/E5M2, MXFP4) on the workload's shape")
     p.add_argument("--fast-math", action="store_true",
                    help="the fast-math variant (approximate reciprocal; FP32 RHT columnwise)")
     args = p.parse_args()
@@ -502,6 +648,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.mx:
+        run_mx(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

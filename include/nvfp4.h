@@ -213,6 +213,39 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const n
 nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, uint8_t* out,
                                   void* stream);
 
+/* MX formats ([Perplexity] "CuTeDSL at Perplexity", its Blackwell paragraph: MXFP8 and MXFP4
+ * beside NVFP4, with block maxima over 32 elements). Blocks of 32 consecutive elements share a
+ * power-of-two scale stored as E8M0 (value 2^(code - 127)); there is no tensor-wide scale.
+ * The scale and rounding rules are the OCP Microscaling Formats v1.0 conversion: exponent =
+ * floor(log2(block max)) - emax, emax = 8 (E4M3), 15 (E5M2), 2 (E2M1), at least -127 (an
+ * all-zero block gets code 0); elements are x / 2^exponent rounded to nearest-even, saturating
+ * at the format's largest magnitude (448, 57344, 6). Inputs must be finite. */
+typedef enum {
+  NVFP4_MX_E4M3 = 0, /* MXFP8, E4M3 elements, one byte each */
+  NVFP4_MX_E5M2 = 1, /* MXFP8, E5M2 elements, one byte each */
+  NVFP4_MX_E2M1 = 2  /* MXFP4, E2M1 elements, two per byte, the even element in the low nibble */
+} nvfp4_mx_format;
+
+/* MX quantization of a BF16 [M][N] row-major device tensor in one pass (no amax).
+ *   rowwise    (N % 32 == 0): row_codes [M][N] (FP8) or [M][N/2] (FP4), row_scales [M][N/32].
+ *   columnwise (M % 32 == 0, N % 8 == 0): the transposed tensor's, col_codes [N][M] or
+ *              [N][M/2], col_scales [N][M/32] (blocks are 32 consecutive rows of a column).
+ * Alignment: x 16 bytes; code buffers 32 bytes (FP8) or 16 bytes (FP4); row_scales 4 bytes.
+ * Buffers of an orientation not selected may be NULL. Asynchronous on `stream`; an empty
+ * tensor returns NVFP4_OK without a launch. Errors: NVFP4_ERR_INVALID_ARG (format, NULL
+ * buffers, negative sizes), NVFP4_ERR_UNSUPPORTED (neither orientation), NVFP4_ERR_SHAPE,
+ * NVFP4_ERR_ALIGN, NVFP4_ERR_CUDA; a device-side wait that gives up sets NVFP4_DEVICE_TIMEOUT. */
+nvfp4_status nvfp4_mx_quantize(const void* x, int64_t M, int64_t N, int32_t format,
+                               int32_t rowwise, int32_t columnwise, uint8_t* row_codes,
+                               uint8_t* row_scales, uint8_t* col_codes, uint8_t* col_scales,
+                               void* stream);
+
+/* out[r][c] = element(code) * 2^(scale - 127) in binary32 (one rounding of the exact product)
+ * for codes [R][C] (FP8) or [R][C/2] (FP4) and scales [R][C/32]; C % 32 == 0; codes and out
+ * 16-byte aligned. */
+nvfp4_status nvfp4_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int32_t format,
+                                 int64_t R, int64_t C, float* out, void* stream);
+
 /* Synchronize `stream`, then read and clear the current device's status word into
  * *device_status (NVFP4_DEVICE_* bits). Returns NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT
  * when bits were set, NVFP4_OK otherwise. */

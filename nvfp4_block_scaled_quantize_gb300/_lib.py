@@ -22,7 +22,8 @@ DEVICE_TIMEOUT = 0x2
 EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped",
             "nvfp4_dequantize", "nvfp4_get_status", "nvfp4_quantize_noalloc",
             "nvfp4_host_pipeline_create", "nvfp4_host_pipeline_submit",
-            "nvfp4_host_pipeline_join", "nvfp4_host_pipeline_destroy", "nvfp4_swizzle_scales"]
+            "nvfp4_host_pipeline_join", "nvfp4_host_pipeline_destroy", "nvfp4_swizzle_scales",
+            "nvfp4_mx_quantize", "nvfp4_mx_dequantize"]
 
 
 class Config(ctypes.Structure):
@@ -93,6 +94,10 @@ def load(build_if_missing: bool = False):
     L.nvfp4_host_pipeline_destroy.argtypes = [vp]
     L.nvfp4_swizzle_scales.restype = ctypes.c_int
     L.nvfp4_swizzle_scales.argtypes = [vp, i64, i64, vp, vp]
+    L.nvfp4_mx_quantize.restype = ctypes.c_int
+    L.nvfp4_mx_quantize.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.nvfp4_mx_dequantize.restype = ctypes.c_int
+    L.nvfp4_mx_dequantize.argtypes = [vp, vp, i32, i64, i64, vp, vp]
     L.nvfp4_get_status.restype = ctypes.c_int
     L.nvfp4_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     _lib = L

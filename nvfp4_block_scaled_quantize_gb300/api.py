@@ -161,6 +161,56 @@ def nvfp4_swizzle_scales(scales):
     return out
 
 
+MX_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
+
+
+def _mx_format(fmt):
+    if fmt in MX_FORMATS:
+        return MX_FORMATS[fmt]
+    raise ValueError("MX format must be one of %s" % sorted(MX_FORMATS))
+
+
+def alloc_mx_outputs(M, N, device, fmt="e4m3", rowwise=True, columnwise=False):
+    """Output buffers of nvfp4_mx_quantize (torch.empty on `device`)."""
+    fp4 = _mx_format(fmt) == MX_FORMATS["e2m1"]
+    out = {}
+    if rowwise:
+        out["row_codes"] = torch.empty((M, N // 2 if fp4 else N), dtype=torch.uint8, device=device)
+        out["row_scales"] = torch.empty((M, N // 32), dtype=torch.uint8, device=device)
+    if columnwise:
+        out["col_codes"] = torch.empty((N, M // 2 if fp4 else M), dtype=torch.uint8, device=device)
+        out["col_scales"] = torch.empty((N, M // 32), dtype=torch.uint8, device=device)
+    return out
+
+
+def nvfp4_mx_quantize(x, fmt="e4m3", rowwise=True, columnwise=False, out=None):
+    """MX quantization (MXFP8 "e4m3" / "e5m2", MXFP4 "e2m1") of a BF16 [M, N] CUDA tensor:
+    codes and E8M0 scales (uint8), rowwise and/or columnwise (transposed)."""
+    _check_x(x)
+    L = _lib.load()
+    M, N = x.shape
+    f = _mx_format(fmt)
+    if out is None:
+        out = alloc_mx_outputs(M, N, x.device, fmt, rowwise, columnwise)
+    _raise_if(L.nvfp4_mx_quantize(_ptr(x), M, N, f, int(bool(rowwise)), int(bool(columnwise)),
+                                  _ptr(out.get("row_codes")), _ptr(out.get("row_scales")),
+                                  _ptr(out.get("col_codes")), _ptr(out.get("col_scales")),
+                                  _stream(x.device)), "nvfp4_mx_quantize")
+    return out
+
+
+def nvfp4_mx_dequantize(codes, scales, fmt="e4m3"):
+    """FP32 [R, C] values of MX codes [R, C] (FP8) or [R, C/2] (FP4) and scales [R, C/32]."""
+    L = _lib.load()
+    f = _mx_format(fmt)
+    R = codes.shape[0]
+    C = codes.shape[1] * (2 if f == MX_FORMATS["e2m1"] else 1)
+    out = torch.empty((R, C), dtype=torch.float32, device=codes.device)
+    _raise_if(L.nvfp4_mx_dequantize(_ptr(codes), _ptr(scales), f, R, C, _ptr(out),
+                                    _stream(codes.device)), "nvfp4_mx_dequantize")
+    return out
+
+
 def nvfp4_get_status(device=None):
     """Synchronize the current stream and return (status, device status bits); clears them."""
     L = _lib.load()

@@ -121,6 +121,7 @@ cudaError_t prepare_quantize_kernels() {
   if ((r = prepare_quantize_rowcol_rht()) != cudaSuccess) e = r;
   if ((r = prepare_quantize_2d()) != cudaSuccess) e = r;
   if ((r = prepare_amax_tiles()) != cudaSuccess) e = r;
+  if ((r = prepare_mx_kernels()) != cudaSuccess) e = r;
   return e;
 }
 
@@ -387,6 +388,67 @@ NVFP4_EXPORT nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t R,
   const int64_t chunks = ((R + 127) / 128) * ((C + 3) / 4) * 32;
   return cuda_status(launch_swizzle_scales(scales, R, C, out, amax_grid(ds, chunks, 256),
                                            static_cast<cudaStream_t>(stream)));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_mx_quantize(const void* x, int64_t M, int64_t N, int32_t format,
+                                            int32_t rowwise, int32_t columnwise,
+                                            uint8_t* row_codes, uint8_t* row_scales,
+                                            uint8_t* col_codes, uint8_t* col_scales,
+                                            void* stream) {
+  if (format < NVFP4_MX_E4M3 || format > NVFP4_MX_E2M1 || M < 0 || N < 0)
+    return NVFP4_ERR_INVALID_ARG;
+  const bool row = rowwise != 0, col = columnwise != 0;
+  if (!row && !col) return NVFP4_ERR_UNSUPPORTED;
+  if ((row && N % 32 != 0) || (col && (M % 32 != 0 || N % 8 != 0))) return NVFP4_ERR_SHAPE;
+  if (M > INT32_MAX - kMxUnitM || N > INT32_MAX - kMxUnitN ||
+      ((M + kMxUnitM - 1) / kMxUnitM) * ((N + kMxUnitN - 1) / kMxUnitN) > INT32_MAX / 2)
+    return NVFP4_ERR_SHAPE;
+  if (M * N == 0) return NVFP4_OK;
+  if (x == nullptr || (row && (row_codes == nullptr || row_scales == nullptr)) ||
+      (col && (col_codes == nullptr || col_scales == nullptr)))
+    return NVFP4_ERR_INVALID_ARG;
+  const uintptr_t code_align = format == NVFP4_MX_E2M1 ? 16 : 32;  // one block per store
+  if (!aligned(x, 16) || (row && (!aligned(row_codes, code_align) || !aligned(row_scales, 4))) ||
+      (col && !aligned(col_codes, code_align)))
+    return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  MxArgs a;
+  std::memset(&a, 0, sizeof a);
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kMxUnitM};  // 128-byte rows: the 128-byte swizzle span
+  cuuint32_t estr[2] = {1, 1};
+  if (g_encode(&a.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return NVFP4_ERR_CUDA;
+  a.rows = M; a.cols = N;
+  a.row_codes = row ? row_codes : nullptr; a.row_scales = row ? row_scales : nullptr;
+  a.col_codes = col ? col_codes : nullptr; a.col_scales = col ? col_scales : nullptr;
+  a.status = ds->workspace;
+  const int64_t units = ((M + kMxUnitM - 1) / kMxUnitM) * ((N + kMxUnitN - 1) / kMxUnitN);
+  const int64_t ctas = (units + kMxWarps - 1) / kMxWarps;
+  const int grid = (int)(ctas < ds->sm_count ? ctas : ds->sm_count);
+  return cuda_status(launch_mx_quantize(format, row, col, a, grid, static_cast<cudaStream_t>(stream)));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_mx_dequantize(const uint8_t* codes, const uint8_t* scales,
+                                              int32_t format, int64_t R, int64_t C, float* out,
+                                              void* stream) {
+  if (format < NVFP4_MX_E4M3 || format > NVFP4_MX_E2M1 || R < 0 || C < 0)
+    return NVFP4_ERR_INVALID_ARG;
+  if (C % 32 != 0) return NVFP4_ERR_SHAPE;
+  if (R * C == 0) return NVFP4_OK;
+  if (codes == nullptr || scales == nullptr || out == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(out, 16)) return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  return cuda_status(launch_mx_dequantize(format, codes, scales, R, C, out,
+                                          amax_grid(ds, R * (C / 32), 256),
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status) {

@@ -119,3 +119,23 @@ def test_swizzle_argument_checks_return_before_any_cuda_call(L):
     assert L.nvfp4_swizzle_scales(None, 0, 4, None, None) == 0           # empty: nothing to do
     assert L.nvfp4_swizzle_scales(None, 4, 4, p(FAKE), None) == 1
     assert L.nvfp4_swizzle_scales(p(FAKE), 4, 4, p(FAKE + 8), None) == 3  # misaligned output
+
+
+def test_mx_argument_checks_return_before_any_cuda_call(L):
+    p = ctypes.c_void_p
+    q = lambda M, N, fmt=0, row=1, col=0, x=FAKE, out=FAKE: L.nvfp4_mx_quantize(
+        p(x), M, N, fmt, row, col, p(out), p(out), p(out), p(out), None)
+    assert q(32, 32, fmt=3) == 1 and q(32, 32, fmt=-1) == 1     # no such format
+    assert q(-1, 32) == 1
+    assert q(32, 32, row=0, col=0) == 4                          # neither orientation
+    assert q(32, 48) == 2                                        # rowwise: N % 32
+    assert q(48, 32, row=0, col=1) == 2                          # columnwise: M % 32
+    assert q(32, 36, row=0, col=1) == 2                          # columnwise: N % 8 (TMA pitch)
+    assert q(0, 32) == 0                                         # empty: nothing to do
+    assert q(32, 32, x=0) == 1                                   # NULL input
+    assert q(32, 32, x=FAKE + 8) == 3                            # input not 16-byte aligned
+    assert q(32, 32, out=FAKE + 16) == 3                         # FP8 codes need 32 bytes
+    assert L.nvfp4_mx_dequantize(p(FAKE), p(FAKE), 0, 4, 48, p(FAKE), None) == 2   # C % 32
+    assert L.nvfp4_mx_dequantize(p(FAKE), p(FAKE), 5, 4, 32, p(FAKE), None) == 1
+    assert L.nvfp4_mx_dequantize(None, None, 0, 0, 32, None, None) == 0           # empty
+    assert L.nvfp4_mx_dequantize(p(FAKE + 8), p(FAKE), 0, 4, 32, p(FAKE), None) == 3
