@@ -416,21 +416,51 @@ NVFP4_EXPORT nvfp4_status nvfp4_mx_quantize(const void* x, int64_t M, int64_t N,
   if (st != NVFP4_OK) return st;
   MxArgs a;
   std::memset(&a, 0, sizeof a);
-  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
-  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kMxUnitM};  // 128-byte rows: the 128-byte swizzle span
-  cuuint32_t estr[2] = {1, 1};
-  if (g_encode(&a.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  // x: 32 x 64 BF16 boxes (128-byte rows: the 128-byte swizzle span); outputs: byte tensors
+  // stored from swizzled staging, one box per unit and orientation
+  auto encode = [&](CUtensorMap* map, CUtensorMapDataType type, const void* p, int64_t inner,
+                    int64_t rows, int64_t pitch, uint32_t box_inner, uint32_t box_rows,
+                    CUtensorMapSwizzle swizzle) {
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, type, 2, const_cast<void*>(p), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  // column codes [N][Mb] (Mb bytes per column) as a 3D tensor {Mb, N/4, 4}: column 4 g + j at
+  // (., g, j); a unit's box {32 (FP4: 16), 32, 4} is staged as [j][g][row], which the kernel
+  // writes without shared-memory bank conflicts
+  auto encode_col_codes = [&](CUtensorMap* map, void* p, int64_t mb, int64_t n, bool fp4_) {
+    cuuint64_t dims[3] = {(cuuint64_t)mb, (cuuint64_t)(n / 4), 4};
+    cuuint64_t strides[2] = {(cuuint64_t)(4 * mb), (cuuint64_t)mb};
+    cuuint32_t box[3] = {fp4_ ? 16u : 32u, (cuuint32_t)(kMxUnitN / 4), 4};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    fp4_ ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_32B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+  };
+  const bool fp4 = format == NVFP4_MX_E2M1;
+  // each box's swizzle span is its row: 128 bytes for x and FP8 row codes, 64 for FP4 row
+  // codes, 32 for FP8 column codes, none for the 16-byte rows of FP4 column codes
+  if (!encode(&a.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, N, M, N * 2, 64, kMxUnitM,
+              CU_TENSOR_MAP_SWIZZLE_128B) ||
+      (row && !encode(&a.tmap_row, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_codes, fp4 ? N / 2 : N, M,
+                      fp4 ? N / 2 : N, fp4 ? 64 : 128, kMxUnitM,
+                      fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) ||
+      (col && !encode_col_codes(&a.tmap_col, col_codes, fp4 ? M / 2 : M, N, fp4)))
     return NVFP4_ERR_CUDA;
   a.rows = M; a.cols = N;
   a.row_codes = row ? row_codes : nullptr; a.row_scales = row ? row_scales : nullptr;
   a.col_codes = col ? col_codes : nullptr; a.col_scales = col ? col_scales : nullptr;
   a.status = ds->workspace;
-  const int64_t units = ((M + kMxUnitM - 1) / kMxUnitM) * ((N + kMxUnitN - 1) / kMxUnitN);
-  const int64_t ctas = (units + kMxWarps - 1) / kMxWarps;
-  const int grid = (int)(ctas < ds->sm_count ? ctas : ds->sm_count);
+  // one CTA per SM at most; a CTA round is kMxWarps vertically adjacent units
+  const int64_t units_m = (M + kMxUnitM - 1) / kMxUnitM;
+  const int64_t groups = ((units_m + kMxWarps - 1) / kMxWarps) * ((N + kMxUnitN - 1) / kMxUnitN);
+  const int grid = (int)(groups < ds->sm_count ? groups : ds->sm_count);
   return cuda_status(launch_mx_quantize(format, row, col, a, grid, static_cast<cudaStream_t>(stream)));
 }
 

@@ -104,16 +104,20 @@ cudaError_t prepare_quantize_2d();
 
 // ---- MX formats (mx_kernel.cu): 32-element blocks, E8M0 scales, no tensor scale ----
 // A warp quantizes 32 x 128 units alone, kMxStages of them in flight in its own ring; a unit is
-// two TMA boxes of 32 rows x 64 BF16 columns (128-byte rows, 128-byte swizzle).
+// two TMA boxes of 32 rows x 64 BF16 columns (128-byte rows, 128-byte swizzle). Its codes are
+// staged in kMxOutBytes of shared memory per warp and leave by TMA stores.
 constexpr int kMxUnitM = 32;
 constexpr int kMxUnitN = 128;
 constexpr int kMxWarps = 8;
-constexpr int kMxStages = 3;
-constexpr int kMxSmemBytes =
-    kMxWarps * kMxStages * (kMxUnitM * kMxUnitN * 2) + kMxWarps * kMxStages * 8 + 1024;
+constexpr int kMxStages = 2;
+constexpr int kMxOutBytes = 8192;  // row codes, then column codes: 4 KiB each (FP8)
+constexpr int kMxSmemBytes = kMxWarps * (kMxStages * (kMxUnitM * kMxUnitN * 2) + kMxOutBytes) +
+                             2 * kMxWarps * kMxUnitN + kMxWarps * kMxStages * 8 + 1024;
 
 struct MxArgs {
   CUtensorMap tmap;        // x as BF16 [rows][cols], box {64, 32}, 128-byte swizzle
+  CUtensorMap tmap_row;    // row codes as bytes, box {128 (FP4: 64), 32}, swizzle span = row
+  CUtensorMap tmap_col;    // column codes as bytes {M, N/4, 4}, box {32 (FP4: 16), 32, 4}
   int64_t rows, cols;
   uint8_t* row_codes;      // [rows][cols] FP8 or [rows][cols / 2] FP4
   uint8_t* row_scales;     // [rows][cols / 32] E8M0
