@@ -75,6 +75,9 @@ def lib():
                                                        ctypes.c_uint64, ctypes.c_uint32,
                                                        _u8p, _u8p, _f32p, _u8p, _u8p, _f32p]),
             "oracle_dequantize": (None, [_u8p, _u8p, ctypes.c_float, _i64, _i64, _f32p]),
+            "oracle_inverse_rht16": (None, [_f32p, ctypes.c_uint32, _f32p]),
+            "oracle_inverse_rht_rows": (None, [_f32p, _i64, _i64, ctypes.c_uint32]),
+            "oracle_f32_to_bf16_n": (None, [_f32p, _i64, _u16p]),
             "oracle_e5m2_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "oracle_e5m2_decode": (ctypes.c_float, [ctypes.c_uint8]),
             "oracle_e8m0_decode": (ctypes.c_double, [ctypes.c_uint8]),
@@ -307,6 +310,32 @@ def dequantize(codes, scales, s_dec) -> np.ndarray:
     lib().oracle_dequantize(_ptr(c, _u8p), _ptr(s, _u8p), float(np.float32(s_dec)), R, C,
                             _ptr(out, _f32p))
     return out
+
+
+def inverse_rht16(y, sign_mask: int) -> np.ndarray:
+    """v = d * (0.25 * FWHT16(y)) in binary32 (reading R13)."""
+    a = np.ascontiguousarray(y, dtype=np.float32)
+    v = np.zeros(16, dtype=np.float32)
+    lib().oracle_inverse_rht16(_ptr(a, _f32p), sign_mask, _ptr(v, _f32p))
+    return v
+
+
+def f32_to_bf16_array(values) -> np.ndarray:
+    """binary32 -> BF16 bit patterns (uint16), round to nearest-even, any shape."""
+    a = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.zeros(a.shape, dtype=np.uint16)
+    lib().oracle_f32_to_bf16_n(_ptr(a, _f32p), a.size, _ptr(out, _u16p))
+    return out
+
+
+def dequantize_ex(codes, scales, s_dec, inverse_rht=False, sign_mask=0, bf16=False):
+    """dequantize(), then optionally the inverse RHT of every 16-element block of every row
+    (columnwise RHT outputs) and optionally BF16 rounding (bit patterns as uint16)."""
+    out = dequantize(codes, scales, s_dec)
+    if inverse_rht:
+        R, C = out.shape
+        lib().oracle_inverse_rht_rows(_ptr(out, _f32p), R, C, sign_mask)
+    return f32_to_bf16_array(out) if bf16 else out
 
 
 def swizzle_scales(scales) -> np.ndarray:

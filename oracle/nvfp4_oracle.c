@@ -566,6 +566,44 @@ ORACLE_API void oracle_dequantize(const uint8_t* codes, const uint8_t* scales, f
   }
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* Verification at the GEMM boundary: BF16 dequantization and the inverse RHT.                */
+/*   R13 The columnwise RHT output y of a 16-element block is undone as v = d * (0.25 *       */
+/*       FWHT16(y)) in binary32 with the same butterflies as R6 (H16 H16 = 16 I, so 0.25 H16  */
+/*       is its own inverse, and so is d). Applied to dequantized values it reconstructs the  */
+/*       pre-transform column up to the quantization error. BF16 outputs are the binary32    */
+/*       results rounded to nearest-even.                                                      */
+/* ------------------------------------------------------------------------------------------ */
+
+static void inverse_rht16(const float y[16], uint32_t sign_mask, float v[16]) {
+  float w[16];
+  for (int i = 0; i < 16; i++) w[i] = y[i];
+  fwht16(w);
+  for (int i = 0; i < 16; i++) {
+    float scaled = 0.25f * w[i];
+    v[i] = ((sign_mask >> i) & 1u) ? -scaled : scaled;
+  }
+}
+
+ORACLE_API void oracle_inverse_rht16(const float y[16], uint32_t sign_mask, float v[16]) {
+  inverse_rht16(y, sign_mask, v);
+}
+
+/* In place on x [R][C] (C % 16 == 0): every 16-element block of every row. */
+ORACLE_API void oracle_inverse_rht_rows(float* x, int64_t R, int64_t C, uint32_t sign_mask) {
+  for (int64_t r = 0; r < R; r++) {
+    for (int64_t b = 0; b < C / 16; b++) {
+      float v[16];
+      inverse_rht16(x + r * C + 16 * b, sign_mask, v);
+      for (int i = 0; i < 16; i++) x[r * C + 16 * b + i] = v[i];
+    }
+  }
+}
+
+ORACLE_API void oracle_f32_to_bf16_n(const float* in, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; i++) out[i] = f32_to_bf16_rne(in[i]);
+}
+
 /* ========================================================================================== */
 /* MX formats: MXFP8 (E4M3 or E5M2 elements) and MXFP4 (E2M1 elements). Blocks of 32         */
 /* consecutive elements share one power-of-two scale stored as E8M0; there is no tensor-wide   */

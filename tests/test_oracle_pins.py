@@ -545,3 +545,59 @@ def test_swizzled_scales_are_a_permutation_padded_with_zeros():
         nz = out[out != 0]
         assert len(nz) == R * C
         assert np.array_equal(np.sort(nz), np.arange(1, R * C + 1, dtype=np.uint8))
+
+
+# ------------------------------------------------------------------------------------------
+# Verification at the GEMM boundary: inverse RHT and BF16 dequantization (reading R13)
+# ------------------------------------------------------------------------------------------
+
+def _sylvester16():
+    h = np.array([[1.0]])
+    for _ in range(4):
+        h = np.kron(np.array([[1.0, 1.0], [1.0, -1.0]]), h)
+    return h
+
+
+def test_inverse_rht_equals_dense_product_on_exact_inputs():
+    H = _sylvester16()
+    rng = np.random.default_rng(41)
+    for mask in (0x0000, 0xFFFF, 0x1234, 0xB3C5):
+        d = np.array([-1.0 if (mask >> i) & 1 else 1.0 for i in range(16)])
+        y = rng.integers(-64, 65, size=16).astype(np.float64)
+        want = d * (0.25 * (H @ y))        # small integers: every binary32 step is exact
+        assert np.array_equal(oracle.inverse_rht16(y, mask).astype(np.float64), want), mask
+
+
+def test_inverse_rht_undoes_the_rht_when_its_bf16_rounding_is_exact():
+    rng = np.random.default_rng(42)
+    for mask in (0x0F0F, 0x5A3C, 0xFFFF):
+        v = rng.integers(-7, 8, size=16).astype(np.float32)  # 0.25 H (d v): <= 8 significant bits
+        assert np.array_equal(oracle.inverse_rht16(oracle.rht16(v, mask), mask), v), mask
+
+
+def test_f32_to_bf16_array_matches_torch_including_ties():
+    rng = np.random.default_rng(43)
+    bits = rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64).astype(np.uint32)
+    bits[:2000] = (bits[:2000] & 0xFFFF0000) | 0x8000      # exact ties
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.f32_to_bf16_array(x), ref)
+
+
+def test_inverse_rht_dequantization_keeps_the_transformed_domain_error():
+    """0.25 H16 d is orthogonal, so the columnwise reconstruction error of an RHT-quantized
+    tensor is the quantization error of the transformed values (up to their BF16 rounding)."""
+    x = workloads.normal_with_outliers(256, 96, seed=44, fraction=0.01, gain=20.0)
+    mask = 0x6A5C
+    cc, cs, gs = oracle.quantize_colwise(x, rht=True, sign_mask=mask)
+    xt = x.float().numpy().T.astype(np.float64)            # [N][M]: the columns of x
+    rec = oracle.dequantize_ex(cc, cs, gs[1], inverse_rht=True, sign_mask=mask).astype(np.float64)
+    yq = oracle.dequantize(cc, cs, gs[1]).astype(np.float64)  # transformed domain
+    y = np.stack([np.concatenate([oracle.rht16(xt[n, 16 * b:16 * b + 16].astype(np.float32), mask)
+                                  for b in range(xt.shape[1] // 16)]) for n in range(xt.shape[0])])
+    err_x = ((rec - xt) ** 2).sum()
+    err_y = ((yq - y) ** 2).sum()
+    assert abs(err_x / err_y - 1.0) < 0.02, (err_x, err_y)
+    db = 10 * np.log10((xt ** 2).sum() / err_x)
+    assert 15.0 < db < 22.0, db
