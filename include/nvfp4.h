@@ -173,6 +173,21 @@ nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
 nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
                               int64_t R, int64_t C, float* out, void* stream);
 
+/* Dequantization for checks at the GEMM boundary ([PR4798]: columnwise operands carry the
+ * 16-point RHT, "Config surface and AUTO"; the reconstruction of "Correctness"): as
+ * nvfp4_dequantize, then
+ *   inverse_rht = 1: every 16-element block of a row (a columnwise output: 16 consecutive
+ *     tokens of one column) goes through the inverse transform v = d * (0.25 * FWHT16(y)),
+ *     d_i = -1 where bit i of rht_sign_mask is set, binary32 butterflies in stages 1, 2, 4, 8
+ *     (0.25 H16 is its own inverse), which returns the pre-transform column up to the
+ *     quantization error;
+ *   out_bf16 = 1: out is BF16 [R][C] (round to nearest-even), else float [R][C].
+ * out 16-byte aligned, codes 8-byte aligned; C % 16 == 0. Errors: NVFP4_ERR_INVALID_ARG for
+ * flags other than 0/1, a mask above 0xFFFF or NULL buffers; NVFP4_ERR_SHAPE; NVFP4_ERR_ALIGN. */
+nvfp4_status nvfp4_dequantize_ex(const uint8_t* codes, const uint8_t* scales, const float* gscale,
+                                 int64_t R, int64_t C, int32_t inverse_rht, uint32_t rht_sign_mask,
+                                 int32_t out_bf16, void* out, void* stream);
+
 /* nvfp4_quantize with fused_amax, for callers that cannot allocate device memory: code that
  * runs inside a memory allocator's own callbacks, a latency-critical path that must never
  * reach cudaMalloc (it can synchronize the whole device), or a host that gives this library a

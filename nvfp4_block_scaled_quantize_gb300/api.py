@@ -149,6 +149,20 @@ def nvfp4_dequantize(codes, scales, gscale):
     return out
 
 
+def nvfp4_dequantize_ex(codes, scales, gscale, inverse_rht=False, sign_mask=0, bf16=False):
+    """nvfp4_dequantize, then optionally the inverse RHT of every 16-element block of every row
+    (columnwise RHT outputs) and BF16 rounding: FP32 or BF16 [R, C]."""
+    L = _lib.load()
+    R, half = codes.shape
+    C = 2 * half
+    out = torch.empty((R, C), dtype=torch.bfloat16 if bf16 else torch.float32,
+                      device=codes.device)
+    _raise_if(L.nvfp4_dequantize_ex(_ptr(codes), _ptr(scales), _ptr(gscale), R, C,
+                                    int(bool(inverse_rht)), int(sign_mask), int(bool(bf16)),
+                                    _ptr(out), _stream(codes.device)), "nvfp4_dequantize_ex")
+    return out
+
+
 def nvfp4_swizzle_scales(scales):
     """uint8 [R, C] E4M3 scales -> the flat 128 x 4 tiled layout of the block-scaled GEMMs."""
     L = _lib.load()

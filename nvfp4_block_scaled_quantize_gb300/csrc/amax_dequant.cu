@@ -4,6 +4,8 @@
 // Page cited: "[nvfp4_training] Optimize CuteDSL kernels for NVFP4 training" (pytorch/ao pull
 // request #4798): the amax pre-pass ("Optimization" item 5: "Linear RHT amax"; "Performance":
 // grouped amax) and the dequantized reconstruction its "Correctness" section measures SQNR on.
+#include <cuda_bf16.h>
+
 #include "nvfp4_device.cuh"
 #include "nvfp4_internal.h"
 
@@ -67,11 +69,15 @@ __device__ __forceinline__ float e2m1_value(uint32_t nib) {
   return (nib & 8u) ? -mag : mag;
 }
 
-// out[r][c] = (e2m1(code) * e4m3(scale)) * S_dec, one 16-element block per step.
+// out[r][c] = (e2m1(code) * e4m3(scale)) * S_dec, one 16-element block per step. RHT: then the
+// inverse 16-point RHT of the block, v = d * (0.25 * FWHT16(y)) with the forward butterflies
+// (stages 1, 2, 4, 8; (a, b) -> (a + b, a - b)); BF16: the results rounded to nearest-even.
+template <bool RHT, bool BF16>
 __global__ void __launch_bounds__(256) dequantize_kernel(const uint8_t* __restrict__ codes,
                                                          const uint8_t* __restrict__ scales,
                                                          const float* __restrict__ gscale,
-                                                         int64_t R, int64_t C, float* out) {
+                                                         int64_t R, int64_t C, uint32_t sign_mask,
+                                                         void* out) {
   const float s_dec = gscale[1];
   const int64_t nbc = C / 16;
   const int64_t nblk = R * nbc;
@@ -87,9 +93,39 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint8_t* __restri
       const uint32_t nib = (word >> (4 * (i & 7))) & 0xFu;
       v[i] = __fmul_rn(__fmul_rn(e2m1_value(nib), s), s_dec);
     }
-    float4* o = reinterpret_cast<float4*>(out + r * C + 16 * k);
+    if (RHT) {
 #pragma unroll
-    for (int i = 0; i < 4; i++) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+          if ((i & h) == 0) {
+            const float x0 = v[i], x1 = v[i + h];
+            v[i] = __fadd_rn(x0, x1);
+            v[i + h] = __fsub_rn(x0, x1);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; i++) {
+        const float t = __fmul_rn(0.25f, v[i]);
+        v[i] = ((sign_mask >> i) & 1u) ? -t : t;
+      }
+    }
+    if (BF16) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&p2);
+      }
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + r * C + 16 * k);
+      o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + r * C + 16 * k);
+#pragma unroll
+      for (int i = 0; i < 4; i++) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
   }
 }
 
@@ -140,8 +176,16 @@ cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float*
 }
 
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
-                              int64_t R, int64_t C, float* out, int grid, cudaStream_t s) {
-  dequantize_kernel<<<grid, 256, 0, s>>>(codes, scales, gscale, R, C, out);
+                              int64_t R, int64_t C, bool inverse_rht, uint32_t sign_mask,
+                              bool out_bf16, void* out, int grid, cudaStream_t s) {
+  if (inverse_rht && out_bf16)
+    dequantize_kernel<true, true><<<grid, 256, 0, s>>>(codes, scales, gscale, R, C, sign_mask, out);
+  else if (inverse_rht)
+    dequantize_kernel<true, false><<<grid, 256, 0, s>>>(codes, scales, gscale, R, C, sign_mask, out);
+  else if (out_bf16)
+    dequantize_kernel<false, true><<<grid, 256, 0, s>>>(codes, scales, gscale, R, C, sign_mask, out);
+  else
+    dequantize_kernel<false, false><<<grid, 256, 0, s>>>(codes, scales, gscale, R, C, sign_mask, out);
   return cudaGetLastError();
 }
 

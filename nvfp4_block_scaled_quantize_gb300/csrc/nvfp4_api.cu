@@ -371,7 +371,28 @@ NVFP4_EXPORT nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* 
   DeviceState* ds = nullptr;
   nvfp4_status st = device_state(&ds);
   if (st != NVFP4_OK) return st;
-  return cuda_status(launch_dequantize(codes, scales, gscale, R, C, out,
+  return cuda_status(launch_dequantize(codes, scales, gscale, R, C, false, 0u, false, out,
+                                       amax_grid(ds, R * (C / 16), 256),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_dequantize_ex(const uint8_t* codes, const uint8_t* scales,
+                                              const float* gscale, int64_t R, int64_t C,
+                                              int32_t inverse_rht, uint32_t rht_sign_mask,
+                                              int32_t out_bf16, void* out, void* stream) {
+  if (R < 0 || C < 0 || (inverse_rht != 0 && inverse_rht != 1) || (out_bf16 != 0 && out_bf16 != 1) ||
+      rht_sign_mask > 0xFFFFu)
+    return NVFP4_ERR_INVALID_ARG;
+  if (C % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (R * C == 0) return NVFP4_OK;
+  if (codes == nullptr || scales == nullptr || gscale == nullptr || out == nullptr)
+    return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(codes, 8) || !aligned(gscale, 4) || !aligned(out, 16)) return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  return cuda_status(launch_dequantize(codes, scales, gscale, R, C, inverse_rht != 0,
+                                       rht_sign_mask, out_bf16 != 0, out,
                                        amax_grid(ds, R * (C / 16), 256),
                                        static_cast<cudaStream_t>(stream)));
 }

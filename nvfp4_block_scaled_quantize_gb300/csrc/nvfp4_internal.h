@@ -137,6 +137,7 @@ cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float*
 cudaError_t launch_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, uint8_t* out,
                                   int grid, cudaStream_t s);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,
-                              int64_t R, int64_t C, float* out, int grid, cudaStream_t s);
+                              int64_t R, int64_t C, bool inverse_rht, uint32_t sign_mask,
+                              bool out_bf16, void* out, int grid, cudaStream_t s);
 
 }  // namespace nvfp4

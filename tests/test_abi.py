@@ -139,3 +139,14 @@ def test_mx_argument_checks_return_before_any_cuda_call(L):
     assert L.nvfp4_mx_dequantize(p(FAKE), p(FAKE), 5, 4, 32, p(FAKE), None) == 1
     assert L.nvfp4_mx_dequantize(None, None, 0, 0, 32, None, None) == 0           # empty
     assert L.nvfp4_mx_dequantize(p(FAKE + 8), p(FAKE), 0, 4, 32, p(FAKE), None) == 3
+
+
+def test_dequantize_ex_argument_checks_return_before_any_cuda_call(L):
+    p = ctypes.c_void_p
+    d = lambda R, C, rht=0, mask=0, bf=0, out=FAKE: L.nvfp4_dequantize_ex(
+        p(FAKE), p(FAKE), p(FAKE), R, C, rht, mask, bf, p(out), None)
+    assert d(4, 24) == 2                                    # C % 16
+    assert d(4, 32, rht=2) == 1 and d(4, 32, bf=-1) == 1    # flags are 0 or 1
+    assert d(4, 32, mask=0x10000) == 1
+    assert d(0, 32) == 0                                    # empty
+    assert d(4, 32, out=FAKE + 8) == 3                      # output not 16-byte aligned
