@@ -78,6 +78,9 @@ def lib():
             "oracle_inverse_rht16": (None, [_f32p, ctypes.c_uint32, _f32p]),
             "oracle_inverse_rht_rows": (None, [_f32p, _i64, _i64, ctypes.c_uint32]),
             "oracle_f32_to_bf16_n": (None, [_f32p, _i64, _u16p]),
+            "oracle_rsqrt_rn": (ctypes.c_float, [ctypes.c_float]),
+            "oracle_rmsnorm": (ctypes.c_float, [_u16p, _u16p, _i64, _i64, ctypes.c_float,
+                                                ctypes.c_float, _u16p]),
             "oracle_e5m2_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "oracle_e5m2_decode": (ctypes.c_float, [ctypes.c_uint8]),
             "oracle_e8m0_decode": (ctypes.c_double, [ctypes.c_uint8]),
@@ -336,6 +339,23 @@ def dequantize_ex(codes, scales, s_dec, inverse_rht=False, sign_mask=0, bf16=Fal
         R, C = out.shape
         lib().oracle_inverse_rht_rows(_ptr(out, _f32p), R, C, sign_mask)
     return f32_to_bf16_array(out) if bf16 else out
+
+
+def rsqrt_rn(a: float) -> np.float32:
+    """1/sqrt(a) correctly rounded to binary32."""
+    return np.float32(lib().oracle_rsqrt_rn(float(np.float32(a))))
+
+
+def rmsnorm(x, w, eps: float, bias: float = 0.0):
+    """RMSNorm producer (reading R14): (y as BF16 bit patterns [M, N], amax of y)."""
+    xb = as_bf16_bits(x)
+    wb = as_bf16_bits(w).reshape(-1)
+    M, N = xb.shape
+    assert wb.shape == (N,) and N % 8 == 0
+    y = np.zeros((M, N), dtype=np.uint16)
+    amax = lib().oracle_rmsnorm(_ptr(xb, _u16p), _ptr(np.ascontiguousarray(wb), _u16p), M, N,
+                                float(np.float32(eps)), float(np.float32(bias)), _ptr(y, _u16p))
+    return y, np.float32(amax)
 
 
 def swizzle_scales(scales) -> np.ndarray:

@@ -604,6 +604,88 @@ ORACLE_API void oracle_f32_to_bf16_n(const float* in, int64_t n, uint16_t* out) 
   for (int64_t i = 0; i < n; i++) out[i] = f32_to_bf16_rne(in[i]);
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* A producer with the amax in its epilogue: RMSNorm ([Perplexity] "CuTeDSL at Perplexity",   */
+/* its RMS-norm kernel).                                                                       */
+/*   R14 y_i = bf16_rne(fl(fl(w_i + bias) * fl(x_i * rms))), rms = rsqrt_rn(fl(fl(s / N) +    */
+/*       eps)), s = sum of x_i^2 in binary32 in the page's order: lane l of a 32-lane group    */
+/*       sums, one rounding per term, the squares of its 8-element vectors l, l + 32, l + 64,  */
+/*       ... of the row (elements in order), then the 32 partial sums meet in a butterfly      */
+/*       (xor 16, 8, 4, 2, 1; each step s + partner's s). rsqrt_rn is 1/sqrt correctly rounded */
+/*       to binary32. The epilogue's amax is max |y_i| over the tensor.                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Is m^2 * a (m, a > 0 finite, m with at most 25 and a with at most 24 significant bits)
+ * below (-1), equal to (0) or above (+1) one? Exact, in 128-bit integers. */
+static int square_times_vs_one(double m, double a) {
+  int em, ea;
+  double fm = frexp(m, &em), fa = frexp(a, &ea);
+  unsigned __int128 Mm = (unsigned __int128)ldexp(fm, 25), Ma = (unsigned __int128)ldexp(fa, 24);
+  int k = -(2 * (em - 25) + (ea - 24));  /* m^2 a = Mm^2 Ma 2^-k */
+  unsigned __int128 P = Mm * Mm * Ma;      /* < 2^74 */
+  if (k < 0) return 1;
+  if (k >= 127) return -1;
+  unsigned __int128 one = (unsigned __int128)1 << k;
+  return P < one ? -1 : (P > one ? 1 : 0);
+}
+
+/* 1 / sqrt(a), correctly rounded to binary32 (round to nearest, ties to even), a > 0 finite:
+ * a candidate from double arithmetic, moved until 1/sqrt(a) lies between the midpoints to its
+ * neighbours (exact comparisons m^2 a against 1). */
+static float rsqrt_rn(float a) {
+  float c = (float)(1.0 / sqrt((double)a));
+  for (int it = 0; it < 4; it++) {
+    float up = nextafterf(c, INFINITY), dn = nextafterf(c, 0.0f);
+    double hi = ((double)c + (double)up) / 2, lo = ((double)c + (double)dn) / 2;
+    int h = square_times_vs_one(hi, a), l = square_times_vs_one(lo, a);
+    if (h < 0) { c = up; continue; }          /* 1/sqrt(a) > hi */
+    if (l > 0) { c = dn; continue; }          /* 1/sqrt(a) < lo */
+    if (h == 0 && (bits_of_f32(c) & 1u)) c = up;   /* exactly on a midpoint: the even one */
+    if (l == 0 && (bits_of_f32(c) & 1u)) c = dn;
+    break;
+  }
+  return c;
+}
+
+ORACLE_API float oracle_rsqrt_rn(float a) { return rsqrt_rn(a); }
+
+/* RMSNorm of x [M][N] (BF16, N % 8 == 0) with weight w [N] (BF16) into y [M][N] (BF16 bits);
+ * returns the amax of y. Reading R14. */
+ORACLE_API float oracle_rmsnorm(const uint16_t* x, const uint16_t* w, int64_t M, int64_t N,
+                                float eps, float bias, uint16_t* y) {
+  float amax = 0.0f;
+  for (int64_t r = 0; r < M; r++) {
+    const uint16_t* xr = x + r * N;
+    float part[32];
+    for (int l = 0; l < 32; l++) {
+      float s = 0.0f;
+      for (int64_t v = l; v < N / 8; v += 32)
+        for (int i = 0; i < 8; i++) {
+          float e = bf16_to_f32(xr[8 * v + i]);
+          float sq = e * e;
+          s = s + sq;
+        }
+      part[l] = s;
+    }
+    for (int o = 16; o >= 1; o >>= 1) {
+      float next[32];
+      for (int l = 0; l < 32; l++) next[l] = part[l] + part[l ^ o];
+      for (int l = 0; l < 32; l++) part[l] = next[l];
+    }
+    float mean = part[0] / (float)N;
+    float rms = rsqrt_rn(mean + eps);
+    for (int64_t i = 0; i < N; i++) {
+      float wb = bf16_to_f32(w[i]) + bias;
+      float xr_ = bf16_to_f32(xr[i]) * rms;
+      uint16_t q = f32_to_bf16_rne(wb * xr_);
+      y[r * N + i] = q;
+      float mag = fabsf(bf16_to_f32(q));
+      if (mag > amax) amax = mag;
+    }
+  }
+  return amax;
+}
+
 /* ========================================================================================== */
 /* MX formats: MXFP8 (E4M3 or E5M2 elements) and MXFP4 (E2M1 elements). Blocks of 32         */
 /* consecutive elements share one power-of-two scale stored as E8M0; there is no tensor-wide   */

@@ -601,3 +601,65 @@ def test_inverse_rht_dequantization_keeps_the_transformed_domain_error():
     assert abs(err_x / err_y - 1.0) < 0.02, (err_x, err_y)
     db = 10 * np.log10((xt ** 2).sum() / err_x)
     assert 15.0 < db < 22.0, db
+
+
+# ------------------------------------------------------------------------------------------
+# RMSNorm producer with the amax in its epilogue (reading R14)
+# ------------------------------------------------------------------------------------------
+
+def test_rsqrt_rn_is_correctly_rounded():
+    """Against exact rational arithmetic: the result's two midpoints enclose 1/sqrt(a), i.e.
+    lo^2 a <= 1 <= hi^2 a (Fractions, independent of the oracle's integer comparison)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(51)
+    a = np.concatenate([rng.uniform(0.5, 2.0, 3000), 2.0 ** rng.uniform(-140, 120, 3000),
+                        np.array([1.0, 2.0, 4.0, 0.25, 3.0])]).astype(np.float32)
+    # hard cases: a whose 1/sqrt(a) is close to a binary32 midpoint
+    m = (np.float32(1.25) + np.nextafter(np.float32(1.25), np.float32(2))) / 2
+    a = np.concatenate([a, np.array([1 / float(m) ** 2], dtype=np.float32),
+                        np.nextafter(np.array([1 / float(m) ** 2], dtype=np.float32), 2)])
+    for ai in a:
+        y = oracle.rsqrt_rn(ai)
+        up = np.nextafter(y, np.float32(np.inf))
+        dn = np.nextafter(y, np.float32(0))
+        fa = Fraction(float(ai))
+        hi = (Fraction(float(y)) + Fraction(float(up))) / 2
+        lo = (Fraction(float(y)) + Fraction(float(dn))) / 2
+        assert lo * lo * fa <= 1 <= hi * hi * fa, (ai, y)
+
+
+def _bf16(a):
+    return torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def test_rmsnorm_closed_forms():
+    rng = np.random.default_rng(52)
+    N = 512
+    w = _bf16(rng.normal(0, 1, N))
+    wf = w.float().numpy()
+    for c in (1.0, 2.0 ** -5, 2.0 ** 7):       # constant rows: mean = c^2 exactly, rms = 1/c
+        x = _bf16(np.full((3, N), c))
+        y, amax = oracle.rmsnorm(x, w, eps=0.0)
+        yf = (y.astype(np.uint32) << 16).view(np.float32)
+        assert np.array_equal(yf, np.broadcast_to(wf, yf.shape)), c
+        assert amax == np.abs(wf).max()
+    x = _bf16(np.ones((2, N)))
+    y, _ = oracle.rmsnorm(x, w, eps=0.0, bias=1.0)   # y = bf16(w + 1)
+    want = oracle.f32_to_bf16_array((wf + np.float32(1.0)).astype(np.float32))
+    assert np.array_equal(y[0], want) and np.array_equal(y[1], want)
+
+
+def test_rmsnorm_within_one_bf16_step_of_float64_and_amax():
+    rng = np.random.default_rng(53)
+    M, N = 64, 4096
+    x = workloads.normal_with_outliers(M, N, seed=54, fraction=0.01, gain=20.0)
+    w = _bf16(rng.normal(1.0, 0.2, N))
+    eps, bias = 1e-6, 0.5
+    y, amax = oracle.rmsnorm(x, w, eps=eps, bias=bias)
+    xf = x.double().numpy()
+    wf = w.double().numpy()
+    ref = (wf + np.float32(bias)) * xf / np.sqrt((xf ** 2).mean(axis=1, keepdims=True) + np.float32(eps))
+    yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    assert (np.abs(yf - ref) <= ulp * 1.0001).all()
+    assert amax == np.float32(np.abs(yf).max())
