@@ -627,6 +627,90 @@ def run_mx(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+PRODUCER_METRIC = "RMSNorm + NVFP4 quantize GB/s (BF16 in) with the amax in the norm's epilogue, 1 GPU"
+
+
+def run_producer(args, world, rank, local):
+    """--producer rmsnorm: nvfp4_rmsnorm_quantize (the norm's epilogue gives the amax: norm +
+    quantize, two launches) on the workload, timed beside the same norm followed by
+    nvfp4_quantize computing its own amax in one launch (fused_amax)."""
+    from nvfp4_block_scaled_quantize_gb300 import api, _lib
+    _lib.load()
+    dev = torch.device("cuda", local)
+    w = workloads.WORKLOADS[args.workload]
+    if w.grouped:
+        raise SystemExit("--producer runs on plain workloads")
+    inp = workloads.make_input(w)
+    x = inp["x"].to(dev)
+    kw = quant_kwargs(w, inp)
+    weight = torch.ones(w.cols, dtype=torch.bfloat16, device=dev)
+    out = api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise)
+    y = torch.empty_like(x)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    n = w.rows * w.cols
+    # x read, y written and read back, plus the quantize outputs
+    ideal = 2 * n + 2 * n + ideal_bytes(w)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def fused():
+        api.nvfp4_rmsnorm_quantize(x, weight, eps=1e-6, out=out, y=y, amax=amax, **kw)
+
+    def unfused():
+        api.nvfp4_rmsnorm_amax(x, weight, eps=1e-6, y=y, amax=amax)
+        api.nvfp4_quantize(y, out=out, fused_amax=True, **kw)
+
+    def timed(fn, steps):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [e[0].elapsed_time(e[1]) for e in ev]
+
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        time.sleep(0.3)
+        barrier(world)
+        clocks.mark_start()
+        step_ms = timed(fused, args.steps)
+        clocks.mark_end()
+        base_ms = timed(unfused, args.steps)
+    status, bits = api.nvfp4_get_status(dev)
+    if status != 0:
+        raise RuntimeError("device status %d (bits %#x)" % (status, bits))
+    total_s = max_over_ranks(world, sum(step_ms) / 1e3)
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    value = ideal * args.steps * world / total_s / 1e9
+    line = {
+        "metric": PRODUCER_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": [w.rows, w.cols], "ideal_bytes_per_step": ideal,
+                   "pipeline": "nvfp4_rmsnorm_quantize: norm (amax in its epilogue) + quantize",
+                   "l2": "flushed before every timed step (256 MiB write)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+        "step_us": {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
+                    "max": max(step_ms) * 1e3},
+        "unfused_step_us": {"median": statistics.median(base_ms) * 1e3,
+                            "what": "the same norm, then nvfp4_quantize computing its own amax "
+                                    "(fused_amax, one launch)"},
+        "roofline": {"bound": "hbm", "achieved": value, "peak": hbm, "unit": "GB/s",
+                     "frac": value / hbm, "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "rmsnorm_amax_kernel + quantize_tiles_kernel (the step)"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -640,6 +724,8 @@ def main():
                         "quantize kernel")
     p.add_argument("--mx", choices=["e4m3", "e5m2", "e2m1"], default=None,
                    help="time the MX quantizer (MXFP8 E4M3/E5M2, MXFP4) on the workload's shape")
+    p.add_argument("--producer", choices=["rmsnorm"], default=None,
+                   help="time the RMSNorm producer with the amax in its epilogue + quantize")
     p.add_argument("--fast-math", action="store_true",
                    help="the fast-math variant (approximate reciprocal; FP32 RHT columnwise)")
     args = p.parse_args()
@@ -650,6 +736,8 @@ def main():
         run_reference(args, world, rank)
     elif args.mx:
         run_mx(args, world, rank, local)
+    elif args.producer:
+        run_producer(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

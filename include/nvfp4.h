@@ -228,6 +228,29 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const n
 nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, uint8_t* out,
                                   void* stream);
 
+/* A producer with the amax in its epilogue ([Perplexity] "CuTeDSL at Perplexity", its RMS-norm
+ * kernel): y = bf16_rne((w + weight_bias) * (x * rms)), rms = rsqrt(sum(x^2) / N + eps) per row,
+ * every step one IEEE binary32 operation (the reciprocal square root correctly rounded); the
+ * sum of squares as that kernel takes it (lane l of a warp sums its 8-element vectors l, l + 32,
+ * ... in order, then a butterfly of shuffles, xor 16 .. 1). The epilogue writes amax =
+ * max |y| over the tensor, so that nvfp4_quantize(y, amax_row = amax, ...) needs no amax pass.
+ *   x (device) BF16 [M][N], weight (device) BF16 [N], y (device) BF16 [M][N]: 16-byte aligned,
+ *   N % 8 == 0; amax (device) float[1], zeroed on `stream` before the kernel.
+ * Errors: NVFP4_ERR_INVALID_ARG (NULL buffers, negative sizes, non-finite eps or bias),
+ * NVFP4_ERR_SHAPE, NVFP4_ERR_ALIGN, NVFP4_ERR_CUDA. */
+nvfp4_status nvfp4_rmsnorm_amax(const void* x, const void* weight, int64_t M, int64_t N,
+                                float eps, float weight_bias, void* y, float* amax, void* stream);
+
+/* nvfp4_rmsnorm_amax, then nvfp4_quantize of y with that amax (N % 16 == 0): two launches
+ * instead of norm, amax pass and quantize. With rht_col the columnwise amax (that of the
+ * transformed columns) still comes from an amax pass over y. Outputs and errors as
+ * nvfp4_quantize. */
+nvfp4_status nvfp4_rmsnorm_quantize(const void* x, const void* weight, int64_t M, int64_t N,
+                                    float eps, float weight_bias, const nvfp4_config* cfg,
+                                    void* y, float* amax, uint8_t* row_codes, uint8_t* row_scales,
+                                    float* row_gscale, uint8_t* col_codes, uint8_t* col_scales,
+                                    float* col_gscale, void* stream);
+
 /* MX formats ([Perplexity] "CuTeDSL at Perplexity", its Blackwell paragraph: MXFP8 and MXFP4
  * beside NVFP4, with block maxima over 32 elements). Blocks of 32 consecutive elements share a
  * power-of-two scale stored as E8M0 (value 2^(code - 127)); there is no tensor-wide scale.

@@ -23,7 +23,8 @@ EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quanti
             "nvfp4_dequantize", "nvfp4_get_status", "nvfp4_quantize_noalloc",
             "nvfp4_host_pipeline_create", "nvfp4_host_pipeline_submit",
             "nvfp4_host_pipeline_join", "nvfp4_host_pipeline_destroy", "nvfp4_swizzle_scales",
-            "nvfp4_mx_quantize", "nvfp4_mx_dequantize", "nvfp4_dequantize_ex"]
+            "nvfp4_mx_quantize", "nvfp4_mx_dequantize", "nvfp4_dequantize_ex",
+            "nvfp4_rmsnorm_amax", "nvfp4_rmsnorm_quantize"]
 
 
 class Config(ctypes.Structure):
@@ -100,6 +101,12 @@ def load(build_if_missing: bool = False):
     L.nvfp4_mx_dequantize.argtypes = [vp, vp, i32, i64, i64, vp, vp]
     L.nvfp4_dequantize_ex.restype = ctypes.c_int
     L.nvfp4_dequantize_ex.argtypes = [vp, vp, vp, i64, i64, i32, ctypes.c_uint32, i32, vp, vp]
+    f32 = ctypes.c_float
+    L.nvfp4_rmsnorm_amax.restype = ctypes.c_int
+    L.nvfp4_rmsnorm_amax.argtypes = [vp, vp, i64, i64, f32, f32, vp, vp, vp]
+    L.nvfp4_rmsnorm_quantize.restype = ctypes.c_int
+    L.nvfp4_rmsnorm_quantize.argtypes = [vp, vp, i64, i64, f32, f32, cfgp, vp, vp, vp, vp, vp,
+                                         vp, vp, vp, vp]
     L.nvfp4_get_status.restype = ctypes.c_int
     L.nvfp4_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     _lib = L

@@ -175,6 +175,48 @@ def nvfp4_swizzle_scales(scales):
     return out
 
 
+def nvfp4_rmsnorm_amax(x, weight, eps=1e-6, weight_bias=0.0, y=None, amax=None):
+    """RMSNorm producer with the amax in its epilogue: returns (y BF16 [M, N], amax float32[1])
+    device tensors."""
+    _check_x(x)
+    L = _lib.load()
+    M, N = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    _raise_if(L.nvfp4_rmsnorm_amax(_ptr(x), _ptr(weight.contiguous()), M, N, float(eps),
+                                   float(weight_bias), _ptr(y), _ptr(amax), _stream(x.device)),
+              "nvfp4_rmsnorm_amax")
+    return y, amax
+
+
+def nvfp4_rmsnorm_quantize(x, weight, eps=1e-6, weight_bias=0.0, out=None, y=None, amax=None,
+                           **cfg):
+    """RMSNorm with the amax in its epilogue, then NVFP4 quantization of the normed tensor
+    (options as nvfp4_quantize). Returns the quantize outputs plus "y" and "amax"."""
+    _check_x(x)
+    L = _lib.load()
+    M, N = x.shape
+    c = make_config(cfg.get("rowwise", True), cfg.get("columnwise", False),
+                    cfg.get("block2d", False), cfg.get("round_row", "rn"), cfg.get("round_col", "rn"),
+                    cfg.get("rht_col", False), cfg.get("sign_mask", 0), cfg.get("seed", 0),
+                    cfg.get("offset", 0), cfg.get("fused_amax", False), cfg.get("fast_math", False))
+    if out is None:
+        out = alloc_outputs(M, N, x.device, bool(c.rowwise), bool(c.columnwise))
+    if y is None:
+        y = torch.empty_like(x)
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    p = lambda k: _ptr(out.get(k))
+    _raise_if(L.nvfp4_rmsnorm_quantize(_ptr(x), _ptr(weight.contiguous()), M, N, float(eps),
+                                       float(weight_bias), ctypes.byref(c), _ptr(y), _ptr(amax),
+                                       p("row_codes"), p("row_scales"), p("row_gscale"),
+                                       p("col_codes"), p("col_scales"), p("col_gscale"),
+                                       _stream(x.device)), "nvfp4_rmsnorm_quantize")
+    return dict(out, y=y, amax=amax)
+
+
 MX_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
 
 

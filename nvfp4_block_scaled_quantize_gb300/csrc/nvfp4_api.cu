@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -409,6 +410,47 @@ NVFP4_EXPORT nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t R,
   const int64_t chunks = ((R + 127) / 128) * ((C + 3) / 4) * 32;
   return cuda_status(launch_swizzle_scales(scales, R, C, out, amax_grid(ds, chunks, 256),
                                            static_cast<cudaStream_t>(stream)));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_rmsnorm_amax(const void* x, const void* weight, int64_t M,
+                                             int64_t N, float eps, float weight_bias, void* y,
+                                             float* amax, void* stream) {
+  if (M < 0 || N < 0 || amax == nullptr || !std::isfinite(eps) || !std::isfinite(weight_bias))
+    return NVFP4_ERR_INVALID_ARG;
+  if (N % 8 != 0) return NVFP4_ERR_SHAPE;
+  if (M * N > 0 && (x == nullptr || weight == nullptr || y == nullptr)) return NVFP4_ERR_INVALID_ARG;
+  if ((M * N > 0 && (!aligned(x, 16) || !aligned(weight, 16) || !aligned(y, 16))) ||
+      !aligned(amax, 4))
+    return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(amax, 0, 4, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (M * N == 0) return NVFP4_OK;
+  const int64_t rows = rmsnorm_rows_per_cta();
+  int64_t grid = (M + rows - 1) / rows;
+  if (grid > (int64_t)ds->sm_count * 8) grid = (int64_t)ds->sm_count * 8;
+  return cuda_status(launch_rmsnorm_amax(x, weight, M, N, eps, weight_bias, y, amax, (int)grid, s));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_rmsnorm_quantize(const void* x, const void* weight, int64_t M,
+                                                 int64_t N, float eps, float weight_bias,
+                                                 const nvfp4_config* cfg, void* y, float* amax,
+                                                 uint8_t* row_codes, uint8_t* row_scales,
+                                                 float* row_gscale, uint8_t* col_codes,
+                                                 uint8_t* col_scales, float* col_gscale,
+                                                 void* stream) {
+  nvfp4_status st = check_config(cfg);
+  if (st != NVFP4_OK) return st;
+  if (N % 16 != 0) return NVFP4_ERR_SHAPE;
+  if ((st = nvfp4_rmsnorm_amax(x, weight, M, N, eps, weight_bias, y, amax, stream)) != NVFP4_OK)
+    return st;
+  // the producer's amax serves every orientation except the RHT columnwise one, whose amax is
+  // that of the transformed columns
+  const bool rht = cfg->rht_col != 0 && cfg->columnwise != 0;
+  return nvfp4_quantize(y, M, N, cfg, amax, rht ? nullptr : amax, row_codes, row_scales,
+                        row_gscale, col_codes, col_scales, col_gscale, stream);
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_mx_quantize(const void* x, int64_t M, int64_t N, int32_t format,

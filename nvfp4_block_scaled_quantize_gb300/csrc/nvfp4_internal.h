@@ -132,6 +132,12 @@ cudaError_t prepare_mx_kernels();
 cudaError_t launch_mx_dequantize(int fmt, const uint8_t* codes, const uint8_t* scales, int64_t R,
                                  int64_t C, float* out, int grid, cudaStream_t s);
 
+// RMSNorm producer with the amax in its epilogue (producer.cu): y and an atomic max of |y|
+// into *amax (zeroed by the caller); rmsnorm_rows_per_cta() rows per CTA.
+cudaError_t launch_rmsnorm_amax(const void* x, const void* w, int64_t M, int64_t N, float eps,
+                                float bias, void* y, float* amax, int grid, cudaStream_t s);
+int rmsnorm_rows_per_cta();
+
 cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float* out1, int grid,
                              cudaStream_t s);
 cudaError_t launch_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, uint8_t* out,

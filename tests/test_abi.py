@@ -150,3 +150,18 @@ def test_dequantize_ex_argument_checks_return_before_any_cuda_call(L):
     assert d(4, 32, mask=0x10000) == 1
     assert d(0, 32) == 0                                    # empty
     assert d(4, 32, out=FAKE + 8) == 3                      # output not 16-byte aligned
+
+
+def test_rmsnorm_argument_checks_return_before_any_cuda_call(L):
+    p = ctypes.c_void_p
+    n = lambda M, N, eps=1e-6, bias=0.0, x=FAKE, amax=FAKE: L.nvfp4_rmsnorm_amax(
+        p(x), p(FAKE), M, N, eps, bias, p(FAKE), p(amax), None)
+    assert n(4, 12) == 2                                     # N % 8
+    assert n(-1, 16) == 1
+    assert n(4, 16, eps=float("nan")) == 1 and n(4, 16, bias=float("inf")) == 1
+    assert n(4, 16, amax=0) == 1                             # amax is required
+    assert n(4, 16, x=FAKE + 8) == 3                         # input not 16-byte aligned
+    cfg = _cfg()
+    assert L.nvfp4_rmsnorm_quantize(p(FAKE), p(FAKE), 4, 24, 1e-6, 0.0, ctypes.byref(cfg),
+                                    p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None, None,
+                                    None, None) == 2         # N % 16
