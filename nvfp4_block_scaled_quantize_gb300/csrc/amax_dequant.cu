@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 
 #include "nvfp4_device.cuh"
+#include "aux_internal.h"
 #include "nvfp4_internal.h"
 
 namespace nvfp4 {

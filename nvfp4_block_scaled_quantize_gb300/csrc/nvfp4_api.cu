@@ -10,6 +10,7 @@
 
 #include "nvfp4.h"
 #include "nvfp4_device.cuh"
+#include "aux_internal.h"
 #include "nvfp4_internal.h"
 
 #define NVFP4_EXPORT extern "C" __attribute__((visibility("default")))

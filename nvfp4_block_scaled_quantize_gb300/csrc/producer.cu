@@ -15,6 +15,7 @@
 #include <cstdint>
 
 #include "nvfp4_device.cuh"
+#include "aux_internal.h"
 #include "nvfp4_internal.h"
 
 namespace nvfp4 {
