@@ -197,6 +197,12 @@ def max_over_ranks(world, value):
     return float(t.item())
 
 
+def aggregate_gbs(ideal_bytes_per_step, steps, world, total_s):
+    """Whole-job throughput: every rank's bytes (replicas: the same work per rank) over the
+    slowest rank's timed region."""
+    return ideal_bytes_per_step * steps * world / total_s / 1e9
+
+
 def quant_kwargs(w, inp):
     return dict(rowwise=w.rowwise, columnwise=w.columnwise, block2d=w.block2d,
                 rht_col=w.rht_col, sign_mask=inp["sign_mask"], seed=inp["seed"],
@@ -397,7 +403,7 @@ def run_ours(args, world, rank, local):
                     else [e[1].elapsed_time(e[2]) for e in events])
     total_s = sum(step_ms) / 1e3
     total_s = max_over_ranks(world, total_s)
-    value = ideal * args.steps * world / total_s / 1e9
+    value = aggregate_gbs(ideal, args.steps, world, total_s)
 
     # end to end through the public API: pinned host input -> device -> quantize -> pinned host.
     # Plain tensors go through the host pipeline (the copy in of one step overlaps the copy out
@@ -572,7 +578,7 @@ def run_mx(args, world, rank, local):
     barrier(world)
     step_ms = [e[0].elapsed_time(e[1]) for e in events]
     total_s = max_over_ranks(world, sum(step_ms) / 1e3)
-    value = ideal * args.steps * world / total_s / 1e9
+    value = aggregate_gbs(ideal, args.steps, world, total_s)
 
     # end to end: pinned host input -> device -> quantize -> pinned host outputs, one stream
     x_host = inp["x"].pin_memory()
@@ -688,7 +694,7 @@ def run_producer(args, world, rank, local):
     if rank != 0:
         return
     hbm, peak_kind = peaks()
-    value = ideal * args.steps * world / total_s / 1e9
+    value = aggregate_gbs(ideal, args.steps, world, total_s)
     line = {
         "metric": PRODUCER_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
