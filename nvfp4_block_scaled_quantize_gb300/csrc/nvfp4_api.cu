@@ -280,7 +280,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   q.amax_row_stride = 2; q.amax_col_stride = 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
-  q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
+  q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
   q.x = x;
   q.fused = fused ? 1 : 0;
   q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
@@ -353,7 +353,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   q.amax_row_stride = 2; q.amax_col_stride = 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
-  q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
+  q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
   q.fast = cfg->fast_math ? 1 : 0;
   const QuantMode mode{row, col, rht, false, sr_row != 0, sr_col != 0, q.fast && rht};
   const int64_t tiles = ((T + kTileM - 1) / kTileM + E) * ((H + kTileN - 1) / kTileN);

@@ -297,24 +297,21 @@ __device__ __forceinline__ uint32_t e2m1x4(float t0, float t1, float t2, float t
 // SC'11). One draw per 16-element block, all four words used ([PR4798] "Optimization" item 3;
 // the counter is the block's position, so results do not depend on the visit order).
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// The round keys are precomputed on the host (k[0][r], k[1][r] for round r: the seed's halves
+// bumped by the Weyl constants), so that the XORs take them straight from the kernel parameters.
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&k)[2][10]) {
 #pragma unroll
   for (int round = 0; round < 10; round++) {
     uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
     uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1,
-                   (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k[0][round], (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ k[1][round], (uint32_t)p0);
   }
   return c;
 }
-
-// The four words of block b: key (lo32 seed, hi32 seed), counter (lo32 b, hi32 b, tag, offset).
-__device__ __forceinline__ uint4 block_random(uint64_t seed, uint32_t offset, uint32_t tag,
-                                              uint64_t b) {
-  return philox4x32_10(make_uint4((uint32_t)b, (uint32_t)(b >> 32), tag, offset),
-                       (uint32_t)seed, (uint32_t)(seed >> 32));
+__device__ __forceinline__ uint4 block_random_rk(const uint32_t (&k)[2][10], uint32_t offset,
+                                                 uint32_t tag, uint64_t b) {
+  return philox4x32_10_rk(make_uint4((uint32_t)b, (uint32_t)(b >> 32), tag, offset), k);
 }
 
 // ------------------------------------------------------------------------------------------

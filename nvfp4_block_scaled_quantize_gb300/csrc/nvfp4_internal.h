@@ -68,6 +68,7 @@ struct QuantArgs {
   uint8_t* col_scales;
   float* col_gscale;
   uint64_t seed;
+  uint32_t philox_key[2][10];       // Philox round keys of seed (set_philox_keys)
   uint32_t rng_offset;
   uint32_t* status;
   int32_t fused;                    // 1: compute the amax inside this launch (one segment)
@@ -76,6 +77,19 @@ struct QuantArgs {
   uint64_t fuse_epoch;              // larger than any earlier launch's on fuse_ws (< 2^48)
   uint32_t* fuse_ws;                // kFuseWsWords words, 8-byte aligned
 };
+
+// Round keys of Philox4x32-10 for a 64-bit seed: key (lo32, hi32) bumped by the Weyl constants
+// 0x9E3779B9 and 0xBB67AE85 each round. Computed once per launch on the host, so that the
+// kernels read them from their parameters instead of recomputing the schedule per draw.
+inline void set_philox_keys(QuantArgs& a, uint64_t seed) {
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; r++) {
+    a.philox_key[0][r] = k0;
+    a.philox_key[1][r] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
 
 // What one quantize launch produces.
 struct QuantMode {

@@ -576,8 +576,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           for (int q = 0; q < 4; q++) {
             const uint64_t b0 = (uint64_t)(row_g0 + 4 * q + (odd ? 2 : 0)) * (uint64_t)row_nb +
                                 (uint64_t)(c.n0 / 16 + kb);
-            const uint4 D0 = block_random(a.seed, a.rng_offset, 0u, b0);
-            const uint4 D1 = block_random(a.seed, a.rng_offset, 0u, b0 + (uint64_t)row_nb);
+            const uint4 D0 = block_random_rk(a.philox_key, a.rng_offset, 0u, b0);
+            const uint4 D1 = block_random_rk(a.philox_key, a.rng_offset, 0u, b0 + (uint64_t)row_nb);
             const uint32_t x0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? D0.x : D0.z, 1);
             const uint32_t x1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? D0.y : D0.w, 1);
             const uint32_t x2 = __shfl_xor_sync(0xFFFFFFFFu, odd ? D1.x : D1.z, 1);
@@ -675,8 +675,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           if (SR_COL) {
             const uint64_t b0 = (uint64_t)(c.n0 + lane * 8 + 2 * k) * (uint64_t)col_nb +
                                 (uint64_t)(c.colpos / 16 + rb);
-            W0 = block_random(a.seed, a.rng_offset, 1u, b0);
-            W1 = block_random(a.seed, a.rng_offset, 1u, b0 + (uint64_t)col_nb);
+            W0 = block_random_rk(a.philox_key, a.rng_offset, 1u, b0);
+            W1 = block_random_rk(a.philox_key, a.rng_offset, 1u, b0 + (uint64_t)col_nb);
           }
           uint32_t code[2][2];  // [column of the pair][rows 0..7, 8..15]
 #pragma unroll

@@ -139,7 +139,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   q.amax_row_stride = 2; q.amax_col_stride = 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
-  q.seed = cfg->rng_seed; q.rng_offset = cfg->rng_offset;
+  q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset;
   q.status = d->scratch + kScratchStatus;
   q.fused = 1;
   q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
