@@ -22,6 +22,7 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kNormWarps = 8;
+constexpr int kBatch = 4;  // vectors per lane loaded together
 
 __global__ void __launch_bounds__(32 * kNormWarps) rmsnorm_amax_kernel(
     const uint4* __restrict__ x, const uint4* __restrict__ w, int64_t M, int64_t N, float eps,
@@ -35,32 +36,50 @@ __global__ void __launch_bounds__(32 * kNormWarps) rmsnorm_amax_kernel(
        r += (int64_t)gridDim.x * kNormWarps) {
     const uint4* xr = x + r * nv;
     float s = 0.0f;
-    for (int64_t v = lane; v < nv; v += 32) {
-      const uint4 q = xr[v];
-      const uint32_t e[4] = {q.x, q.y, q.z, q.w};
+    // kBatch of the lane's vectors loaded at once (more loads in flight), then summed in order
+    for (int64_t v0 = lane; v0 < nv; v0 += 32 * kBatch) {
+      uint4 q[kBatch];
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const float lo = bf16_lo(e[i]), hi = bf16_hi(e[i]);
-        s = __fadd_rn(s, __fmul_rn(lo, lo));
-        s = __fadd_rn(s, __fmul_rn(hi, hi));
+      for (int j = 0; j < kBatch; j++)
+        q[j] = v0 + 32 * j < nv ? xr[v0 + 32 * j] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < kBatch; j++) {
+        const uint32_t e[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const float lo = bf16_lo(e[i]), hi = bf16_hi(e[i]);
+          s = __fadd_rn(s, __fmul_rn(lo, lo));  // (vectors past the row add +0: s unchanged)
+          s = __fadd_rn(s, __fmul_rn(hi, hi));
+        }
       }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
     const float rms = __frsqrt_rn(__fadd_rn(__fdiv_rn(s, (float)N), eps));
-    for (int64_t v = lane; v < nv; v += 32) {
-      const uint4 q = xr[v], qw = w[v];
-      const uint32_t e[4] = {q.x, q.y, q.z, q.w}, g[4] = {qw.x, qw.y, qw.z, qw.w};
-      uint32_t o[4];
+    for (int64_t v0 = lane; v0 < nv; v0 += 32 * kBatch) {
+      uint4 q[kBatch], qw[kBatch];
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const float y0 = __fmul_rn(__fadd_rn(bf16_lo(g[i]), bias), __fmul_rn(bf16_lo(e[i]), rms));
-        const float y1 = __fmul_rn(__fadd_rn(bf16_hi(g[i]), bias), __fmul_rn(bf16_hi(e[i]), rms));
-        const __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);
-        o[i] = *reinterpret_cast<const uint32_t*>(&p);
-        m = max(m, max(o[i] & 0x7FFFu, (o[i] >> 16) & 0x7FFFu));
+      for (int j = 0; j < kBatch; j++) {
+        const bool in = v0 + 32 * j < nv;
+        q[j] = in ? xr[v0 + 32 * j] : make_uint4(0u, 0u, 0u, 0u);
+        qw[j] = in ? w[v0 + 32 * j] : make_uint4(0u, 0u, 0u, 0u);
       }
-      y[r * nv + v] = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+      for (int j = 0; j < kBatch; j++) {
+        if (v0 + 32 * j >= nv) break;
+        const uint32_t e[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+        const uint32_t g[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const float y0 = __fmul_rn(__fadd_rn(bf16_lo(g[i]), bias), __fmul_rn(bf16_lo(e[i]), rms));
+          const float y1 = __fmul_rn(__fadd_rn(bf16_hi(g[i]), bias), __fmul_rn(bf16_hi(e[i]), rms));
+          const __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);
+          o[i] = *reinterpret_cast<const uint32_t*>(&p);
+          m = max(m, max(o[i] & 0x7FFFu, (o[i] >> 16) & 0x7FFFu));
+        }
+        y[r * nv + v0 + 32 * j] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
   }
   // epilogue: the CTA's largest magnitude, one atomic max on the float's bits (non-negative
