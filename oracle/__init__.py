@@ -75,6 +75,9 @@ def lib():
                                                        ctypes.c_uint64, ctypes.c_uint32,
                                                        _u8p, _u8p, _f32p, _u8p, _u8p, _f32p]),
             "oracle_dequantize": (None, [_u8p, _u8p, ctypes.c_float, _i64, _i64, _f32p]),
+            "oracle_quantize_grouped_2d": (ctypes.c_int, [_u16p, _i64, _i64, _i32p,
+                                                          ctypes.c_int32, _i64, _u8p, _u8p,
+                                                          _f32p, _u8p, _u8p, _f32p]),
             "oracle_inverse_rht16": (None, [_f32p, ctypes.c_uint32, _f32p]),
             "oracle_inverse_rht_rows": (None, [_f32p, _i64, _i64, ctypes.c_uint32]),
             "oracle_f32_to_bf16_n": (None, [_f32p, _i64, _u16p]),
@@ -277,7 +280,7 @@ def padded_capacity(offsets) -> int:
 
 def quantize_grouped(x, offsets, cap=None, rowwise=True, columnwise=True, round_row_sr=False,
                      round_col_sr=False, rht_col=False, sign_mask=0, seed=0, offset=0,
-                     fill=0):
+                     fill=0, block2d=False):
     """Grouped quantization. Output buffers start filled with ``fill`` so that untouched
     regions (the tail past the last offset, columns past the padded total) stay visible."""
     xb = as_bf16_bits(x)
@@ -293,6 +296,14 @@ def quantize_grouped(x, offsets, cap=None, rowwise=True, columnwise=True, round_
     cs = np.full((H, cap // 16), fill, dtype=np.uint8) if columnwise else None
     cg = np.zeros((E, 2), dtype=np.float32) if columnwise else None
     rc_ = rc if rowwise else None
+    if block2d:
+        assert not (round_row_sr or round_col_sr or rht_col), "2D has no SR or RHT"
+        status = lib().oracle_quantize_grouped_2d(
+            _ptr(xb, _u16p), T, H, _ptr(off, _i32p), E, cap, _ptr(rc_, _u8p), _ptr(rs, _u8p),
+            _ptr(rg, _f32p), _ptr(cc, _u8p), _ptr(cs, _u8p), _ptr(cg, _f32p))
+        if status != 0:
+            raise ValueError("invalid offsets or capacity for grouped quantization")
+        return rc, rs, rg, cc, cs, cg
     status = lib().oracle_quantize_grouped(
         _ptr(xb, _u16p), T, H, _ptr(off, _i32p), E, cap, int(bool(round_row_sr)),
         int(bool(round_col_sr)), int(bool(rht_col)), sign_mask, seed, offset,

@@ -54,6 +54,7 @@
 #include <float.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_API __attribute__((visibility("default")))
@@ -547,6 +548,65 @@ ORACLE_API int oracle_quantize_grouped(const uint16_t* x, int64_t T, int64_t H,
                      round_col_sr, seed, offset, col_codes, col_scales);
     }
     col_start += 16 * nblk;
+  }
+  return 0;
+}
+
+/* Grouped 2D (weights of several experts stacked along the rows). Reading R15: expert e's 16x16
+ * tiles start at its first row and its last row tile is zero-padded (as R11 pads columnwise
+ * blocks); each expert has its own amax and global scales; the tile scale is written for every
+ * row of the expert in the rowwise outputs (padding rows belong to no output) and into the
+ * expert's padded columns of the columnwise outputs (starting at sum_{j<e} pad16(n_j)). Any
+ * orientation may be absent (NULL). Returns -1 for offsets that are not non-decreasing within
+ * [0, T] or a capacity below the padded total. */
+ORACLE_API int oracle_quantize_grouped_2d(const uint16_t* x, int64_t T, int64_t H,
+                                          const int32_t* offsets, int32_t E, int64_t cap,
+                                          uint8_t* row_codes, uint8_t* row_scales,
+                                          float* row_gscale, uint8_t* col_codes,
+                                          uint8_t* col_scales, float* col_gscale) {
+  int64_t padded_total = 0, prev = 0;
+  for (int32_t e = 0; e < E; e++) {
+    if (offsets[e] < prev || offsets[e] > T) return -1;
+    padded_total += ((offsets[e] - prev) + 15) / 16 * 16;
+    prev = offsets[e];
+  }
+  if (col_codes && padded_total > cap) return -1;
+  int64_t col_start = 0;
+  for (int32_t e = 0; e < E; e++) {
+    int64_t start = (e == 0) ? 0 : offsets[e - 1];
+    int64_t n = offsets[e] - start;
+    int64_t P = (n + 15) / 16 * 16;
+    float amax = oracle_amax(x + start * H, n, H);
+    float gs[2];
+    if (P > 0) {
+      /* the expert's rows, zero-padded to whole tiles, through the plain 2D quantizer */
+      uint16_t* xs = (uint16_t*)calloc((size_t)(P * H), sizeof(uint16_t));
+      uint8_t* rc = (uint8_t*)malloc((size_t)(P * H / 2));
+      uint8_t* rs = (uint8_t*)malloc((size_t)(P * H / 16));
+      uint8_t* cc = (uint8_t*)malloc((size_t)(P * H / 2));
+      uint8_t* cs = (uint8_t*)malloc((size_t)(P * H / 16));
+      if (!xs || !rc || !rs || !cc || !cs) { free(xs); free(rc); free(rs); free(cc); free(cs); return -2; }
+      memcpy(xs, x + start * H, (size_t)(n * H) * sizeof(uint16_t));
+      oracle_quantize_2d(xs, P, H, amax, rc, rs, cc, cs, gs);
+      if (row_codes) {
+        memcpy(row_codes + start * (H / 2), rc, (size_t)(n * H / 2));
+        memcpy(row_scales + start * (H / 16), rs, (size_t)(n * H / 16));
+      }
+      if (col_codes) {
+        for (int64_t h = 0; h < H; h++) {
+          memcpy(col_codes + h * (cap / 2) + col_start / 2, cc + h * (P / 2), (size_t)(P / 2));
+          memcpy(col_scales + h * (cap / 16) + col_start / 16, cs + h * (P / 16), (size_t)(P / 16));
+        }
+      }
+      free(xs); free(rc); free(rs); free(cc); free(cs);
+    } else {
+      float s_enc;
+      global_scale(amax, &s_enc, &gs[1]);
+      gs[0] = amax;
+    }
+    if (row_gscale) { row_gscale[2 * e] = gs[0]; row_gscale[2 * e + 1] = gs[1]; }
+    if (col_gscale) { col_gscale[2 * e] = gs[0]; col_gscale[2 * e + 1] = gs[1]; }
+    col_start += P;
   }
   return 0;
 }

@@ -663,3 +663,45 @@ def test_rmsnorm_within_one_bf16_step_of_float64_and_amax():
     ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
     assert (np.abs(yf - ref) <= ulp * 1.0001).all()
     assert amax == np.float32(np.abs(yf).max())
+
+
+# ------------------------------------------------------------------------------------------
+# Grouped 2D weights (reading R15)
+# ------------------------------------------------------------------------------------------
+
+def test_grouped_2d_tile_scales_transposes_padding_and_special_cases():
+    T, H = 150, 64
+    x = oracle.as_bf16_bits(workloads.normal_with_outliers(T, H, seed=61, fraction=0.02, gain=20.0))
+    offsets = np.array([32, 32, 57, 100, 140], dtype=np.int32)  # whole, empty, ragged; tail 140..
+    cap = oracle.padded_capacity(offsets) + 16
+    rc, rs, rg, cc, cs, cg = oracle.quantize_grouped(x, offsets, cap=cap, block2d=True, fill=0xEE)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    assert np.all(rc[140:] == 0xEE) and np.all(rs[140:] == 0xEE)
+    prev, col = 0, 0
+    for e, end in enumerate(offsets.tolist()):
+        n = end - prev
+        if n == 0:
+            assert list(rg[e]) == [0.0, 1.0] and list(cg[e]) == [0.0, 1.0]
+            continue
+        P = (n + 15) // 16 * 16
+        amax = np.abs(xf[prev:end]).max()
+        s_enc, s_dec = oracle.global_scale(amax)
+        assert rg[e][0] == amax and rg[e][1] == s_dec and list(cg[e]) == list(rg[e])
+        for t in range(P // 16):
+            rows = slice(prev + 16 * t, min(prev + 16 * t + 16, end))
+            for tc in range(H // 16):
+                tile_max = np.abs(xf[rows, 16 * tc:16 * tc + 16]).max()
+                s = oracle.block_scale(tile_max, s_enc)
+                assert np.all(rs[rows, tc] == s)                      # every real row of the tile
+                assert np.all(cs[16 * tc:16 * tc + 16, (col + 16 * t) // 16] == s)
+        # column codes are the transposed row codes; the padding rows encode zeros
+        rn = np.stack([rc[prev:end] & 0xF, rc[prev:end] >> 4], axis=-1).reshape(n, H)
+        cn = np.stack([cc[:, col // 2:(col + P) // 2] & 0xF, cc[:, col // 2:(col + P) // 2] >> 4],
+                      axis=-1).reshape(H, P)
+        assert np.array_equal(cn[:, :n], rn.T) and not cn[:, n:].any()
+        if n % 16 == 0:   # a whole-tile expert is a plain 2D call on its slice
+            pc, ps, pcc, pcs, pg = oracle.quantize_2d(x[prev:end])
+            assert np.array_equal(pc, rc[prev:end]) and np.array_equal(ps, rs[prev:end])
+            assert np.array_equal(pcc, cc[:, col // 2:(col + P) // 2])
+        prev, col = end, col + P
+    assert np.all(cc[:, col // 2:] == 0xEE) and np.all(cs[:, col // 16:] == 0xEE)
