@@ -219,7 +219,8 @@ def _oracle_run(w, inp, rows):
         off = np.minimum(inp["offsets"], rows).astype(np.int32)
         oracle.quantize_grouped(xb, off, rowwise=w.rowwise, columnwise=w.columnwise,
                                 round_row_sr=w.round_row_sr, round_col_sr=w.round_col_sr,
-                                rht_col=w.rht_col, sign_mask=inp["sign_mask"], seed=inp["seed"])
+                                rht_col=w.rht_col, sign_mask=inp["sign_mask"], seed=inp["seed"],
+                                block2d=w.block2d)
     else:
         oracle.quantize(xb, oracle.Config(rowwise=w.rowwise, columnwise=w.columnwise,
                                           block2d=w.block2d, round_row_sr=w.round_row_sr,
@@ -347,7 +348,7 @@ def run_ours(args, world, rank, local):
             if ev:
                 ev[0].record(stream)
             api.nvfp4_quantize_grouped(x, offsets, col_capacity=cap, out=out,
-                                       **{k: v for k, v in kw.items() if k != "block2d"})
+                                       **kw)
             if ev:
                 ev[2].record(stream)
         launches_per_step = 2
@@ -417,7 +418,7 @@ def run_ours(args, world, rank, local):
         def e2e_step():
             xd = x_host.to(dev, non_blocking=True)
             o = api.nvfp4_quantize_grouped(xd, offsets, col_capacity=cap,
-                                           **{k: v for k, v in kw.items() if k != "block2d"})
+                                           **kw)
             for k, v in o.items():
                 host_out[k].copy_(v, non_blocking=True)
 

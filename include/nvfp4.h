@@ -157,8 +157,11 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N, const nvfp4_con
  *   over its zero-padded blocks for the columnwise side. Outputs:
  *   row_codes [T][H/2], row_scales [T][H/16], row_gscale [E][2];
  *   col_codes [H][col_capacity/2], col_scales [H][col_capacity/16], col_gscale [E][2].
- * H % 16 == 0. block2d and fused_amax are not supported here. Offsets that break the rules
- * above set NVFP4_DEVICE_BAD_OFFSETS and the kernels write no codes. */
+ * block2d (stacked expert weights, the pages' grouped 2D weight quantize): each expert's 16x16
+ *   tiles start at its first row, its last row tile zero-padded; one amax and global scale per
+ *   expert for both orientations; no RHT or SR (NVFP4_ERR_UNSUPPORTED).
+ * H % 16 == 0. fused_amax is not supported here. Offsets that break the rules above set
+ * NVFP4_DEVICE_BAD_OFFSETS and the kernels write no codes. */
 nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
                                     const int32_t* offsets, int32_t E, int64_t col_capacity,
                                     const nvfp4_config* cfg,

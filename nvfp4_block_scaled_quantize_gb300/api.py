@@ -114,9 +114,10 @@ def padded_capacity(counts) -> int:
 
 def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwise=True,
                            round_row="rn", round_col="rn", rht_col=False, sign_mask=0, seed=0,
-                           offset=0, out=None, fast_math=False):
+                           offset=0, out=None, fast_math=False, block2d=False):
     """Grouped quantization of a packed BF16 [T, H] tensor; `offsets` is an int32 [E] device
-    tensor of cumulative expert ends. col_capacity defaults to T + 16 * E (always enough)."""
+    tensor of cumulative expert ends. col_capacity defaults to T + 16 * E (always enough).
+    block2d: 16x16 tiles per expert (stacked expert weights), no RHT or SR."""
     _check_x(x)
     L = _lib.load()
     if offsets.dtype != torch.int32 or not offsets.is_cuda or offsets.dim() != 1:
@@ -125,7 +126,7 @@ def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwi
     E = offsets.shape[0]
     if col_capacity is None:
         col_capacity = (T + 15) // 16 * 16 + 16 * E
-    cfg = make_config(rowwise, columnwise, False, round_row, round_col, rht_col, sign_mask, seed,
+    cfg = make_config(rowwise, columnwise, block2d, round_row, round_col, rht_col, sign_mask, seed,
                       offset, fast_math=fast_math)
     if out is None:
         out = alloc_outputs(T, H, x.device, rowwise, columnwise, col_ld=col_capacity, groups=E)

@@ -313,7 +313,10 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   const bool col = cfg->columnwise != 0;
   const bool rht = cfg->rht_col != 0 && col;
   if (!row && !col) return NVFP4_ERR_UNSUPPORTED;
-  if (cfg->block2d || cfg->fused_amax) return NVFP4_ERR_UNSUPPORTED;
+  const bool two_d = cfg->block2d != 0;
+  if (cfg->fused_amax) return NVFP4_ERR_UNSUPPORTED;
+  if (two_d && (cfg->rht_col || cfg->round_row == NVFP4_ROUND_SR || cfg->round_col == NVFP4_ROUND_SR))
+    return NVFP4_ERR_UNSUPPORTED;
   if (T < 0 || H < 0 || E < 1 || E > kMaxSegments || offsets == nullptr) return NVFP4_ERR_INVALID_ARG;
   if (H % 16 != 0 || (col && (col_capacity < 0 || col_capacity % 16 != 0))) return NVFP4_ERR_SHAPE;
   if (T > INT32_MAX - kTileM || H > INT32_MAX - kTileN || col_capacity > INT32_MAX)
@@ -349,13 +352,14 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   q.rows = T; q.cols = H; q.offsets = offsets; q.segments = E;
   const int sr_row = cfg->round_row == NVFP4_ROUND_SR, sr_col = cfg->round_col == NVFP4_ROUND_SR;
   q.sign_mask = cfg->rht_sign_mask; q.col_ld = col ? col_capacity : 0;
-  q.amax_row = row_gscale; q.amax_col = col_gscale;
+  // 2D reads the one per-expert amax from amax_row (kept in col_gscale when only columnwise)
+  q.amax_row = row ? row_gscale : (two_d ? col_gscale : nullptr); q.amax_col = col_gscale;
   q.amax_row_stride = 2; q.amax_col_stride = 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
   q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
-  q.fast = cfg->fast_math ? 1 : 0;
-  const QuantMode mode{row, col, rht, false, sr_row != 0, sr_col != 0, q.fast && rht};
+  q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
+  const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};
   const int64_t tiles = ((T + kTileM - 1) / kTileM + E) * ((H + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
   return cuda_status(launch_quantize(mode, q, grid, s));

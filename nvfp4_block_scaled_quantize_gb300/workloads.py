@@ -52,6 +52,10 @@ WORKLOADS = {
                  columnwise=True, rht_col=True, round_col_sr=True),
         Workload("moe_64experts_32768x7168_row_rtne_col_rht_sr", 32768, 7168, "normal", 1.0, 5,
                  columnwise=True, rht_col=True, round_col_sr=True, experts=64, zero_experts=4),
+        # four local experts' gate/up weights stacked along the rows (the pages' grouped 2D
+        # weight quantize, DeepSeek-V3 hidden 7168), equal row counts
+        Workload("moe_weights_4experts_16384x7168_2d_rtne", 16384, 7168, "normal", 0.02, 6,
+                 columnwise=True, block2d=True, experts=4, extra={"equal_experts": True}),
     ]
 }
 
@@ -119,7 +123,9 @@ def make_input(w: Workload, rows: int = None) -> dict:
         raise ValueError(w.dist)
     out = {"x": x, "seed": w.seed, "offset": 0,
            "sign_mask": sign_mask(w.seed) if w.rht_col else 0}
-    if w.grouped:
+    if w.grouped and w.extra.get("equal_experts"):
+        out["offsets"] = (np.arange(1, w.experts + 1) * (rows // w.experts)).astype(np.int32)
+    elif w.grouped:
         out["offsets"] = expert_offsets(rows, w.experts, w.zero_experts, w.seed)
     return out
 

@@ -89,7 +89,10 @@ def test_grouped_and_dequant_argument_checks(L):
     assert grouped(64, 24, p(FAKE), 2, 64) == 2     # H % 16
     assert grouped(64, 32, p(FAKE), 2, 40) == 2     # capacity % 16
     assert grouped(64, 32, p(FAKE + 2), 2, 64) == 3
-    assert grouped(64, 32, p(FAKE), 2, 64, _cfg(columnwise=1, block2d=1)) == 4
+    # grouped 2D has no RHT or SR, and no grouped call takes the single-launch amax
+    assert grouped(64, 32, p(FAKE), 2, 64, _cfg(columnwise=1, block2d=1, rht_col=1)) == 4
+    assert grouped(64, 32, p(FAKE), 2, 64, _cfg(columnwise=1, block2d=1, round_col=1)) == 4
+    assert grouped(64, 32, p(FAKE), 2, 64, _cfg(columnwise=1, fused_amax=1)) == 4
     assert L.nvfp4_dequantize(p(FAKE), p(FAKE), p(FAKE), 4, 24, p(FAKE), None) == 2
     assert L.nvfp4_dequantize(p(FAKE), p(FAKE), p(FAKE), 4, 32, p(FAKE + 4), None) == 3
     assert L.nvfp4_amax(p(FAKE), 16, 32, ctypes.byref(cfg), None, None, None) == 1

@@ -248,7 +248,8 @@ def run_grouped_both(x_cpu, offsets_np, cap=None, **cfg):
         x_cpu, offsets_np, cap=cap, rowwise=rowwise, columnwise=columnwise,
         round_row_sr=cfg.get("round_row") == "sr", round_col_sr=cfg.get("round_col") == "sr",
         rht_col=cfg.get("rht_col", False), sign_mask=cfg.get("sign_mask", 0),
-        seed=cfg.get("seed", 0), offset=cfg.get("offset", 0), fill=0xEE)
+        seed=cfg.get("seed", 0), offset=cfg.get("offset", 0), fill=0xEE,
+        block2d=cfg.get("block2d", False))
     ref = {}
     if rowwise:
         ref.update(row_codes=rc, row_scales=rs, row_gscale=rg)
@@ -266,6 +267,28 @@ GROUPED_CASES = [
     # followed by experts long enough for whole, aligned 64-row tiles
     ("lead_slabs", 700, 512, list(np.cumsum([16, 200, 32, 150, 48, 200, 1, 53]))),
 ]
+
+
+@pytest.mark.parametrize("case", GROUPED_CASES, ids=lambda c: c[0])
+@pytest.mark.parametrize("mode", ["2d_rowcol", "2d_row", "2d_col"])
+def test_grouped_2d_matches_oracle(case, mode):
+    """Stacked expert weights with 16x16 tiles per expert (ragged experts zero-padded)."""
+    name, T, H, offs = case
+    cfg = {"2d_rowcol": dict(rowwise=True, columnwise=True),
+           "2d_row": dict(rowwise=True, columnwise=False),
+           "2d_col": dict(rowwise=False, columnwise=True)}[mode]
+    x = workloads.normal_with_outliers(T, H, seed=T * 5 + H, fraction=0.01, gain=30.0)
+    out, ref = run_grouped_both(x, offs, block2d=True, **cfg)
+    assert_same(out, ref, "%s/%s" % (name, mode))
+
+
+def test_grouped_2d_weights_of_the_pages_shape():
+    """E = 4 experts' stacked weights (DeepSeek-V3 gate/up-like rows of 7168), 16x16 tiles."""
+    E, rows, H = 4, 512, 7168
+    offs = list(np.cumsum([rows] * E))
+    x = workloads.normal(E * rows, H, 0.02, seed=71)
+    out, ref = run_grouped_both(x, offs, block2d=True, rowwise=True, columnwise=True)
+    assert_same(out, ref, "grouped 2D weights")
 
 
 @pytest.mark.parametrize("case", GROUPED_CASES, ids=lambda c: c[0])
@@ -323,7 +346,8 @@ def test_full_size_workload_matches_oracle(name):
     if w.grouped:
         cfg = dict(rowwise=w.rowwise, columnwise=w.columnwise, rht_col=w.rht_col,
                    sign_mask=inp["sign_mask"], round_col="sr" if w.round_col_sr else "rn",
-                   round_row="sr" if w.round_row_sr else "rn", seed=inp["seed"])
+                   round_row="sr" if w.round_row_sr else "rn", seed=inp["seed"],
+                   block2d=w.block2d)
         out, ref = run_grouped_both(x, inp["offsets"], **cfg)
     else:
         cfg = dict(rowwise=w.rowwise, columnwise=w.columnwise, block2d=w.block2d,
