@@ -50,6 +50,10 @@
  *      [N][M/16] scale tensors.
  *   R11 grouped: expert e owns rows [off[e-1], off[e]) (off[-1] = 0); its columnwise output
  *      starts at column sum_{j<e} pad16(n_j) and covers pad16(n_e) zero-padded tokens.
+ *   R12 fast math has no CPU statement (a hardware reciprocal); it is bounded against the exact
+ *      path by the GPU tests, not computed here.
+ *   R13 inverse RHT (checks at the GEMM boundary), R14 the RMSNorm producer, R15 grouped 2D
+ *      and M1-M4 (MX formats) are stated beside their code below.
  */
 #include <float.h>
 #include <math.h>
