@@ -38,6 +38,7 @@
 #ifndef NVFP4_H
 #define NVFP4_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -286,6 +287,22 @@ nvfp4_status nvfp4_mx_quantize(const void* x, int64_t M, int64_t N, int32_t form
  * 16-byte aligned. */
 nvfp4_status nvfp4_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int32_t format,
                                  int64_t R, int64_t C, float* out, void* stream);
+
+/* The per-device workspace: the status word the kernels report to, and the arrival count and
+ * epoch-tagged maxima of the single-launch amax. By default the library allocates it with
+ * cudaMalloc (once per device, on the first call that needs it, zeroed) and never frees it. */
+#define NVFP4_WORKSPACE_BYTES 16384
+
+/* Use caller-owned device memory as the current device's workspace instead, e.g. memory from
+ * the caller's own allocator, set up before stream capture so that no later call allocates.
+ *   workspace (device) at least NVFP4_WORKSPACE_BYTES, 256-byte aligned; NULL returns to the
+ *   library's own workspace. The library zeroes it (synchronously: the call waits for the
+ *   device) and uses it for every later call on this device; the caller keeps it alive while
+ *   any call may use it, and calls this only when no work of the library is in flight on the
+ *   device.
+ * Errors: NVFP4_ERR_INVALID_ARG (bytes below NVFP4_WORKSPACE_BYTES), NVFP4_ERR_ALIGN,
+ * NVFP4_ERR_CUDA. */
+nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes);
 
 /* Synchronize `stream`, then read and clear the current device's status word into
  * *device_status (NVFP4_DEVICE_* bits). Returns NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT

@@ -268,6 +268,20 @@ def nvfp4_mx_dequantize(codes, scales, fmt="e4m3"):
     return out
 
 
+WORKSPACE_BYTES = 16384
+
+
+def nvfp4_set_workspace(workspace=None):
+    """Make a caller-owned CUDA tensor (at least WORKSPACE_BYTES, 256-byte aligned) the current
+    device's workspace; None returns to the library's own. Keep the tensor alive meanwhile."""
+    L = _lib.load()
+    if workspace is None:
+        _raise_if(L.nvfp4_set_workspace(None, 0), "nvfp4_set_workspace")
+        return
+    nbytes = workspace.numel() * workspace.element_size()
+    _raise_if(L.nvfp4_set_workspace(_ptr(workspace), nbytes), "nvfp4_set_workspace")
+
+
 def nvfp4_get_status(device=None):
     """Synchronize the current stream and return (status, device status bits); clears them."""
     L = _lib.load()

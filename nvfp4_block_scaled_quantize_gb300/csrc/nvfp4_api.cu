@@ -19,14 +19,15 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kWorkspaceBytes = 16384;
+constexpr size_t kWorkspaceBytes = NVFP4_WORKSPACE_BYTES;
 constexpr int kFuseWsOffset = 16;  // words: [0] status, [16 .. 16 + kFuseWsWords) fused barrier
 static_assert((kFuseWsOffset + kFuseWsWords) * 4 <= (int)kWorkspaceBytes, "workspace too small");
 
 struct DeviceState {
   bool ready = false;
   int sm_count = 0;
-  uint32_t* workspace = nullptr;  // [0] status word
+  uint32_t* workspace = nullptr;  // [0] status word; the library's own or the caller's
+  uint32_t* own = nullptr;        // the library's own workspace, allocated on first need
   uint64_t fuse_epoch = 0;        // epoch of the last single-launch amax on this workspace
   uint32_t fuse_count = 0;        // the workspace's arrival count after that launch
 };
@@ -40,29 +41,40 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+// Everything of a device's state but its workspace (under g_mutex).
+nvfp4_status init_device(DeviceState& st, int dev) {
+  if (st.ready) return NVFP4_OK;
+  if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  if (prepare_quantize_kernels() != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return NVFP4_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  st.ready = true;
+  return NVFP4_OK;
+}
+
 nvfp4_status device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState& st = g_devices[dev];
-  if (!st.ready) {
-    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    void* ws = nullptr;
-    if (cudaMalloc(&ws, kWorkspaceBytes) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (cudaMemset(ws, 0, kWorkspaceBytes) != cudaSuccess) return NVFP4_ERR_CUDA;
-    st.workspace = static_cast<uint32_t*>(ws);
-    if (prepare_quantize_kernels() != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (g_encode == nullptr) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return NVFP4_ERR_CUDA;
-      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  nvfp4_status r = init_device(st, dev);
+  if (r != NVFP4_OK) return r;
+  if (st.workspace == nullptr) {  // no caller workspace: the library's own, zeroed once
+    if (st.own == nullptr) {
+      void* ws = nullptr;
+      if (cudaMalloc(&ws, kWorkspaceBytes) != cudaSuccess) return NVFP4_ERR_CUDA;
+      if (cudaMemset(ws, 0, kWorkspaceBytes) != cudaSuccess) return NVFP4_ERR_CUDA;
+      st.own = static_cast<uint32_t*>(ws);
     }
-    st.ready = true;
+    st.workspace = st.own;
   }
   *out = &st;
   return NVFP4_OK;
@@ -547,6 +559,27 @@ NVFP4_EXPORT nvfp4_status nvfp4_mx_dequantize(const uint8_t* codes, const uint8_
   return cuda_status(launch_mx_dequantize(format, codes, scales, R, C, out,
                                           amax_grid(ds, R * (C / 32), 256),
                                           static_cast<cudaStream_t>(stream)));
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes) {
+  if (workspace != nullptr && bytes < kWorkspaceBytes) return NVFP4_ERR_INVALID_ARG;
+  if (workspace != nullptr && !aligned(workspace, 256)) return NVFP4_ERR_ALIGN;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  nvfp4_status r = init_device(st, dev);
+  if (r != NVFP4_OK) return r;
+  // the single-launch amax counts arrivals and tags maxima with epochs on the workspace: a
+  // workspace taken into use starts from zero, and so do the host's counters
+  uint32_t* ws = workspace != nullptr ? static_cast<uint32_t*>(workspace) : st.own;
+  if (ws != nullptr && (cudaMemset(ws, 0, kWorkspaceBytes) != cudaSuccess ||
+                        cudaDeviceSynchronize() != cudaSuccess))
+    return NVFP4_ERR_CUDA;
+  st.workspace = ws;  // NULL: the library's own, allocated on the next call if it has none
+  st.fuse_epoch = 0;
+  st.fuse_count = 0;
+  return NVFP4_OK;
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status) {

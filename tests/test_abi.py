@@ -168,3 +168,9 @@ def test_rmsnorm_argument_checks_return_before_any_cuda_call(L):
     assert L.nvfp4_rmsnorm_quantize(p(FAKE), p(FAKE), 4, 24, 1e-6, 0.0, ctypes.byref(cfg),
                                     p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None, None,
                                     None, None) == 2         # N % 16
+
+
+def test_set_workspace_argument_checks_return_before_any_cuda_call(L):
+    p = ctypes.c_void_p
+    assert L.nvfp4_set_workspace(p(FAKE), 16383) == 1       # below NVFP4_WORKSPACE_BYTES
+    assert L.nvfp4_set_workspace(p(FAKE + 16), 16384) == 3  # not 256-byte aligned

@@ -397,3 +397,23 @@ def test_full_size_workload_fused_matches_oracle(name):
                round_row="sr" if w.round_row_sr else "rn", seed=inp["seed"], fused_amax=True)
     out, ref = run_both(inp["x"], **cfg)
     assert_same(out, ref, "fused " + name)
+
+
+def test_caller_workspace_serves_the_fused_path_and_status():
+    """nvfp4_set_workspace: the single-launch amax and the status word on caller memory, then
+    back on the library's own; outputs equal the oracle's either way."""
+    dev = _cuda()
+    ws = torch.empty(api.WORKSPACE_BYTES // 4 + 64, dtype=torch.int32, device=dev)
+    try:
+        api.nvfp4_set_workspace(ws)
+        for seed in (1, 2):
+            x = workloads.normal_with_outliers(320, 1040, seed=seed, fraction=0.01, gain=30.0)
+            out, ref = run_both(x, rowwise=True, columnwise=True, fused_amax=True)
+            assert_same(out, ref, "caller workspace %d" % seed)
+        assert api.nvfp4_get_status(dev) == (0, 0)
+    finally:
+        api.nvfp4_set_workspace(None)
+        torch.cuda.synchronize()
+    x = workloads.normal_with_outliers(320, 1040, seed=3, fraction=0.01, gain=30.0)
+    out, ref = run_both(x, rowwise=True, columnwise=True, fused_amax=True)
+    assert_same(out, ref, "own workspace again")
