@@ -229,6 +229,27 @@ def _oracle_run(w, inp, rows):
     return time.perf_counter() - t0
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu's, else /proc/cpuinfo's, else the platform's)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -286,7 +307,7 @@ def cpu_baseline(w, inp, budget_s=15.0):
     cores = 1 if w.grouped else host_cores()
     dtn = dt1 if cores == 1 else _oracle_run_threads(w, inp, rows, cores)
     return {"value": b / dtn / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "single_core_value": b / dt1 / 1e9,
+            "cpu_model": cpu_model(), "single_core_value": b / dt1 / 1e9,
             "sample": "first %d of %d rows of %s (amax + every output): %.2f s on %d cores "
                       "(threads over 64-row chunks), %.2f s on 1 core"
                       % (rows, w.rows, w.name, dtn, cores, dt1)}
@@ -319,7 +340,7 @@ def run_reference(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "sample_rows": rows},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -453,6 +474,7 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+        "elements_per_s": w.rows * w.cols * args.steps * world / total_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": [w.rows, w.cols],
@@ -531,6 +553,7 @@ def mx_cpu_baseline(w, inp, fmt, budget_s=15.0):
     dtn = run(rows, cores)
     b = mx_ideal_bytes(w, fmt, rows)
     return {"value": b / dtn / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": "first %d of %d rows of %s, MX %s (every output): %.2f s on %d cores "
                       "(threads over 64-row chunks)" % (rows, w.rows, w.name, fmt, dtn, cores)}
 
@@ -611,6 +634,7 @@ def run_mx(args, world, rank, local):
     line = {
         "metric": MX_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+        "elements_per_s": w.rows * w.cols * args.steps * world / total_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": [w.rows, w.cols], "format": "MX" + fmt,
@@ -699,6 +723,7 @@ def run_producer(args, world, rank, local):
     line = {
         "metric": PRODUCER_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+        "elements_per_s": w.rows * w.cols * args.steps * world / total_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": [w.rows, w.cols], "ideal_bytes_per_step": ideal,
