@@ -143,6 +143,17 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N, const nvfp4_con
                             uint8_t* col_codes, uint8_t* col_scales, float* col_gscale,
                             void* stream);
 
+/* Per-expert absolute maxima of a grouped tensor ([PR4798] "Performance": the grouped amax
+ * kernel), the amax pass that nvfp4_quantize_grouped runs internally, exposed on its own.
+ *   offsets, E as nvfp4_quantize_grouped; H % 16 == 0.
+ *   amax_row (device) float[E] or NULL: max |x| over each expert's rows.
+ *   amax_col (device) float[E] or NULL: with cfg->rht_col, max |y| over the RHT output of each
+ *            expert's zero-padded 16-row column blocks; else max |x|.
+ * Bad offsets set NVFP4_DEVICE_BAD_OFFSETS (nvfp4_get_status). */
+nvfp4_status nvfp4_amax_grouped(const void* x, int64_t T, int64_t H, const int32_t* offsets,
+                                int32_t E, const nvfp4_config* cfg, float* amax_row,
+                                float* amax_col, void* stream);
+
 /* Grouped (MoE) quantization of a packed [T][H] tensor whose rows are split among E experts
  * by device-side cumulative offsets ([PR4798] "Grouped allocation tail", "Config surface and
  * AUTO": a packed tensor plus device-side offsets; rows past offsets[E-1] are not read or

@@ -24,7 +24,8 @@ EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quanti
             "nvfp4_host_pipeline_create", "nvfp4_host_pipeline_submit",
             "nvfp4_host_pipeline_join", "nvfp4_host_pipeline_destroy", "nvfp4_swizzle_scales",
             "nvfp4_mx_quantize", "nvfp4_mx_dequantize", "nvfp4_dequantize_ex",
-            "nvfp4_rmsnorm_amax", "nvfp4_rmsnorm_quantize", "nvfp4_set_workspace"]
+            "nvfp4_rmsnorm_amax", "nvfp4_rmsnorm_quantize", "nvfp4_set_workspace",
+            "nvfp4_amax_grouped"]
 
 
 class Config(ctypes.Structure):
@@ -107,6 +108,8 @@ def load(build_if_missing: bool = False):
     L.nvfp4_rmsnorm_quantize.restype = ctypes.c_int
     L.nvfp4_rmsnorm_quantize.argtypes = [vp, vp, i64, i64, f32, f32, cfgp, vp, vp, vp, vp, vp,
                                          vp, vp, vp, vp]
+    L.nvfp4_amax_grouped.restype = ctypes.c_int
+    L.nvfp4_amax_grouped.argtypes = [vp, i64, i64, vp, i32, cfgp, vp, vp, vp]
     L.nvfp4_set_workspace.restype = ctypes.c_int
     L.nvfp4_set_workspace.argtypes = [vp, ctypes.c_size_t]
     L.nvfp4_get_status.restype = ctypes.c_int

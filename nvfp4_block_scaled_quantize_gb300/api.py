@@ -139,6 +139,22 @@ def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwi
     return out
 
 
+def nvfp4_amax_grouped(x, offsets, rht_col=False, sign_mask=0):
+    """Per-expert amax of a packed grouped tensor: (max |x|, max |RHT(x)| if rht_col else
+    max |x|) as float32 [E] device tensors."""
+    _check_x(x)
+    L = _lib.load()
+    T, H = x.shape
+    E = offsets.shape[0]
+    cfg = make_config(rht_col=rht_col, sign_mask=sign_mask)
+    a_row = torch.empty(E, dtype=torch.float32, device=x.device)
+    a_col = torch.empty(E, dtype=torch.float32, device=x.device)
+    _raise_if(L.nvfp4_amax_grouped(_ptr(x), T, H, _ptr(offsets), E, ctypes.byref(cfg),
+                                   _ptr(a_row), _ptr(a_col), _stream(x.device)),
+              "nvfp4_amax_grouped")
+    return a_row, a_col
+
+
 def nvfp4_dequantize(codes, scales, gscale):
     """FP32 [R, C] reconstruction of codes [R, C/2] with scales [R, C/16] and gscale [2]."""
     L = _lib.load()

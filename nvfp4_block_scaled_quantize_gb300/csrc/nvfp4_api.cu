@@ -219,6 +219,30 @@ NVFP4_EXPORT nvfp4_status nvfp4_amax(const void* x, int64_t M, int64_t N, const 
   return cuda_status(launch_amax_flat(x, M * N, amax_row, amax_col, amax_flat_grid(ds, M * N / 8), s));
 }
 
+NVFP4_EXPORT nvfp4_status nvfp4_amax_grouped(const void* x, int64_t T, int64_t H,
+                                             const int32_t* offsets, int32_t E,
+                                             const nvfp4_config* cfg, float* amax_row,
+                                             float* amax_col, void* stream) {
+  nvfp4_status st = check_config(cfg);
+  if (st != NVFP4_OK) return st;
+  if (T < 0 || H < 0 || E < 1 || E > kMaxSegments || offsets == nullptr ||
+      (amax_row == nullptr && amax_col == nullptr))
+    return NVFP4_ERR_INVALID_ARG;
+  if (H % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (T > INT32_MAX - kTileM || H > INT32_MAX - kTileN) return NVFP4_ERR_SHAPE;
+  if ((T * H > 0 && (x == nullptr || !aligned(x, 16))) || !aligned(offsets, 4) ||
+      (amax_row && !aligned(amax_row, 4)) || (amax_col && !aligned(amax_col, 4)))
+    return NVFP4_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (amax_row && cudaMemsetAsync(amax_row, 0, 4 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (amax_col && cudaMemsetAsync(amax_col, 0, 4 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (T * H == 0) return NVFP4_OK;
+  return amax_tiles(ds, x, T, H, offsets, E, cfg->rht_sign_mask, cfg->rht_col != 0 && amax_col,
+                    amax_row, amax_col, 1, s);
+}
+
 NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
                                          const nvfp4_config* cfg, const float* amax_row,
                                          const float* amax_col, uint8_t* row_codes,

@@ -174,3 +174,16 @@ def test_set_workspace_argument_checks_return_before_any_cuda_call(L):
     p = ctypes.c_void_p
     assert L.nvfp4_set_workspace(p(FAKE), 16383) == 1       # below NVFP4_WORKSPACE_BYTES
     assert L.nvfp4_set_workspace(p(FAKE + 16), 16384) == 3  # not 256-byte aligned
+
+
+def test_amax_grouped_argument_checks_return_before_any_cuda_call(L):
+    p = ctypes.c_void_p
+    cfg = _cfg()
+    a = lambda T, H, offs, E, ar=FAKE, ac=FAKE: L.nvfp4_amax_grouped(
+        p(FAKE), T, H, offs, E, ctypes.byref(cfg), p(ar) if ar else None, p(ac) if ac else None,
+        None)
+    assert a(64, 32, p(FAKE), 0) == 1 and a(64, 32, p(FAKE), 257) == 1
+    assert a(64, 32, None, 2) == 1
+    assert a(64, 32, p(FAKE), 2, ar=0, ac=0) == 1           # nothing to write
+    assert a(64, 24, p(FAKE), 2) == 2                        # H % 16
+    assert a(64, 32, p(FAKE + 2), 2) == 3                    # offsets alignment

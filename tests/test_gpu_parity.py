@@ -417,3 +417,18 @@ def test_caller_workspace_serves_the_fused_path_and_status():
     x = workloads.normal_with_outliers(320, 1040, seed=3, fraction=0.01, gain=30.0)
     out, ref = run_both(x, rowwise=True, columnwise=True, fused_amax=True)
     assert_same(out, ref, "own workspace again")
+
+
+@pytest.mark.parametrize("case", GROUPED_CASES, ids=lambda c: c[0])
+@pytest.mark.parametrize("rht", [False, True])
+def test_amax_grouped_matches_oracle(case, rht):
+    dev = _cuda()
+    name, T, H, offs = case
+    x = workloads.normal_with_outliers(T, H, seed=T + 3 * H, fraction=0.01, gain=30.0)
+    mask = 0x3C5A
+    a_row, a_col = api.nvfp4_amax_grouped(x.to(dev), torch.from_numpy(np.asarray(offs, np.int32)).to(dev),
+                                          rht_col=rht, sign_mask=mask)
+    torch.cuda.synchronize()
+    _, _, rg, _, _, cg = oracle.quantize_grouped(x, offs, rht_col=rht, sign_mask=mask)
+    assert np.array_equal(_bits(a_row.cpu().numpy()), _bits(rg[:, 0].copy())), name
+    assert np.array_equal(_bits(a_col.cpu().numpy()), _bits(cg[:, 0].copy())), name
