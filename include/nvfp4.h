@@ -30,9 +30,10 @@
  * error status launched nothing and wrote nothing.
  *
  * Memory: the library allocates no memory on these calls except once per device, on the
- * first call that needs it: a small workspace (status word, the single-launch amax's arrival
- * count and maxima words; 16 KiB) allocated with cudaMalloc and kept until exit. Make that
- * first call outside CUDA-graph capture. The host pipeline (end of this file) allocates its
+ * first call that needs it: a small workspace (status word, the single-launch amax's counts,
+ * maxima words and epoch; 16 KiB) allocated with cudaMalloc and kept until exit. Make that
+ * first call outside CUDA-graph capture. Launches take no host-side state from call to call,
+ * so a captured call replays correctly (the single-launch amax included). The host pipeline (end of this file) allocates its
  * device staging when it is created, and nothing when work is submitted.
  */
 #ifndef NVFP4_H
@@ -89,7 +90,10 @@ typedef struct nvfp4_config {
                              quantize, folds its maxima into the workspace with an atomic max,
                              counts its arrival and waits (bounded) for all CTAs, then
                              quantizes (the re-read of x comes from L2 when x fits there).
-                             Fused calls share the device workspace's count and maxima: on one
+                             Fused calls share the device workspace's counts, maxima and epoch
+                             (kept on the device: once every CTA has arrived, CTA 0 readies
+                             the count for the next launch and advances the epoch, so
+                             captured calls replay correctly): on one
                              device they must not overlap in time (issue them on one stream).
                              Plain tensors only. */
   int32_t fast_math;      /* 0 = exact (default). 1 = the fast variant of [PR4798] "Fast math":
@@ -209,7 +213,7 @@ nvfp4_status nvfp4_dequantize_ex(const uint8_t* codes, const uint8_t* scales, co
  * fixed memory budget. The pages have no counterpart of this entry point; it exists only so
  * that such callers get the single-launch path.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its scratch
- * -- a status word, the CTAs' arrival count and two maxima words, 256 bytes in all -- is a
+ * -- a status word, the CTAs' counts, two maxima words and an epoch, 256 bytes in all -- is a
  * static device array that every GPU loading this library holds until exit. The caller still
  * passes x and every output.
  *   Arguments, layouts and shape rules as nvfp4_quantize with amax_row = amax_col = NULL and
@@ -219,9 +223,10 @@ nvfp4_status nvfp4_dequantize_ex(const uint8_t* codes, const uint8_t* scales, co
  *   A device whose launch would need more than 1024 CTAs is refused with
  *   NVFP4_ERR_UNSUPPORTED (GB300 launches one CTA per SM, 152).
  *   Every call on a device shares the array: calls that overlap on the GPU race (issue them on
- *   one stream). The array is zero when the library loads; each call tags its maxima with a
- *   larger epoch than the last call's and knows the arrival count its CTAs must reach, so
- *   nothing needs clearing between calls. A wait that gives up is recorded in the array's own
+ *   one stream). The array is zero when the library loads; each launch tags its maxima with the
+ *   epoch after the one it reads there, and once its CTAs have arrived CTA 0 readies the count
+ *   for the next launch and advances the epoch, so nothing needs clearing between calls and a
+ *   captured call replays correctly. A wait that gives up is recorded in the array's own
  *   status word, which nvfp4_get_status does not read. */
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const nvfp4_config* cfg,
                                     uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,
@@ -299,8 +304,8 @@ nvfp4_status nvfp4_mx_quantize(const void* x, int64_t M, int64_t N, int32_t form
 nvfp4_status nvfp4_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int32_t format,
                                  int64_t R, int64_t C, float* out, void* stream);
 
-/* The per-device workspace: the status word the kernels report to, and the arrival count and
- * epoch-tagged maxima of the single-launch amax. By default the library allocates it with
+/* The per-device workspace: the status word the kernels report to, and the counts, the
+ * epoch-tagged maxima and the epoch of the single-launch amax. By default the library allocates it with
  * cudaMalloc (once per device, on the first call that needs it, zeroed) and never frees it. */
 #define NVFP4_WORKSPACE_BYTES 16384
 
@@ -319,6 +324,15 @@ nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes);
  * *device_status (NVFP4_DEVICE_* bits). Returns NVFP4_ERR_DEVICE_STATUS or NVFP4_ERR_TIMEOUT
  * when bits were set, NVFP4_OK otherwise. */
 nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status);
+
+/* Test hook for the bounded wait of the single-launch amax: the next nvfp4_quantize call that
+ * takes the single-launch path (on any device) waits for `extra` arrivals more than its grid
+ * has CTAs. With extra > 0 no launch can reach that count, so every CTA gives up after its
+ * bounded wait (about 2 s), stores nothing, sets NVFP4_DEVICE_TIMEOUT and exits; CTA 0 still
+ * readies the workspace for the next launch, so the next call runs normally. The hook is consumed by
+ * that one call (0 clears it). Not for production use.
+ * Errors: NVFP4_ERR_INVALID_ARG (extra outside 0 .. 1024). */
+nvfp4_status nvfp4_debug_fused_extra_arrivals(int32_t extra);
 
 /* Host pipeline: quantization of tensors that live in host memory, with the copies of
  * consecutive submissions overlapped (the input of one on the host-to-device link while the

@@ -307,6 +307,13 @@ def nvfp4_get_status(device=None):
     return status, bits.value
 
 
+def nvfp4_debug_fused_extra_arrivals(extra):
+    """Test hook: the next single-launch amax call waits for `extra` arrivals more than its grid
+    has CTAs, so its bounded wait runs out (about 2 s) and it reports NVFP4_DEVICE_TIMEOUT."""
+    _raise_if(_lib.load().nvfp4_debug_fused_extra_arrivals(int(extra)),
+              "nvfp4_debug_fused_extra_arrivals")
+
+
 def quantize_from_host(x_host, pinned_out=None, **kw):
     """End-to-end call for host data: copy a pinned host BF16 tensor to the device, quantize,
     and copy every output back into pinned host tensors (all on the current stream)."""

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "nvfp4.h"
@@ -28,12 +29,12 @@ struct DeviceState {
   int sm_count = 0;
   uint32_t* workspace = nullptr;  // [0] status word; the library's own or the caller's
   uint32_t* own = nullptr;        // the library's own workspace, allocated on first need
-  uint64_t fuse_epoch = 0;        // epoch of the last single-launch amax on this workspace
-  uint32_t fuse_count = 0;        // the workspace's arrival count after that launch
 };
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
+// Arrivals the next single-launch amax awaits beyond its grid (nvfp4_debug_fused_extra_arrivals)
+std::atomic<int32_t> g_fuse_extra{0};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -324,16 +325,10 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
   const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};
-  if (!fused) return cuda_status(launch_quantize(mode, q, grid, s));
-  // every CTA adds one to the arrival count; the epoch orders this launch's maxima after all
-  // earlier ones (the workspace starts zeroed: epoch 0, count 0)
-  std::lock_guard<std::mutex> lock(g_mutex);
-  q.fuse_epoch = ds->fuse_epoch + 1;
-  q.fuse_target = ds->fuse_count + (uint32_t)grid;
-  if (launch_quantize(mode, q, grid, s) != cudaSuccess) return NVFP4_ERR_CUDA;
-  ds->fuse_epoch = q.fuse_epoch;
-  ds->fuse_count = q.fuse_target;
-  return NVFP4_OK;
+  // the barrier's counts and epoch live on the device (CTA 0 readies them for the next launch),
+  // so the launch depends on no host state and can be captured in a CUDA graph
+  if (fused) q.fuse_extra = g_fuse_extra.exchange(0);
+  return cuda_status(launch_quantize(mode, q, grid, s));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
@@ -594,15 +589,19 @@ NVFP4_EXPORT nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes) {
   DeviceState& st = g_devices[dev];
   nvfp4_status r = init_device(st, dev);
   if (r != NVFP4_OK) return r;
-  // the single-launch amax counts arrivals and tags maxima with epochs on the workspace: a
-  // workspace taken into use starts from zero, and so do the host's counters
+  // the single-launch amax keeps its counts and epoch on the workspace: a workspace taken into
+  // use starts from zero
   uint32_t* ws = workspace != nullptr ? static_cast<uint32_t*>(workspace) : st.own;
   if (ws != nullptr && (cudaMemset(ws, 0, kWorkspaceBytes) != cudaSuccess ||
                         cudaDeviceSynchronize() != cudaSuccess))
     return NVFP4_ERR_CUDA;
   st.workspace = ws;  // NULL: the library's own, allocated on the next call if it has none
-  st.fuse_epoch = 0;
-  st.fuse_count = 0;
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_debug_fused_extra_arrivals(int32_t extra) {
+  if (extra < 0 || extra > kFuseMaxCtas) return NVFP4_ERR_INVALID_ARG;
+  g_fuse_extra.store(extra);
   return NVFP4_OK;
 }
 

@@ -28,8 +28,9 @@ constexpr int kColCodeStage = kWarpsPerGroup * kTileN * 8;   // [4 slabs][128 ch
 constexpr int kColScaleStage = kWarpsPerGroup * kTileN;      // [4 slabs][256 B]
 constexpr int kSmemStages = 0;
 constexpr int kSmemColCodes = kSmemStages + kStages * kStageBytes;
-constexpr int kSmemColScales = kSmemColCodes + kGroups * kColCodeStage;
-constexpr int kSmemTables = kSmemColScales + kGroups * kColScaleStage;  // per group: 2 x 128 f32
+constexpr int kColStageBufs = 2;                             // per group (double-buffered)
+constexpr int kSmemColScales = kSmemColCodes + kGroups * kColStageBufs * kColCodeStage;
+constexpr int kSmemTables = kSmemColScales + kGroups * kColStageBufs * kColScaleStage;  // per group: 2 x 128 f32
 constexpr int kSmemSegStart = kSmemTables + kGroups * 2 * kTableEntries * 4;
 constexpr int kSmemSegEnd = kSmemSegStart + 4 * kMaxSegments;
 constexpr int kSmemSegCol0 = kSmemSegEnd + 4 * kMaxSegments;
@@ -41,12 +42,11 @@ constexpr int kSmemIssued = kSmemFlags + 16;                          // int32 [
 constexpr int kSmemFused = kSmemIssued + 4 * kStages;            // uint32 [32 + 4]
 constexpr int kQuantSmemBytes = kSmemFused + 4 * 36;
 
-// Workspace of the single-launch (fused amax) path, 8-byte aligned: word 0 counts CTA arrivals
-// (it only grows; the host knows the value each launch must reach), words 2-3 and 4-5 are the
-// rowwise and columnwise maxima as (launch epoch << 16) | 16-bit magnitude. Epochs increase
-// from launch to launch, so an atomic max needs no clearing in between.
+// Workspace of the single-launch (fused amax) path, 8-byte aligned, zeroed before first use:
+// the arrival and exit counts of the running launch, the rowwise and columnwise maxima tagged
+// with the launch's epoch, and the epoch itself, all kept on the device (fused_amax.cuh).
 constexpr int kFuseMaxCtas = 1024;
-constexpr int kFuseWsWords = 6;
+constexpr int kFuseWsWords = 8;
 
 // Arguments of the quantize kernel: one BF16 tensor split into row segments (one segment for
 // a plain tensor, one per expert for the grouped case).
@@ -73,9 +73,9 @@ struct QuantArgs {
   uint32_t* status;
   int32_t fused;                    // 1: compute the amax inside this launch (one segment)
   int32_t fast;                     // 1: fast-math element multipliers (rcp.approx)
-  uint32_t fuse_target;             // fuse_ws[0] once every CTA of this launch has arrived
-  uint64_t fuse_epoch;              // larger than any earlier launch's on fuse_ws (< 2^48)
-  uint32_t* fuse_ws;                // kFuseWsWords words, 8-byte aligned
+  int32_t fuse_extra;               // arrivals awaited beyond the grid's: 0 (> 0 only to make
+                                    // the barrier time out on purpose, in tests)
+  uint32_t* fuse_ws;                // kFuseWsWords words, 8-byte aligned (fused_amax.cuh)
 };
 
 // Round keys of Philox4x32-10 for a 64-bit seed: key (lo32, hi32) bumped by the Weyl constants

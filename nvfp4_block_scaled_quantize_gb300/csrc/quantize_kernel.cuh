@@ -309,7 +309,9 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   // ---- single-launch amax: stream the local tiles through the stage ring (last to first),
   // reduce, fold into the workspace maxima, wait for every CTA's arrival ----
   float* fused_amax = reinterpret_cast<float*>(smem + kSmemFused) + 32;  // [0] row, [1] col
+  uint64_t fuse_e = 0u;  // thread 0: the workspace epoch at the start of this launch
   if (fused) {
+    if (tid == 0) fuse_e = fuse_epoch(a.fuse_ws);
     uint32_t m = 0u, mt = 0u;
     bool ok = true;
     for (int k = g; k < n_local; k += kGroups) {
@@ -356,12 +358,13 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     uint32_t mc = mr;
     if (COL && RHT) mc = cta_max(max(mt & 0xFFFFu, mt >> 16), red);
     if (tid == 0) {
-      fuse_arrive(a.fuse_ws, a.fuse_epoch, mr, mc);
+      fuse_arrive(a.fuse_ws, fuse_e, mr, mc);
       uint32_t pr = 0u, pc = 0u;
-      if (!fuse_wait(a.fuse_ws, a.fuse_target, a.fuse_epoch, pr, pc)) {
+      if (!fuse_wait(a.fuse_ws, fuse_e, gridDim.x + (uint32_t)a.fuse_extra, pr, pc)) {
         flags[3] = 1;
         atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
       }
+      if (blockIdx.x == 0) fuse_advance(a.fuse_ws, fuse_e);
       fused_amax[0] = __uint_as_float(pr << 16);
       fused_amax[1] = __uint_as_float(pc << 16);
     }
@@ -400,8 +403,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int kb = lane >> 1;              // rowwise block of the tile row (lane pair)
   float* tab_row = reinterpret_cast<float*>(smem + kSmemTables) + g * 2 * kTableEntries;
   float* tab_col = tab_row + kTableEntries;
-  uint8_t* cc_stage = smem + kSmemColCodes + g * kColCodeStage;
-  uint8_t* cs_stage = smem + kSmemColScales + g * kColScaleStage;
+  // columnwise staging, two buffers per group: a tile's codes and scales are staged in one
+  // while the previous tile's leave from the other
+  uint8_t* cc_base = smem + kSmemColCodes + g * kColStageBufs * kColCodeStage;
+  uint8_t* cs_base = smem + kSmemColScales + g * kColStageBufs * kColScaleStage;
   const int64_t row_nb = N / 16;
   const int64_t col_nb = a.col_ld / 16;
   int cur_seg = -1;
@@ -421,6 +426,64 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     cur_seg = e;
   };
+  // Write-out of a tile's staged columnwise codes and scales by the whole group: thread gt owns
+  // the column pair 2 gt, 2 gt + 1, and a column's 64 codes leave as one 32-byte store.
+  auto write_out = [&](const Coord& wc, const uint8_t* ccs, const uint8_t* css) {
+    const int nrb = (wc.nrows + 15) >> 4;
+    const int64_t col0 = (int64_t)wc.n0 + 2 * gt;   // this thread's column pair
+    if (col0 < N) {
+      uint4 d[kWarpsPerGroup];
+#pragma unroll
+      for (int r = 0; r < kWarpsPerGroup; r++)
+        if (r < nrb) d[r] = *reinterpret_cast<const uint4*>(ccs + r * (kTileN * 8) + swz(gt) * 16);
+      uint8_t* dst0 = a.col_codes + col0 * (a.col_ld / 2) + wc.colpos / 2;
+      uint8_t* dst1 = dst0 + a.col_ld / 2;
+      const uintptr_t dbits = reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1);
+      const bool whole = nrb == kWarpsPerGroup && wc.skip == 0;  // all four slabs are ours
+      if (whole && (dbits & 31) == 0) {
+        // each column's 64 codes are one full 32-byte sector: one store per column
+        stg256(dst0, make_uint4(d[0].x, d[0].y, d[1].x, d[1].y), make_uint4(d[2].x, d[2].y, d[3].x, d[3].y));
+        stg256(dst1, make_uint4(d[0].z, d[0].w, d[1].z, d[1].w), make_uint4(d[2].z, d[2].w, d[3].z, d[3].w));
+      } else if (whole && (dbits & 15) == 0) {
+        reinterpret_cast<uint4*>(dst0)[0] = make_uint4(d[0].x, d[0].y, d[1].x, d[1].y);
+        reinterpret_cast<uint4*>(dst0)[1] = make_uint4(d[2].x, d[2].y, d[3].x, d[3].y);
+        reinterpret_cast<uint4*>(dst1)[0] = make_uint4(d[0].z, d[0].w, d[1].z, d[1].w);
+        reinterpret_cast<uint4*>(dst1)[1] = make_uint4(d[2].z, d[2].w, d[3].z, d[3].w);
+      } else {
+#pragma unroll
+        for (int r = 0; r < kWarpsPerGroup; r++) {
+          if (r >= wc.skip && r < nrb) {
+            *reinterpret_cast<uint2*>(dst0 + 8 * r) = make_uint2(d[r].x, d[r].y);
+            *reinterpret_cast<uint2*>(dst1 + 8 * r) = make_uint2(d[r].z, d[r].w);
+          }
+        }
+      }
+      uint32_t sc0 = 0, sc1 = 0;
+#pragma unroll
+      for (int r = 0; r < kWarpsPerGroup; r++) {
+        if (r < nrb) {
+          const uint32_t pr = *reinterpret_cast<const uint16_t*>(css + r * kTileN + 2 * gt);
+          sc0 |= (pr & 0xFFu) << (8 * r);
+          sc1 |= (pr >> 8) << (8 * r);
+        }
+      }
+      uint8_t* sd0 = a.col_scales + col0 * col_nb + wc.colpos / 16;
+      uint8_t* sd1 = sd0 + col_nb;
+      if (whole && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
+        *reinterpret_cast<uint32_t*>(sd0) = sc0;
+        *reinterpret_cast<uint32_t*>(sd1) = sc1;
+      } else {
+        for (int r = wc.skip; r < nrb; r++) {
+          sd0[r] = (uint8_t)(sc0 >> (8 * r));
+          sd1[r] = (uint8_t)(sc1 >> (8 * r));
+        }
+      }
+    }
+  };
+  Coord prev{};           // the group's previous tile, staged in buffer buf ^ 1
+  bool have_prev = false;
+  int buf = 0;
+
   if (!AMAX_ONLY && plain && n_local > g) set_segment(0);  // overlaps the first loads (or follows the amax)
 
   for (int i = g; i < n_local; i += kGroups) {
@@ -464,8 +527,9 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           if (r >= slab_rows) v[r] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    // All four slabs are in registers: the stage can be refilled, the group's staging is free
-    // (the previous tile was written out), and the group's abort flag is settled.
+    // All four slabs are in registers: the stage can be refilled, the previous tile's staging
+    // is complete (every warp staged it before arriving here), the buffer before it was
+    // written out, and the group's abort flag is settled.
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     if (flags[g]) break;
     if (gt == 0 && i + kStages < n_local) {
@@ -506,6 +570,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       continue;
     }
 
+    if (COL && have_prev)
+      write_out(prev, cc_base + (buf ^ 1) * kColCodeStage, cs_base + (buf ^ 1) * kColScaleStage);
+    uint8_t* cc_stage = cc_base + buf * kColCodeStage;
+    uint8_t* cs_stage = cs_base + buf * kColScaleStage;
     if (c.seg != cur_seg) set_segment(c.seg);  // uniform across the group
 
     const bool lane_cols = (int64_t)c.n0 + lane * 8 < N;  // all 8 of the lane's columns exist
@@ -698,60 +766,14 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       }
     }
 
-    // ---- group write-out of the staged columnwise codes and scales ----
+    // the staged codes leave after the next tile's barrier (or after the loop)
+    prev = c;
+    have_prev = true;
+    buf ^= 1;
+  }
+  if (COL && !AMAX_ONLY && have_prev && !flags[g]) {
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
-    if (COL) {
-      const int nrb = (c.nrows + 15) >> 4;
-      const int64_t col0 = (int64_t)c.n0 + 2 * gt;   // this thread's column pair
-      if (col0 < N) {
-        uint4 d[kWarpsPerGroup];
-#pragma unroll
-        for (int r = 0; r < kWarpsPerGroup; r++)
-          if (r < nrb) d[r] = *reinterpret_cast<const uint4*>(cc_stage + r * (kTileN * 8) + swz(gt) * 16);
-        uint8_t* dst0 = a.col_codes + col0 * (a.col_ld / 2) + c.colpos / 2;
-        uint8_t* dst1 = dst0 + a.col_ld / 2;
-        const uintptr_t dbits = reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1);
-        const bool whole = nrb == kWarpsPerGroup && c.skip == 0;  // all four slabs are ours
-        if (whole && (dbits & 31) == 0) {
-          // each column's 64 codes are one full 32-byte sector: one store per column
-          stg256(dst0, make_uint4(d[0].x, d[0].y, d[1].x, d[1].y), make_uint4(d[2].x, d[2].y, d[3].x, d[3].y));
-          stg256(dst1, make_uint4(d[0].z, d[0].w, d[1].z, d[1].w), make_uint4(d[2].z, d[2].w, d[3].z, d[3].w));
-        } else if (whole && (dbits & 15) == 0) {
-          reinterpret_cast<uint4*>(dst0)[0] = make_uint4(d[0].x, d[0].y, d[1].x, d[1].y);
-          reinterpret_cast<uint4*>(dst0)[1] = make_uint4(d[2].x, d[2].y, d[3].x, d[3].y);
-          reinterpret_cast<uint4*>(dst1)[0] = make_uint4(d[0].z, d[0].w, d[1].z, d[1].w);
-          reinterpret_cast<uint4*>(dst1)[1] = make_uint4(d[2].z, d[2].w, d[3].z, d[3].w);
-        } else {
-#pragma unroll
-          for (int r = 0; r < kWarpsPerGroup; r++) {
-            if (r >= c.skip && r < nrb) {
-              *reinterpret_cast<uint2*>(dst0 + 8 * r) = make_uint2(d[r].x, d[r].y);
-              *reinterpret_cast<uint2*>(dst1 + 8 * r) = make_uint2(d[r].z, d[r].w);
-            }
-          }
-        }
-        uint32_t sc0 = 0, sc1 = 0;
-#pragma unroll
-        for (int r = 0; r < kWarpsPerGroup; r++) {
-          if (r < nrb) {
-            const uint32_t pr = *reinterpret_cast<const uint16_t*>(cs_stage + r * kTileN + 2 * gt);
-            sc0 |= (pr & 0xFFu) << (8 * r);
-            sc1 |= (pr >> 8) << (8 * r);
-          }
-        }
-        uint8_t* sd0 = a.col_scales + col0 * col_nb + c.colpos / 16;
-        uint8_t* sd1 = sd0 + col_nb;
-        if (whole && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
-          *reinterpret_cast<uint32_t*>(sd0) = sc0;
-          *reinterpret_cast<uint32_t*>(sd1) = sc1;
-        } else {
-          for (int r = c.skip; r < nrb; r++) {
-            sd0[r] = (uint8_t)(sc0 >> (8 * r));
-            sd1[r] = (uint8_t)(sc1 >> (8 * r));
-          }
-        }
-      }
-    }
+    write_out(prev, cc_base + (buf ^ 1) * kColCodeStage, cs_base + (buf ^ 1) * kColScaleStage);
   }
 
   // Every load issued into a stage is waited for by the group that owns its tile, unless that

@@ -3,7 +3,7 @@
 // real-time path that must never reach cudaMalloc (which can synchronize the device), or a
 // host that hands this library a fixed memory budget. The regular entry points allocate a
 // small per-device workspace on their first call; this one keeps its scratch (a status word,
-// the CTAs' arrival count and the two launch-tagged maxima words) in a file-scope device array
+// the CTAs' counts, the launch-tagged maxima words and the epoch) in a file-scope device array
 // instead, so it calls no cudaMalloc, cudaFree or other allocating routine.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -21,9 +21,8 @@ namespace nvfp4 {
 namespace {
 
 // Scratch of every nvfp4_quantize_noalloc call on a device (64 words, 256 bytes): word 0 the
-// device status word, words 4 .. 4 + kFuseWsWords the arrival count and the maxima words of
-// the single-launch amax. Zero when the library is loaded (epoch 0, count 0) and kept until
-// exit.
+// device status word, words 4 .. 4 + kFuseWsWords the counts, maxima and epoch of the
+// single-launch amax. Zero when the library is loaded and kept until exit.
 constexpr int kScratchStatus = 0;
 constexpr int kScratchFuse = 4;
 constexpr int kScratchWords = 64;
@@ -36,8 +35,6 @@ struct NoAllocDevice {
   bool ready = false;
   int sm_count = 0;
   uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-  uint64_t epoch = 0;           // epoch of the last call on this device
-  uint32_t count = 0;           // the scratch's arrival count after that call
 };
 
 std::mutex g_mutex;
@@ -144,15 +141,10 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   q.fused = 1;
   q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
   q.fuse_ws = d->scratch + kScratchFuse;
-  // each CTA adds one to the arrival count and tags its maxima with a larger epoch than any
-  // earlier call's, so nothing has to be cleared before the launch
-  std::lock_guard<std::mutex> lock(g_mutex);
-  q.fuse_epoch = d->epoch + 1;
-  q.fuse_target = d->count + (uint32_t)grid;
+  q.fuse_extra = 0;
+  // the barrier's counts and epoch live in the scratch (zero-initialised; CTA 0 readies them for
+  // the next launch), so nothing is cleared before the launch and it can be captured in a graph
   const QuantMode mode{row, col, rht, two_d, cfg->round_row == NVFP4_ROUND_SR,
                        cfg->round_col == NVFP4_ROUND_SR, q.fast && rht};
-  if (launch_quantize(mode, q, grid, s) != cudaSuccess) return NVFP4_ERR_CUDA;
-  d->epoch = q.fuse_epoch;
-  d->count = q.fuse_target;
-  return NVFP4_OK;
+  return launch_quantize(mode, q, grid, s) != cudaSuccess ? NVFP4_ERR_CUDA : NVFP4_OK;
 }

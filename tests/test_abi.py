@@ -187,3 +187,9 @@ def test_amax_grouped_argument_checks_return_before_any_cuda_call(L):
     assert a(64, 32, p(FAKE), 2, ar=0, ac=0) == 1           # nothing to write
     assert a(64, 24, p(FAKE), 2) == 2                        # H % 16
     assert a(64, 32, p(FAKE + 2), 2) == 3                    # offsets alignment
+
+
+def test_debug_hook_argument_checks(L):
+    assert L.nvfp4_debug_fused_extra_arrivals(-1) == 1
+    assert L.nvfp4_debug_fused_extra_arrivals(1025) == 1
+    assert L.nvfp4_debug_fused_extra_arrivals(0) == 0  # clears it: no call consumes it here

@@ -1,0 +1,146 @@
+"""CUDA-graph capture and the bounded wait of the single-launch amax.
+
+A captured call is replayed on new data written into the same input buffer; every replay must
+match the oracle on that data bit for bit. The data's amax falls from replay to replay, so a
+barrier that kept its maxima from an earlier replay (or counted arrivals against a target fixed
+at capture) would show up as a wrong global scale.
+
+The timeout test asks the next single-launch call to wait for one CTA more than its grid has:
+every CTA gives up after its bounded wait, records NVFP4_DEVICE_TIMEOUT and exits, and the call
+after it runs normally on the same workspace. Nothing faults or hangs: the wait has a limit."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_block_scaled_quantize_gb300 import _lib, api, workloads
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("row_codes", "row_scales", "row_gscale", "col_codes", "col_scales", "col_gscale")
+
+
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda")
+
+
+def _bits(a):
+    a = np.asarray(a)
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+def _same(got, ref, what):
+    for k in KEYS:
+        if k in ref:
+            g, r = _bits(got[k].cpu().numpy()), _bits(ref[k])
+            assert g.shape == r.shape, (what, k)
+            assert np.array_equal(g, r), (what, k, int((g != r).sum()))
+
+
+def _oracle_cfg(cfg):
+    return oracle.Config(rowwise=cfg.get("rowwise", True), columnwise=cfg.get("columnwise", False),
+                         block2d=cfg.get("block2d", False),
+                         round_row_sr=cfg.get("round_row", "rn") == "sr",
+                         round_col_sr=cfg.get("round_col", "rn") == "sr",
+                         rht_col=cfg.get("rht_col", False), sign_mask=cfg.get("sign_mask", 0),
+                         seed=cfg.get("seed", 0), offset=cfg.get("offset", 0))
+
+
+# the data of replay k: the same shape, gains falling so that each amax is below the last
+GAINS = (60.0, 20.0, 5.0, 40.0)
+
+MODES = {
+    "fused_rowcol": dict(rowwise=True, columnwise=True, fused_amax=True),
+    "fused_rht_sr": dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x3C5A,
+                         round_col="sr", seed=77, offset=3, fused_amax=True),
+    "fused_2d": dict(rowwise=True, columnwise=True, block2d=True, fused_amax=True),
+    "two_pass_rowcol": dict(rowwise=True, columnwise=True, fused_amax=False),
+}
+
+
+@pytest.mark.parametrize("mode", sorted(MODES))
+@pytest.mark.parametrize("shape", [(304, 1040), (2048, 4096)], ids=lambda s: "%dx%d" % s)
+def test_captured_call_replays_on_new_data(mode, shape):
+    dev = _cuda()
+    M, N = shape
+    cfg = MODES[mode]
+    xs = [workloads.normal_with_outliers(M, N, seed=50 + k, fraction=0.01, gain=g)
+          for k, g in enumerate(GAINS)]
+    static_x = xs[0].to(dev)
+    out = api.alloc_outputs(M, N, dev, cfg["rowwise"], cfg["columnwise"])
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # warm-up outside capture (workspace, kernel setup)
+        api.nvfp4_quantize(static_x, out=out, **cfg)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        api.nvfp4_quantize(static_x, out=out, **cfg)
+    for k, x in enumerate(xs):
+        static_x.copy_(x.to(dev))
+        graph.replay()
+        torch.cuda.synchronize()
+        _same(out, oracle.quantize(x, _oracle_cfg(cfg)), "%s replay %d" % (mode, k))
+    status, bits = api.nvfp4_get_status(dev)
+    assert (status, bits) == (0, 0)
+
+
+def _noalloc(x, out, cfg):
+    L = _lib.load()
+    M, N = x.shape
+    p = lambda k: ctypes.c_void_p(out[k].data_ptr()) if k in out else None
+    stream = ctypes.c_void_p(torch.cuda.current_stream(x.device).cuda_stream)
+    status = L.nvfp4_quantize_noalloc(ctypes.c_void_p(x.data_ptr()), M, N,
+                                      ctypes.byref(api.make_config(**cfg)), p("row_codes"),
+                                      p("row_scales"), p("row_gscale"), p("col_codes"),
+                                      p("col_scales"), p("col_gscale"), stream)
+    assert status == 0, L.nvfp4_status_string(status).decode()
+
+
+def test_captured_noalloc_call_replays_on_new_data():
+    dev = _cuda()
+    M, N = 640, 2064
+    xs = [workloads.normal_with_outliers(M, N, seed=90 + k, fraction=0.01, gain=g)
+          for k, g in enumerate(GAINS)]
+    static_x = xs[0].to(dev)
+    out = api.alloc_outputs(M, N, dev, True, True)
+    cfg = dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x0F0F)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # the first call (set-up) outside capture
+        _noalloc(static_x, out, cfg)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        _noalloc(static_x, out, cfg)
+    for k, x in enumerate(xs):
+        static_x.copy_(x.to(dev))
+        graph.replay()
+        torch.cuda.synchronize()
+        _same(out, oracle.quantize(x, _oracle_cfg(cfg)), "noalloc replay %d" % k)
+
+
+@pytest.mark.parametrize("shape", [(64, 256), (4096, 4096)], ids=lambda s: "%dx%d" % s)
+def test_barrier_wait_runs_out_then_next_call_is_correct(shape):
+    dev = _cuda()
+    M, N = shape
+    x = workloads.normal_with_outliers(M, N, seed=7, fraction=0.01, gain=30.0)
+    cfg = dict(rowwise=True, columnwise=True, fused_amax=True)
+    api.nvfp4_quantize(x.to(dev), **cfg)  # set-up outside the measured part
+    assert api.nvfp4_get_status(dev) == (0, 0)
+    api.nvfp4_debug_fused_extra_arrivals(1)  # one arrival more than the grid can make
+    api.nvfp4_quantize(x.to(dev), **cfg)
+    status, bits = api.nvfp4_get_status(dev)  # waits for the launch (about 2 s)
+    assert _lib.STATUS_NAMES[status] == "NVFP4_ERR_TIMEOUT" and bits & _lib.DEVICE_TIMEOUT, \
+        (status, bits)
+    # the hook was consumed and CTA 0 readied the barrier: a normal call again
+    out = api.nvfp4_quantize(x.to(dev), **cfg)
+    torch.cuda.synchronize()
+    _same(out, oracle.quantize(x, _oracle_cfg(cfg)), "after timeout")
+    assert api.nvfp4_get_status(dev) == (0, 0)
