@@ -5,11 +5,13 @@ kernel a caller runs to turn a BF16 tensor into NVFP4 codes, E4M3 scales and FP3
 scales -- by default one nvfp4_quantize launch that computes the amax itself (fused_amax), or
 with --pipeline two_pass the amax kernel (nvfp4_amax) followed by the quantize kernel.
 Ideal bytes per step = one BF16 read + code writes + scale writes (the metric's roofline
-bytes). L2 is flushed (a 256 MiB write) before every timed step; device time comes from CUDA
-events on the launching stream. Prints ONE JSON line (rank 0).
+bytes). Between timed steps L2 holds none of the step's data: by default (--l2 rotate) the steps
+cycle through K input/output sets whose total is at least three times the L2 size (inputs
+larger than L2), with --l2 flush a 256 MiB buffer is written before every step. Device time
+comes from CUDA events on the launching stream. Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--pipeline fused|two_pass]
+                  [--workload NAME] [--pipeline fused|two_pass] [--l2 rotate|flush]
 """
 import argparse
 import hashlib
@@ -346,6 +348,35 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def nbytes(*tensors):
+    return sum(t.numel() * t.element_size() for t in tensors)
+
+
+def rotation_sets(set_bytes, l2_bytes):
+    """The fewest input/output sets of set_bytes each that together hold 3 x l2_bytes."""
+    return max(1, -(-3 * l2_bytes // set_bytes))
+
+
+def l2_plan(args, dev, set_bytes):
+    """How the timed steps keep their data out of L2. --l2 rotate (default): K input/output sets
+    with K x set_bytes >= 3 x L2 and step j on set j % K, so a step's data was last touched three
+    L2 capacities earlier (inputs larger than L2); --l2 flush: one set, and a 256 MiB buffer
+    written before every step. Returns (K, the flush buffer or None, the note for the config)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    if args.l2 == "flush":
+        return (1, torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev),
+                "flushed before every timed step (256 MiB write)")
+    k = rotation_sets(set_bytes, l2)
+    return k, None, ("inputs larger than L2: %d rotating input/output sets of %.0f MiB (%.1fx "
+                     "the %.0f MiB L2), no flush" % (k, set_bytes / 2**20, k * set_bytes / l2,
+                                                     l2 / 2**20))
+
+
+def clear_l2(flush):
+    if flush is not None:
+        flush.zero_()
+
+
 def run_ours(args, world, rank, local):
     from nvfp4_block_scaled_quantize_gb300 import api, _lib
     _lib.load()
@@ -357,43 +388,51 @@ def run_ours(args, world, rank, local):
     kw["fast_math"] = args.fast_math
     ideal = ideal_bytes(w, offsets=inp.get("offsets"))
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     if w.grouped:
         offsets = torch.from_numpy(inp["offsets"]).to(dev)
         cap = int(sum((int(c) + 15) // 16 * 16 for c in np.diff(np.concatenate([[0], inp["offsets"]]))))
-        out = api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise, col_ld=cap,
-                                groups=w.experts)
+        alloc = lambda: api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise,
+                                          col_ld=cap, groups=w.experts)
+    else:
+        alloc = lambda: api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise)
+    out = alloc()
+    n_sets, flush, l2_note = l2_plan(args, dev, nbytes(x, *out.values()))
+    xs, outs = [x], [out]
+    for _ in range(n_sets - 1):
+        xs.append(x.clone())
+        outs.append(alloc())
 
-        def step(ev=None):
+    if w.grouped:
+        def step(j, ev=None):
             if ev:
                 ev[0].record(stream)
-            api.nvfp4_quantize_grouped(x, offsets, col_capacity=cap, out=out,
-                                       **kw)
+            api.nvfp4_quantize_grouped(xs[j % n_sets], offsets, col_capacity=cap,
+                                       out=outs[j % n_sets], **kw)
             if ev:
                 ev[2].record(stream)
         launches_per_step = 2
         kernel_split = False
     else:
-        out = api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise)
         rht_amax = w.rht_col
 
         if args.pipeline == "fused":
-            def step(ev=None):
+            def step(j, ev=None):
                 if ev:
                     ev[0].record(stream)  # one launch: the step and the kernel are the same span
-                api.nvfp4_quantize(x, out=out, fused_amax=True, **kw)
+                api.nvfp4_quantize(xs[j % n_sets], out=outs[j % n_sets], fused_amax=True, **kw)
                 if ev:
                     ev[2].record(stream)
             launches_per_step = 1
         else:
-            def step(ev=None):
+            def step(j, ev=None):
                 if ev:
                     ev[0].record(stream)
-                a_row, a_col = api.nvfp4_amax(x, rht_col=rht_amax, sign_mask=kw["sign_mask"])
+                xj = xs[j % n_sets]
+                a_row, a_col = api.nvfp4_amax(xj, rht_col=rht_amax, sign_mask=kw["sign_mask"])
                 if ev:
                     ev[1].record(stream)
-                api.nvfp4_quantize(x, amax_row=a_row, amax_col=a_col, out=out, **kw)
+                api.nvfp4_quantize(xj, amax_row=a_row, amax_col=a_col, out=outs[j % n_sets], **kw)
                 if ev:
                     ev[2].record(stream)
             launches_per_step = 2
@@ -402,9 +441,9 @@ def run_ours(args, world, rank, local):
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         time.sleep(0.3)  # the sampler is up before the GPU work starts
-        for _ in range(args.warmup):
-            flush.zero_()
-            step()
+        for j in range(args.warmup):
+            clear_l2(flush)
+            step(j)
         torch.cuda.synchronize(dev)
         status, bits = api.nvfp4_get_status(dev)
         if status != 0:
@@ -413,8 +452,8 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         clocks.mark_start()
         for i in range(args.steps):
-            flush.zero_()
-            step(events[i])
+            clear_l2(flush)
+            step(args.warmup + i, events[i])
         torch.cuda.synchronize(dev)
         clocks.mark_end()
         time.sleep(0.05)
@@ -485,7 +524,7 @@ def run_ours(args, world, rank, local):
                    "math": "fast (rcp.approx multipliers%s)" % (
                        ", FP32 RHT" if w.rht_col else "") if args.fast_math and not w.block2d
                            else "exact",
-                   "l2": "flushed before every timed step (256 MiB write)",
+                   "l2": l2_note,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": launches_per_step * args.steps,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -572,18 +611,21 @@ def run_mx(args, world, rank, local):
     x = inp["x"].to(dev)
     ideal = mx_ideal_bytes(w, fmt)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    out = api.alloc_mx_outputs(w.rows, w.cols, dev, fmt, w.rowwise, w.columnwise)
+    alloc = lambda: api.alloc_mx_outputs(w.rows, w.cols, dev, fmt, w.rowwise, w.columnwise)
+    out = alloc()
+    n_sets, flush, l2_note = l2_plan(args, dev, nbytes(x, *out.values()))
+    sets = [(x, out)] + [(x.clone(), alloc()) for _ in range(n_sets - 1)]
 
-    def step():
-        api.nvfp4_mx_quantize(x, fmt, w.rowwise, w.columnwise, out=out)
+    def step(j):
+        xj, oj = sets[j % n_sets]
+        api.nvfp4_mx_quantize(xj, fmt, w.rowwise, w.columnwise, out=oj)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         time.sleep(0.3)
-        for _ in range(args.warmup):
-            flush.zero_()
-            step()
+        for j in range(args.warmup):
+            clear_l2(flush)
+            step(j)
         torch.cuda.synchronize(dev)
         status, bits = api.nvfp4_get_status(dev)
         if status != 0:
@@ -592,9 +634,9 @@ def run_mx(args, world, rank, local):
         torch.cuda.synchronize(dev)
         clocks.mark_start()
         for i in range(args.steps):
-            flush.zero_()
+            clear_l2(flush)
             events[i][0].record(stream)
-            step()
+            step(args.warmup + i)
             events[i][1].record(stream)
         torch.cuda.synchronize(dev)
         clocks.mark_end()
@@ -640,7 +682,7 @@ def run_mx(args, world, rank, local):
         "config": {"workload": w.name, "shape": [w.rows, w.cols], "format": "MX" + fmt,
                    "rowwise": w.rowwise, "columnwise": w.columnwise,
                    "ideal_bytes_per_step": ideal, "pipeline": "one launch (no amax)",
-                   "l2": "flushed before every timed step (256 MiB write)",
+                   "l2": l2_note,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": args.steps,
         "e2e": {"value": ideal * e2e_steps * world / e2e_s / 1e9, "unit": "GB/s",
@@ -675,32 +717,36 @@ def run_producer(args, world, rank, local):
     x = inp["x"].to(dev)
     kw = quant_kwargs(w, inp)
     weight = torch.ones(w.cols, dtype=torch.bfloat16, device=dev)
-    out = api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise)
+    alloc = lambda: api.alloc_outputs(w.rows, w.cols, dev, w.rowwise, w.columnwise)
+    out = alloc()
     y = torch.empty_like(x)
     amax = torch.empty(1, dtype=torch.float32, device=dev)
     n = w.rows * w.cols
     # x read, y written and read back, plus the quantize outputs
     ideal = 2 * n + 2 * n + ideal_bytes(w)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_sets, flush, l2_note = l2_plan(args, dev, nbytes(x, y, *out.values()))
+    sets = [(x, y, out)] + [(x.clone(), torch.empty_like(x), alloc()) for _ in range(n_sets - 1)]
 
-    def fused():
-        api.nvfp4_rmsnorm_quantize(x, weight, eps=1e-6, out=out, y=y, amax=amax, **kw)
+    def fused(j):
+        xj, yj, oj = sets[j % n_sets]
+        api.nvfp4_rmsnorm_quantize(xj, weight, eps=1e-6, out=oj, y=yj, amax=amax, **kw)
 
-    def unfused():
-        api.nvfp4_rmsnorm_amax(x, weight, eps=1e-6, y=y, amax=amax)
-        api.nvfp4_quantize(y, out=out, fused_amax=True, **kw)
+    def unfused(j):
+        xj, yj, oj = sets[j % n_sets]
+        api.nvfp4_rmsnorm_amax(xj, weight, eps=1e-6, y=yj, amax=amax)
+        api.nvfp4_quantize(yj, out=oj, fused_amax=True, **kw)
 
     def timed(fn, steps):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-        for _ in range(args.warmup):
-            flush.zero_()
-            fn()
+        for j in range(args.warmup):
+            clear_l2(flush)
+            fn(j)
         torch.cuda.synchronize(dev)
         for i in range(steps):
-            flush.zero_()
+            clear_l2(flush)
             ev[i][0].record(stream)
-            fn()
+            fn(args.warmup + i)
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
         return [e[0].elapsed_time(e[1]) for e in ev]
@@ -728,7 +774,7 @@ def run_producer(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": w.name, "shape": [w.rows, w.cols], "ideal_bytes_per_step": ideal,
                    "pipeline": "nvfp4_rmsnorm_quantize: norm (amax in its epilogue) + quantize",
-                   "l2": "flushed before every timed step (256 MiB write)"},
+                   "l2": l2_note},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
         "step_us": {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
@@ -751,6 +797,9 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
+                   help="between timed steps: rotate input/output sets totalling >= 3x L2 "
+                        "(inputs larger than L2), or write a 256 MiB buffer before each step")
     p.add_argument("--pipeline", choices=["fused", "two_pass"], default="fused",
                    help="fused: amax and quantize in one launch; two_pass: amax kernel then "
                         "quantize kernel")

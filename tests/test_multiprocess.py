@@ -59,3 +59,12 @@ def test_aggregate_value_counts_every_rank():
     import bench
     # two ranks of the same ideal bytes over the slowest rank's time
     assert bench.aggregate_gbs(1e9, 10, 2, 2.0) == pytest.approx(10.0)
+
+
+def test_rotation_sets_cover_three_l2_capacities():
+    import bench
+    l2 = 126 << 20  # an L2 of 126 MiB
+    for set_bytes in (1, 335_872, 104_857_600 + 2_097_152, 183_500_800, 419_430_400, 3 * l2):
+        k = bench.rotation_sets(set_bytes, l2)
+        assert k * set_bytes >= 3 * l2 and (k == 1 or (k - 1) * set_bytes < 3 * l2)
+    assert bench.rotation_sets(419_430_400, l2) == 1      # inputs alone larger than L2
