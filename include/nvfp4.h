@@ -26,8 +26,10 @@
  * void*; NULL is the legacy default stream). Pointers marked (device) must be device (or
  * managed) memory, 16-byte aligned. The return value reports argument checks and launch
  * errors only; problems the device detects (bad grouped offsets, a bounded wait that gave up)
- * are recorded in a per-device status word read by nvfp4_get_status. A call that returns an
- * error status launched nothing and wrote nothing.
+ * are recorded in a per-device status word read by nvfp4_get_status. A call rejected by its
+ * argument checks launched nothing and wrote nothing. NVFP4_ERR_CUDA reports a CUDA call or
+ * launch that failed (the runtime's last-error state is cleared; a sticky error stays); kernels
+ * of the call launched before it may have run, so its outputs are undefined.
  *
  * Memory: the library allocates no memory on these calls except once per device, on the
  * first call that needs it: a small workspace (status word, the single-launch amax's counts,
@@ -333,6 +335,13 @@ nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status);
  * that one call (0 clears it). Not for production use.
  * Errors: NVFP4_ERR_INVALID_ARG (extra outside 0 .. 1024). */
 nvfp4_status nvfp4_debug_fused_extra_arrivals(int32_t extra);
+
+/* Test hook for launch failures: with on = 1, the next nvfp4_quantize or nvfp4_quantize_grouped
+ * call (on any device) launches its quantize kernel with an empty grid, which the runtime
+ * rejects before anything reaches the GPU; the call returns NVFP4_ERR_CUDA and the next call
+ * runs normally. on = 0 clears it. Not for production use.
+ * Errors: NVFP4_ERR_INVALID_ARG (on not 0 or 1). */
+nvfp4_status nvfp4_debug_fail_next_launch(int32_t on);
 
 /* Host pipeline: quantization of tensors that live in host memory, with the copies of
  * consecutive submissions overlapped (the input of one on the host-to-device link while the

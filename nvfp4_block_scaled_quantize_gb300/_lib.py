@@ -25,7 +25,8 @@ EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quanti
             "nvfp4_host_pipeline_join", "nvfp4_host_pipeline_destroy", "nvfp4_swizzle_scales",
             "nvfp4_mx_quantize", "nvfp4_mx_dequantize", "nvfp4_dequantize_ex",
             "nvfp4_rmsnorm_amax", "nvfp4_rmsnorm_quantize", "nvfp4_set_workspace",
-            "nvfp4_amax_grouped", "nvfp4_debug_fused_extra_arrivals"]
+            "nvfp4_amax_grouped", "nvfp4_debug_fused_extra_arrivals",
+            "nvfp4_debug_fail_next_launch"]
 
 
 class Config(ctypes.Structure):
@@ -116,5 +117,7 @@ def load(build_if_missing: bool = False):
     L.nvfp4_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.nvfp4_debug_fused_extra_arrivals.restype = ctypes.c_int
     L.nvfp4_debug_fused_extra_arrivals.argtypes = [i32]
+    L.nvfp4_debug_fail_next_launch.restype = ctypes.c_int
+    L.nvfp4_debug_fail_next_launch.argtypes = [i32]
     _lib = L
     return L

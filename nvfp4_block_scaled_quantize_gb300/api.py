@@ -314,6 +314,13 @@ def nvfp4_debug_fused_extra_arrivals(extra):
               "nvfp4_debug_fused_extra_arrivals")
 
 
+def nvfp4_debug_fail_next_launch(on=True):
+    """Test hook: the next quantize call launches an empty grid, which the runtime rejects, so
+    the call raises NVFP4Error(NVFP4_ERR_CUDA); the call after it runs normally."""
+    _raise_if(_lib.load().nvfp4_debug_fail_next_launch(int(bool(on))),
+              "nvfp4_debug_fail_next_launch")
+
+
 def quantize_from_host(x_host, pinned_out=None, **kw):
     """End-to-end call for host data: copy a pinned host BF16 tensor to the device, quantize,
     and copy every output back into pinned host tensors (all on the current stream)."""

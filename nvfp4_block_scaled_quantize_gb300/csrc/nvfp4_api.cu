@@ -35,6 +35,10 @@ std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 // Arrivals the next single-launch amax awaits beyond its grid (nvfp4_debug_fused_extra_arrivals)
 std::atomic<int32_t> g_fuse_extra{0};
+// Set: the next quantize call launches an empty grid, which the runtime rejects
+// (nvfp4_debug_fail_next_launch)
+std::atomic<int32_t> g_fail_next{0};
+int launch_grid(int grid) { return g_fail_next.exchange(0) ? 0 : grid; }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -142,7 +146,14 @@ cudaError_t prepare_quantize_kernels() {
 
 namespace {
 
-nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+// A failed launch or call is reported as NVFP4_ERR_CUDA; the runtime's last-error state is
+// cleared so that the caller's next, unrelated error check does not see it (a sticky error
+// stays sticky).
+nvfp4_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return NVFP4_OK;
+  (void)cudaGetLastError();
+  return NVFP4_ERR_CUDA;
+}
 
 // One wave of the flat amax kernel (four 256-thread CTAs per SM), fewer for small tensors.
 int amax_flat_grid(const DeviceState* st, int64_t nvec) {
@@ -328,7 +339,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   // the barrier's counts and epoch live on the device (CTA 0 readies them for the next launch),
   // so the launch depends on no host state and can be captured in a CUDA graph
   if (fused) q.fuse_extra = g_fuse_extra.exchange(0);
-  return cuda_status(launch_quantize(mode, q, grid, s));
+  return cuda_status(launch_quantize(mode, q, launch_grid(grid), s));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
@@ -393,7 +404,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};
   const int64_t tiles = ((T + kTileM - 1) / kTileM + E) * ((H + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
-  return cuda_status(launch_quantize(mode, q, grid, s));
+  return cuda_status(launch_quantize(mode, q, launch_grid(grid), s));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales,
@@ -602,6 +613,12 @@ NVFP4_EXPORT nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes) {
 NVFP4_EXPORT nvfp4_status nvfp4_debug_fused_extra_arrivals(int32_t extra) {
   if (extra < 0 || extra > kFuseMaxCtas) return NVFP4_ERR_INVALID_ARG;
   g_fuse_extra.store(extra);
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_debug_fail_next_launch(int32_t on) {
+  if (on != 0 && on != 1) return NVFP4_ERR_INVALID_ARG;
+  g_fail_next.store(on);
   return NVFP4_OK;
 }
 

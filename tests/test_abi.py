@@ -193,3 +193,5 @@ def test_debug_hook_argument_checks(L):
     assert L.nvfp4_debug_fused_extra_arrivals(-1) == 1
     assert L.nvfp4_debug_fused_extra_arrivals(1025) == 1
     assert L.nvfp4_debug_fused_extra_arrivals(0) == 0  # clears it: no call consumes it here
+    assert L.nvfp4_debug_fail_next_launch(2) == 1 and L.nvfp4_debug_fail_next_launch(-1) == 1
+    assert L.nvfp4_debug_fail_next_launch(0) == 0

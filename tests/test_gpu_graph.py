@@ -7,7 +7,10 @@ at capture) would show up as a wrong global scale.
 
 The timeout test asks the next single-launch call to wait for one CTA more than its grid has:
 every CTA gives up after its bounded wait, records NVFP4_DEVICE_TIMEOUT and exits, and the call
-after it runs normally on the same workspace. Nothing faults or hangs: the wait has a limit."""
+after it runs normally on the same workspace. Nothing faults or hangs: the wait has a limit.
+The launch-failure test has the next call launch an empty grid, which the runtime rejects
+before anything reaches the GPU: the call reports NVFP4_ERR_CUDA, leaves no error behind for
+the next CUDA call, and the call after it is correct."""
 import ctypes
 
 import numpy as np
@@ -143,4 +146,27 @@ def test_barrier_wait_runs_out_then_next_call_is_correct(shape):
     out = api.nvfp4_quantize(x.to(dev), **cfg)
     torch.cuda.synchronize()
     _same(out, oracle.quantize(x, _oracle_cfg(cfg)), "after timeout")
+    assert api.nvfp4_get_status(dev) == (0, 0)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_pass"])
+def test_failed_launch_is_reported_and_leaves_no_error_behind(fused):
+    dev = _cuda()
+    M, N = 256, 512
+    x = workloads.normal_with_outliers(M, N, seed=3, fraction=0.01, gain=30.0)
+    cfg = dict(rowwise=True, columnwise=True, fused_amax=fused)
+    xd = x.to(dev)
+    api.nvfp4_quantize(xd, **cfg)
+    torch.cuda.synchronize()
+    api.nvfp4_debug_fail_next_launch()
+    with pytest.raises(_lib.NVFP4Error) as e:
+        api.nvfp4_quantize(xd, **cfg)
+    assert "NVFP4_ERR_CUDA" in str(e.value)
+    # torch's next launch and error check see no leftover error
+    y = (xd.float() * 2).sum()
+    torch.cuda.synchronize()
+    assert torch.isfinite(y)
+    out = api.nvfp4_quantize(xd, **cfg)
+    torch.cuda.synchronize()
+    _same(out, oracle.quantize(x, _oracle_cfg(cfg)), "after a failed launch")
     assert api.nvfp4_get_status(dev) == (0, 0)
