@@ -388,6 +388,33 @@ def test_fused_amax_repeated_calls_reuse_the_barrier():
     assert status == 0 and bits == 0
 
 
+# Single launch, rowwise + columnwise RTNE on shapes that mix whole 64 x 256 tiles with ragged
+# row and column tiles, N a multiple of 64 or not.
+FUSED_ROWCOL_SHAPES = [(64, 256), (128, 512), (304, 1088), (576, 2304), (1024, 4096), (320, 1040)]
+
+
+@pytest.mark.parametrize("shape", FUSED_ROWCOL_SHAPES, ids=lambda s: "%dx%d" % s)
+def test_fused_rowcol_whole_and_ragged_tiles_match_oracle(shape):
+    M, N = shape
+    # a second call on other data into reused memory
+    for k, gain in enumerate((40.0, 3.0)):
+        x = workloads.normal_with_outliers(M, N, seed=M + N + k, fraction=0.01, gain=gain)
+        out, ref = run_both(x, rowwise=True, columnwise=True, fused_amax=True)
+        assert_same(out, ref, "fused rowcol %s call %d" % (shape, k))
+
+
+def test_fused_rowcol_special_tiles():
+    # whole tiles that are all zero, all negative, or hold one large negative value
+    M, N = 192, 768
+    x = workloads.normal_with_outliers(M, N, seed=5, fraction=0.01, gain=20.0).float()
+    x[0:64, 0:256] = 0.0
+    x[64:128, 256:512] = -x[64:128, 256:512].abs() - 1e-3
+    x[128:192, 512:768] = 0.0
+    x[150, 600] = -3.0e4
+    out, ref = run_both(x.to(torch.bfloat16), rowwise=True, columnwise=True, fused_amax=True)
+    assert_same(out, ref, "fused rowcol special tiles")
+
+
 @pytest.mark.parametrize("name", [n for n, w in workloads.WORKLOADS.items() if not w.grouped])
 def test_full_size_workload_fused_matches_oracle(name):
     w = workloads.WORKLOADS[name]
