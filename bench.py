@@ -322,7 +322,9 @@ def run_reference(args, world, rank):
     w = workloads.WORKLOADS[args.workload]
     inp = workloads.make_input(w)
     cores = 1 if w.grouped else host_cores()
-    budget = min(10.0, 150.0 / (args.steps + args.warmup))  # seconds per step
+    # seconds per step: about 100 s of oracle work for the whole run (small samples scale
+    # worse than linearly over the threads, so the run takes somewhat longer)
+    budget = min(10.0, 100.0 / (args.steps + args.warmup))
     rows = cpu_sample_rows(w, inp, budget * cores)
     off = np.minimum(inp["offsets"], rows) if w.grouped else None
     b = ideal_bytes(w, rows, off)
@@ -792,7 +794,7 @@ def run_producer(args, world, rank, local):
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
