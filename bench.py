@@ -8,7 +8,8 @@ Ideal bytes per step = one BF16 read + code writes + scale writes (the metric's 
 bytes). Between timed steps L2 holds none of the step's data: by default (--l2 rotate) the steps
 cycle through K input/output sets whose total is at least three times the L2 size (inputs
 larger than L2), with --l2 flush a 256 MiB buffer is written before every step. Device time
-comes from CUDA events on the launching stream. Prints ONE JSON line (rank 0).
+comes from CUDA events on the launching stream: one pair around the K back-to-back steps (with
+the flush, a pair around every step). Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--pipeline fused|two_pass] [--l2 rotate|flush]
@@ -440,7 +441,14 @@ def run_ours(args, world, rank, local):
             launches_per_step = 2
         kernel_split = True
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # With rotating sets the K timed steps run back to back between one pair of events (events
+    # between launches would serialize them). A second pass with events around every step
+    # gives the per-step spread and, for two passes, the quantize kernel alone; with the flush
+    # the timed region itself uses per-step events, so that the flush writes stay outside.
+    per_step_timed = args.l2 == "flush"
+    n_ev = args.steps if per_step_timed else min(args.steps, 1000)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         time.sleep(0.3)  # the sampler is up before the GPU work starts
         for j in range(args.warmup):
@@ -453,18 +461,31 @@ def run_ours(args, world, rank, local):
         barrier(world)
         torch.cuda.synchronize(dev)
         clocks.mark_start()
-        for i in range(args.steps):
-            clear_l2(flush)
-            step(args.warmup + i, events[i])
+        if per_step_timed:
+            for i in range(args.steps):
+                clear_l2(flush)
+                step(args.warmup + i, events[i])
+        else:
+            t_start.record(stream)
+            for i in range(args.steps):
+                step(args.warmup + i)
+            t_end.record(stream)
         torch.cuda.synchronize(dev)
         clocks.mark_end()
         time.sleep(0.05)
     barrier(world)
+    if not per_step_timed:
+        for i in range(n_ev):
+            step(args.warmup + args.steps + i, events[i])
+        torch.cuda.synchronize(dev)
+    status, bits = api.nvfp4_get_status(dev)
+    if status != 0:
+        raise RuntimeError("device status %d (bits %#x) after the timed steps" % (status, bits))
     step_ms = [e[0].elapsed_time(e[2]) for e in events]
     if kernel_split:
         quant_ms = ([e[0].elapsed_time(e[2]) for e in events] if args.pipeline == "fused"
                     else [e[1].elapsed_time(e[2]) for e in events])
-    total_s = sum(step_ms) / 1e3
+    total_s = (sum(step_ms) if per_step_timed else t_start.elapsed_time(t_end)) / 1e3
     total_s = max_over_ranks(world, total_s)
     value = aggregate_gbs(ideal, args.steps, world, total_s)
 
@@ -536,9 +557,15 @@ def run_ours(args, world, rank, local):
         "clocks": clocks.summary(),
     }
     line["step_us"] = {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,
-                       "max": max(step_ms) * 1e3}
+                       "max": max(step_ms) * 1e3,
+                       "from": ("the timed steps" if per_step_timed else
+                                "%d further steps with events around each (events between "
+                                "launches serialize them)" % n_ev)}
     if kernel_split:
-        qk = statistics.mean(quant_ms) / 1e3
+        # the single launch is the step, so its duration is the timed region's per-step time;
+        # the two-pass pipeline's quantize kernel is timed alone by the events around it
+        qk = (total_s / args.steps if args.pipeline == "fused" and not per_step_timed
+              else statistics.mean(quant_ms) / 1e3)
         achieved = ideal / qk / 1e9
         line["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                             "frac": achieved / hbm, "peak_kind": peak_kind,
@@ -622,7 +649,12 @@ def run_mx(args, world, rank, local):
         xj, oj = sets[j % n_sets]
         api.nvfp4_mx_quantize(xj, fmt, w.rowwise, w.columnwise, out=oj)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    # timed as in run_ours: back to back between one event pair with rotating sets, per-step
+    # events (a separate pass) for the spread; per-step events in the timed region with the flush
+    per_step_timed = args.l2 == "flush"
+    n_ev = args.steps if per_step_timed else min(args.steps, 1000)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_ev)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         time.sleep(0.3)
         for j in range(args.warmup):
@@ -635,17 +667,30 @@ def run_mx(args, world, rank, local):
         barrier(world)
         torch.cuda.synchronize(dev)
         clocks.mark_start()
-        for i in range(args.steps):
-            clear_l2(flush)
-            events[i][0].record(stream)
-            step(args.warmup + i)
-            events[i][1].record(stream)
+        if per_step_timed:
+            for i in range(args.steps):
+                clear_l2(flush)
+                events[i][0].record(stream)
+                step(args.warmup + i)
+                events[i][1].record(stream)
+        else:
+            t_start.record(stream)
+            for i in range(args.steps):
+                step(args.warmup + i)
+            t_end.record(stream)
         torch.cuda.synchronize(dev)
         clocks.mark_end()
         time.sleep(0.05)
     barrier(world)
+    if not per_step_timed:
+        for i in range(n_ev):
+            events[i][0].record(stream)
+            step(args.warmup + args.steps + i)
+            events[i][1].record(stream)
+        torch.cuda.synchronize(dev)
     step_ms = [e[0].elapsed_time(e[1]) for e in events]
-    total_s = max_over_ranks(world, sum(step_ms) / 1e3)
+    total_s = max_over_ranks(world, (sum(step_ms) if per_step_timed
+                                     else t_start.elapsed_time(t_end)) / 1e3)
     value = aggregate_gbs(ideal, args.steps, world, total_s)
 
     # end to end: pinned host input -> device -> quantize -> pinned host outputs, one stream
@@ -673,7 +718,7 @@ def run_mx(args, world, rank, local):
     if rank != 0:
         return
     hbm, peak_kind = peaks()
-    kus = statistics.mean(step_ms) * 1e3
+    kus = total_s * 1e6 / args.steps  # one launch per step
     achieved = ideal / (kus / 1e6) / 1e9
     line = {
         "metric": MX_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -740,18 +785,28 @@ def run_producer(args, world, rank, local):
         api.nvfp4_quantize(yj, out=oj, fused_amax=True, **kw)
 
     def timed(fn, steps):
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        """Per-step times in ms: per-step events with the flush; otherwise the steps run back
+        to back between one event pair and every step gets the mean."""
         for j in range(args.warmup):
             clear_l2(flush)
             fn(j)
         torch.cuda.synchronize(dev)
+        if args.l2 == "flush":
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+            for i in range(steps):
+                clear_l2(flush)
+                ev[i][0].record(stream)
+                fn(args.warmup + i)
+                ev[i][1].record(stream)
+            torch.cuda.synchronize(dev)
+            return [e[0].elapsed_time(e[1]) for e in ev]
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
         for i in range(steps):
-            clear_l2(flush)
-            ev[i][0].record(stream)
             fn(args.warmup + i)
-            ev[i][1].record(stream)
+        a1.record(stream)
         torch.cuda.synchronize(dev)
-        return [e[0].elapsed_time(e[1]) for e in ev]
+        return [a0.elapsed_time(a1) / steps] * steps
 
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         time.sleep(0.3)

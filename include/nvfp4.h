@@ -88,15 +88,26 @@ typedef struct nvfp4_config {
   uint32_t rng_offset;    /* Philox counter word 3 (advance it to draw a new stream) */
   uint64_t rng_seed;      /* Philox key = (low 32 bits, high 32 bits) */
   int32_t fused_amax;     /* when the amax inputs are NULL: 0 = amax pass + quantize pass,
-                             1 = one cooperative launch: every CTA reduces the tiles it will
+                             1 = one launch: every CTA (one per SM) reduces the tiles it will
                              quantize, folds its maxima into the workspace with an atomic max,
                              counts its arrival and waits (bounded) for all CTAs, then
                              quantizes (the re-read of x comes from L2 when x fits there).
+                             All CTAs must be resident at once: a device's calls are
+                             cooperative launches (which check that) until one with a CTA on
+                             every SM has succeeded; later ones use programmatic dependent
+                             launch, so that a call may start on the SMs the previous
+                             single-launch call leaves. Such a launch waits for the previous
+                             kernel in the stream before it reads anything. A kernel launched
+                             after it with programmatic dependent launch may start before it
+                             ends and must wait for it before reading its outputs. On a device
+                             that cannot hold one CTA per SM for this call (e.g. a reduced
+                             MPS share), the wait gives up after about 2 s and reports
+                             NVFP4_DEVICE_TIMEOUT: use 0 there.
                              Fused calls share the device workspace's counts, maxima and epoch
                              (kept on the device: once every CTA has arrived, CTA 0 readies
                              the count for the next launch and advances the epoch, so
-                             captured calls replay correctly): on one
-                             device they must not overlap in time (issue them on one stream).
+                             captured calls replay correctly): on one device they must not
+                             overlap in time (issue them on one stream).
                              Plain tensors only. */
   int32_t fast_math;      /* 0 = exact (default). 1 = the fast variant of [PR4798] "Fast math":
                              the element multiplier is rcp.approx.ftz(float(s) * S_dec) instead

@@ -29,6 +29,9 @@ struct DeviceState {
   int sm_count = 0;
   uint32_t* workspace = nullptr;  // [0] status word; the library's own or the caller's
   uint32_t* own = nullptr;        // the library's own workspace, allocated on first need
+  // a cooperative single-launch call with one CTA per SM has succeeded on this device, so
+  // later ones may use programmatic dependent launch (quantize_kernel.cuh, launch)
+  std::atomic<bool> full_grid_checked{false};
 };
 
 std::mutex g_mutex;
@@ -338,8 +341,14 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};
   // the barrier's counts and epoch live on the device (CTA 0 readies them for the next launch),
   // so the launch depends on no host state and can be captured in a CUDA graph
-  if (fused) q.fuse_extra = g_fuse_extra.exchange(0);
-  return cuda_status(launch_quantize(mode, q, launch_grid(grid), s));
+  if (fused) {
+    q.fuse_extra = g_fuse_extra.exchange(0);
+    q.coop_launch = ds->full_grid_checked.load() ? 0 : 1;
+  }
+  const cudaError_t e = launch_quantize(mode, q, launch_grid(grid), s);
+  if (e == cudaSuccess && fused && q.coop_launch && grid == ds->sm_count)
+    ds->full_grid_checked.store(true);
+  return cuda_status(e);
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,

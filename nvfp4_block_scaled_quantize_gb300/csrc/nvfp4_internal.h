@@ -76,6 +76,8 @@ struct QuantArgs {
   int32_t fuse_extra;               // arrivals awaited beyond the grid's: 0 (> 0 only to make
                                     // the barrier time out on purpose, in tests)
   uint32_t* fuse_ws;                // kFuseWsWords words, 8-byte aligned (fused_amax.cuh)
+  int32_t coop_launch;              // host side: 1 = cooperative launch (checks co-residency),
+                                    // 0 = programmatic dependent launch (fused only)
 };
 
 // Round keys of Philox4x32-10 for a 64-bit seed: key (lo32, hi32) bumped by the Weyl constants

@@ -163,6 +163,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
+  // The single-launch kernel may be launched before the previous kernel in the stream has
+  // finished (programmatic dependent launch): wait for it before touching any memory, since
+  // that kernel may have produced x or still use the workspace and the outputs.
+  if (FUSED) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   int32_t* seg_start = reinterpret_cast<int32_t*>(smem + kSmemSegStart);
   int32_t* seg_end = reinterpret_cast<int32_t*>(smem + kSmemSegEnd);
@@ -365,6 +369,9 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
       }
       if (blockIdx.x == 0) fuse_advance(a.fuse_ws, fuse_e);
+      // past the barrier this CTA no longer uses the workspace: the next kernel in the
+      // stream may start on the SMs that finished CTAs leave
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       fused_amax[0] = __uint_as_float(pr << 16);
       fused_amax[1] = __uint_as_float(pc << 16);
     }
@@ -798,15 +805,25 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
 cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
-  if (args.fused) {  // every CTA waits for all the others: a cooperative launch
+  if (args.fused) {
+    // Every CTA waits for all the others, so all must be resident at once (one per SM). A
+    // cooperative launch checks that; the host uses it for a device's first single-launch
+    // call. Later calls use programmatic dependent launch instead (the two do not combine):
+    // their CTAs may start on SMs that the previous single-launch kernel's CTAs leave, and
+    // wait for that kernel at entry.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kQuantThreads);
     cfg.dynamicSmemBytes = kQuantSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    if (args.coop_launch) {
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+    } else {
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(

@@ -170,3 +170,31 @@ def test_failed_launch_is_reported_and_leaves_no_error_behind(fused):
     torch.cuda.synchronize()
     _same(out, oracle.quantize(x, _oracle_cfg(cfg)), "after a failed launch")
     assert api.nvfp4_get_status(dev) == (0, 0)
+
+
+GAINS6 = (50.0, 2.0, 30.0, 7.0, 90.0, 1.0)
+
+
+@pytest.mark.parametrize("mode", ["fused_rowcol", "fused_rht_sr"])
+def test_back_to_back_single_launch_calls(mode):
+    """Single-launch calls queued with no synchronization in between: after the first one,
+    each may start on SMs the previous one leaves (programmatic dependent launch) and waits for
+    it at entry. A full grid (one CTA per SM); every call's outputs match the oracle, into
+    separate buffers and into one buffer reused by all (the last call's outputs remain)."""
+    dev = _cuda()
+    M, N = 2048, 4096
+    cfg = MODES[mode]
+    xs_cpu = [workloads.normal_with_outliers(M, N, seed=300 + k, fraction=0.01, gain=g)
+              for k, g in enumerate(GAINS6)]
+    xs = [x.to(dev) for x in xs_cpu]
+    torch.cuda.synchronize()
+    outs = [api.nvfp4_quantize(x, **cfg) for x in xs]
+    shared = api.alloc_outputs(M, N, dev, True, True)
+    for x in xs:
+        api.nvfp4_quantize(x, out=shared, **cfg)
+    torch.cuda.synchronize()
+    refs = [oracle.quantize(x, _oracle_cfg(cfg)) for x in xs_cpu]
+    for k, (o, r) in enumerate(zip(outs, refs)):
+        _same(o, r, "%s call %d" % (mode, k))
+    _same(shared, refs[-1], "%s reused outputs" % mode)
+    assert api.nvfp4_get_status(dev) == (0, 0)
