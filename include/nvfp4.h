@@ -23,7 +23,11 @@
  * rowwise outputs of x transposed, optionally after a 16-point random Hadamard transform.
  *
  * Execution: every call is asynchronous on the caller's stream (a cudaStream_t passed as
- * void*; NULL is the legacy default stream). Pointers marked (device) must be device (or
+ * void*; NULL is the legacy default stream). The quantize, amax and MX kernels are launched
+ * with programmatic dependent launch: each waits for the previous kernel in the stream before
+ * it touches memory, and lets the next kernel launched that way start early, so a kernel of
+ * the caller's launched after them with programmatic dependent launch must wait
+ * (cudaGridDependencySynchronize) before it reads their outputs, as that mechanism requires. Pointers marked (device) must be device (or
  * managed) memory, 16-byte aligned. The return value reports argument checks and launch
  * errors only; problems the device detects (bad grouped offsets, a bounded wait that gave up)
  * are recorded in a per-device status word read by nvfp4_get_status. A call rejected by its
@@ -93,9 +97,9 @@ typedef struct nvfp4_config {
                              counts its arrival and waits (bounded) for all CTAs, then
                              quantizes (the re-read of x comes from L2 when x fits there).
                              All CTAs must be resident at once: a device's calls are
-                             cooperative launches (which check that) until one with a CTA on
-                             every SM has succeeded; later ones use programmatic dependent
-                             launch, so that a call may start on the SMs the previous
+                             cooperative launches (which check that) until one with at least
+                             as large a grid has succeeded; later ones use programmatic
+                             dependent launch, so that a call may start on the SMs the previous
                              single-launch call leaves. Such a launch waits for the previous
                              kernel in the stream before it reads anything. A kernel launched
                              after it with programmatic dependent launch may start before it

@@ -48,6 +48,8 @@ __device__ __forceinline__ void block_max_out(uint32_t v, float* out0, float* ou
 constexpr int kFlatUnroll = 8;
 __global__ void __launch_bounds__(256, 4) amax_flat_kernel(const uint4* __restrict__ x, int64_t nvec,
                                                            float* out0, float* out1) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel may produce x
+  pdl_allow_next();
   uint32_t m = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
@@ -172,8 +174,8 @@ cudaError_t launch_swizzle_scales(const uint8_t* scales, int64_t R, int64_t C, u
 
 cudaError_t launch_amax_flat(const void* x, int64_t n_elems, float* out0, float* out1, int grid,
                              cudaStream_t s) {
-  amax_flat_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), n_elems / 8, out0, out1);
-  return cudaGetLastError();
+  return launch_pdl(amax_flat_kernel, dim3(grid), dim3(256), 0, s,
+                    reinterpret_cast<const uint4*>(x), n_elems / 8, out0, out1);
 }
 
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, const float* gscale,

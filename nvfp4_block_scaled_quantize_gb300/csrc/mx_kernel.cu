@@ -148,6 +148,8 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 template <int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(32 * kMxWarps, 1) mx_quantize_kernel(const __grid_constant__ MxArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel may produce x
+  pdl_allow_next();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   // the 128-byte swizzle is a function of the shared address bits 7..9: every box and staging
@@ -419,8 +421,8 @@ __global__ void __launch_bounds__(32 * kMxWarps, 1) mx_quantize_kernel(const __g
 
 template <int FMT, bool ROW, bool COL>
 cudaError_t launch_t(const MxArgs& args, int grid, cudaStream_t s) {
-  mx_quantize_kernel<FMT, ROW, COL><<<grid, 32 * kMxWarps, kMxSmemBytes, s>>>(args);
-  return cudaGetLastError();
+  return launch_pdl(mx_quantize_kernel<FMT, ROW, COL>, dim3(grid), dim3(32 * kMxWarps),
+                    kMxSmemBytes, s, args);
 }
 
 template <int FMT, bool ROW, bool COL>

@@ -29,9 +29,10 @@ struct DeviceState {
   int sm_count = 0;
   uint32_t* workspace = nullptr;  // [0] status word; the library's own or the caller's
   uint32_t* own = nullptr;        // the library's own workspace, allocated on first need
-  // a cooperative single-launch call with one CTA per SM has succeeded on this device, so
-  // later ones may use programmatic dependent launch (quantize_kernel.cuh, launch)
-  std::atomic<bool> full_grid_checked{false};
+  // the largest grid of a cooperative single-launch call that has succeeded on this device:
+  // calls with a grid no larger are known to fit at once and use programmatic dependent
+  // launch instead (quantize_kernel.cuh, launch)
+  std::atomic<int> coop_checked_grid{0};
 };
 
 std::mutex g_mutex;
@@ -152,6 +153,13 @@ namespace {
 // A failed launch or call is reported as NVFP4_ERR_CUDA; the runtime's last-error state is
 // cleared so that the caller's next, unrelated error check does not see it (a sticky error
 // stays sticky).
+// Raise the largest cooperatively checked grid to g (concurrent callers may race: keep the max).
+void note_checked_grid(std::atomic<int>& checked, int g) {
+  int cur = checked.load();
+  while (cur < g && !checked.compare_exchange_weak(cur, g)) {
+  }
+}
+
 nvfp4_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return NVFP4_OK;
   (void)cudaGetLastError();
@@ -343,11 +351,10 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   // so the launch depends on no host state and can be captured in a CUDA graph
   if (fused) {
     q.fuse_extra = g_fuse_extra.exchange(0);
-    q.coop_launch = ds->full_grid_checked.load() ? 0 : 1;
+    q.coop_launch = grid > ds->coop_checked_grid.load() ? 1 : 0;
   }
   const cudaError_t e = launch_quantize(mode, q, launch_grid(grid), s);
-  if (e == cudaSuccess && fused && q.coop_launch && grid == ds->sm_count)
-    ds->full_grid_checked.store(true);
+  if (e == cudaSuccess && fused && q.coop_launch) note_checked_grid(ds->coop_checked_grid, grid);
   return cuda_status(e);
 }
 

@@ -356,6 +356,14 @@ __device__ __forceinline__ void rht16_pair(uint32_t (&w)[16], uint32_t sign_mask
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// Programmatic dependent launch. A kernel launched with launch_pdl (nvfp4_internal.h) may
+// start before the previous kernel in its stream has ended: it calls pdl_wait() before it
+// touches memory, and pdl_allow_next() lets the next such kernel start on SMs that finish.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One 32-byte global store (a full sector); p must be 32-byte aligned.
 __device__ __forceinline__ void stg256(void* p, const uint4& lo, const uint4& hi) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(lo.x),

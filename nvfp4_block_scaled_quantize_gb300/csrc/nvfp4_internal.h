@@ -80,6 +80,24 @@ struct QuantArgs {
                                     // 0 = programmatic dependent launch (fused only)
 };
 
+// Launch with programmatic dependent launch: the kernel may start before the previous kernel
+// in the stream ends, so it must call pdl_wait() (nvfp4_device.cuh) before any memory access.
+template <typename... KernelArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KernelArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Round keys of Philox4x32-10 for a 64-bit seed: key (lo32, hi32) bumped by the Weyl constants
 // 0x9E3779B9 and 0xBB67AE85 each round. Computed once per launch on the host, so that the
 // kernels read them from their parameters instead of recomputing the schedule per draw.

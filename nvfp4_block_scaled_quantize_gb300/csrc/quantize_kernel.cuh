@@ -163,10 +163,13 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  // The single-launch kernel may be launched before the previous kernel in the stream has
-  // finished (programmatic dependent launch): wait for it before touching any memory, since
-  // that kernel may have produced x or still use the workspace and the outputs.
-  if (FUSED) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Launched with programmatic dependent launch, the kernel may start before the previous
+  // kernel in the stream has finished: wait for it before touching any memory, since that
+  // kernel may have produced x or still use the workspace and the outputs. The next kernel
+  // may start at once (it waits for this one in turn), except after a single-launch kernel,
+  // which lets it start only once past its grid barrier (below).
+  pdl_wait();
+  if (!FUSED) pdl_allow_next();
 
   int32_t* seg_start = reinterpret_cast<int32_t*>(smem + kSmemSegStart);
   int32_t* seg_end = reinterpret_cast<int32_t*>(smem + kSmemSegEnd);
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       if (blockIdx.x == 0) fuse_advance(a.fuse_ws, fuse_e);
       // past the barrier this CTA no longer uses the workspace: the next kernel in the
       // stream may start on the SMs that finished CTAs leave
-      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      pdl_allow_next();
       fused_amax[0] = __uint_as_float(pr << 16);
       fused_amax[1] = __uint_as_float(pc << 16);
     }
@@ -830,17 +833,15 @@ cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
         &cfg, quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT>,
         args);
   }
-  quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT>
-      <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
-  return cudaGetLastError();
+  return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT>,
+                    dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
 }
 
 // The amax pass (AMAX_ONLY) of a plain or grouped tensor.
 template <bool RHT>
 cudaError_t launch_amax_pass(const QuantArgs& args, int grid, cudaStream_t s) {
-  quantize_tiles_kernel<true, false, RHT, false, false, false, false, true>
-      <<<grid, kQuantThreads, kQuantSmemBytes, s>>>(args);
-  return cudaGetLastError();
+  return launch_pdl(quantize_tiles_kernel<true, false, RHT, false, false, false, false, true>,
+                    dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
 }
 template <bool RHT>
 cudaError_t prepare_amax_pass() {

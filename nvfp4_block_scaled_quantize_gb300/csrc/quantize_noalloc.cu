@@ -36,9 +36,9 @@ struct NoAllocDevice {
   bool ready = false;
   int sm_count = 0;
   uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-  // a cooperative launch with one CTA per SM has succeeded here: later launches may use
-  // programmatic dependent launch (quantize_kernel.cuh, launch)
-  std::atomic<bool> full_grid_checked{false};
+  // the largest grid of a cooperative launch that has succeeded here: launches with a grid
+  // no larger use programmatic dependent launch (quantize_kernel.cuh, launch)
+  std::atomic<int> coop_checked_grid{0};
 };
 
 std::mutex g_mutex;
@@ -150,11 +150,15 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   // the next launch), so nothing is cleared before the launch and it can be captured in a graph
   const QuantMode mode{row, col, rht, two_d, cfg->round_row == NVFP4_ROUND_SR,
                        cfg->round_col == NVFP4_ROUND_SR, q.fast && rht};
-  q.coop_launch = d->full_grid_checked.load() ? 0 : 1;
+  q.coop_launch = grid > d->coop_checked_grid.load() ? 1 : 0;
   if (launch_quantize(mode, q, grid, s) != cudaSuccess) {
     (void)cudaGetLastError();  // leave no error behind for the caller's next check
     return NVFP4_ERR_CUDA;
   }
-  if (q.coop_launch && grid == d->sm_count) d->full_grid_checked.store(true);
+  if (q.coop_launch) {
+    int cur = d->coop_checked_grid.load();
+    while (cur < grid && !d->coop_checked_grid.compare_exchange_weak(cur, grid)) {
+    }
+  }
   return NVFP4_OK;
 }
