@@ -36,10 +36,12 @@ __device__ __forceinline__ uint32_t cta_max(uint32_t v, volatile uint32_t* red) 
 // stay below 2^48 for longer than any process runs). A launch reads the epoch E when it starts,
 // counts its arrivals on word E & 1 and tags its maxima with E + 1; once CTA 0 has seen every
 // arrival (or given up) it zeroes the other count, which the next launch uses, and stores
-// E + 1. Every CTA has read E before it arrives, and the next launch starts only when this one
-// has ended, so plain stores suffice and no launch depends on host-side state: launches can be
+// E + 1. Every CTA has read E before it arrives, and the next launch on the stream reads the
+// words only once this one has ended (even when it starts early, it waits for this launch at
+// entry), so plain stores suffice and no launch depends on host-side state: launches can be
 // captured in a CUDA graph and replayed, and a launch whose barrier timed out leaves the words
-// ready for the next. Launches sharing a workspace must not overlap in time.
+// ready for the next. Launches sharing a workspace must be ordered (one stream): launches on
+// unordered streams would use the words at the same time.
 
 // The epoch (one thread per CTA, at the start of the launch; the value is needed only at the
 // arrival, so the load's latency hides behind the amax phase).
