@@ -95,27 +95,29 @@ __device__ __forceinline__ void global_scale(float amax, float& s_enc, float& s_
   s_dec = __frcp_rn(enc);
 }
 
-// x / 6 correctly rounded, for the finite BF16 magnitudes a block amax can take: the product
-// by the rounded reciprocal of 6, corrected by one remainder step (Markstein's correction for
-// a divisor known in advance; see Brisebarre, Muller and Raina, "Accelerating correctly
-// rounded floating-point division when the divisor is known in advance", IEEE Trans.
-// Computers 53(8), 2004). Equal to IEEE division on all 32,640 finite BF16 magnitudes.
-__device__ __forceinline__ float div6(float x) {
-  const float c = 0.16666667163372039794921875f;  // binary32 nearest to 1/6
-  float q = __fmul_rn(x, c);
-  float r = __fmaf_rn(-q, 6.0f, x);
-  return __fmaf_rn(r, c, q);
+// x / 6 correctly rounded for both lanes of a packed pair: the product by the rounded
+// reciprocal of 6, corrected by one remainder step (Markstein's correction for a divisor known
+// in advance; Brisebarre, Muller and Raina, "Accelerating correctly rounded floating-point
+// division when the divisor is known in advance", IEEE Trans. Computers 53(8), 2004). The
+// remainder x - 6q is exact (one fused multiply-add) and the corrected quotient equals IEEE
+// division by 6 on every non-negative binary32 whose quotient is normal; a quotient in the
+// subnormal range that lies exactly halfway between two subnormals can round the other way.
+// No BF16 value is such a case (a BF16 subnormal is an even multiple of 2^-149, so its sixth
+// is never an odd multiple of 2^-150), so the block maxima of BF16 blocks are always divided
+// exactly; the fast-math FP32 transform's maxima are outside that guarantee only at quotients
+// below 2^-126. A GPU test checks both statements over every non-negative finite binary32.
+__device__ __forceinline__ uint64_t div6x2(uint64_t x) {
+  const uint64_t c = f2_pack(0.16666667163372039794921875f, 0.16666667163372039794921875f);
+  const uint64_t neg6 = f2_pack(-6.0f, -6.0f);
+  const uint64_t q = f2_mul(x, c);
+  const uint64_t r = f2_fma(q, neg6, x);
+  return f2_fma(r, c, q);
 }
 
 // Two E4M3 block scales from two block maxima: s = E4M3_rn_satfinite((bamax / 6) * S_enc),
-// with x / 6 as in div6 (packed). Returns the pair as a 16-bit word, `lo` in the low byte.
+// with x / 6 as in div6x2. Returns the pair as a 16-bit word, `lo` in the low byte.
 __device__ __forceinline__ uint16_t block_scales2(float bamax_lo, float bamax_hi, float s_enc) {
-  const uint64_t c = f2_pack(0.16666667163372039794921875f, 0.16666667163372039794921875f);
-  const uint64_t neg6 = f2_pack(-6.0f, -6.0f);
-  const uint64_t x = f2_pack(bamax_lo, bamax_hi);
-  const uint64_t q = f2_mul(x, c);
-  const uint64_t r = f2_fma(q, neg6, x);
-  const float2 s = f2_unpack(f2_mul(f2_fma(r, c, q), f2_pack(s_enc, s_enc)));
+  const float2 s = f2_unpack(f2_mul(div6x2(f2_pack(bamax_lo, bamax_hi)), f2_pack(s_enc, s_enc)));
   uint16_t d;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(s.y), "f"(s.x));
   return d;

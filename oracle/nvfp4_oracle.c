@@ -334,6 +334,20 @@ ORACLE_API float oracle_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
 ORACLE_API uint8_t oracle_e2m1_encode_rn(float t) { return e2m1_encode_rn_satfinite(t); }
 ORACLE_API uint8_t oracle_e2m1_encode_sr(float t, uint32_t r16) { return e2m1_encode_sr_satfinite(t, r16); }
 ORACLE_API uint32_t oracle_sr_random16(uint32_t w, int32_t i) { return sr_random16(w, i); }
+/* One cvt.rs.satfinite.e2m1x4.f32 per random word, as reading R8 models it: element 4k+i
+ * (i = 0..3) of t is rounded with the 16-bit value that word k gives lane i; one code per
+ * byte of `codes` (sign in bit 3). The batch form of the per-element step of encode_block. */
+ORACLE_API void oracle_sr_convert4_n(const float* t, const uint32_t* words, int64_t n_words,
+                                     uint8_t* codes) {
+  for (int64_t k = 0; k < n_words; k++)
+    for (int i = 0; i < 4; i++)
+      codes[4 * k + i] = e2m1_encode_sr_satfinite(t[4 * k + i], sr_random16(words[k], i));
+}
+/* Round-to-nearest-even encoding of n values, one code per byte (the batch form of
+ * e2m1_encode_rn_satfinite). */
+ORACLE_API void oracle_e2m1_encode_rn_n(const float* t, int64_t n, uint8_t* codes) {
+  for (int64_t k = 0; k < n; k++) codes[k] = e2m1_encode_rn_satfinite(t[k]);
+}
 ORACLE_API float oracle_e2m1_decode(uint8_t n) { return e2m1_decode(n); }
 ORACLE_API void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
   philox4x32_10(ctr, key, out);

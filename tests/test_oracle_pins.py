@@ -705,3 +705,15 @@ def test_grouped_2d_tile_scales_transposes_padding_and_special_cases():
             assert np.array_equal(pcc, cc[:, col // 2:(col + P) // 2])
         prev, col = end, col + P
     assert np.all(cc[:, col // 2:] == 0xEE) and np.all(cs[:, col // 16:] == 0xEE)
+
+
+def test_batch_conversion_helpers_equal_the_per_element_steps():
+    """oracle.sr_convert4 and oracle.e2m1_encode_rn_n (used to check the conversion
+    instructions on the GPU) are batch forms of the pinned per-element encoders."""
+    rng = np.random.default_rng(77)
+    t = rng.uniform(-7, 7, size=4 * 300).astype(np.float32)
+    w = rng.integers(0, 2**32, size=300, dtype=np.uint64).astype(np.uint32)
+    one = np.array([oracle.e2m1_encode_sr(t[k], oracle.sr_random16(int(w[k // 4]), k % 4))[0]
+                    for k in range(t.size)], dtype=np.uint8)
+    assert np.array_equal(oracle.sr_convert4(t, w), one)
+    assert np.array_equal(oracle.e2m1_encode_rn_n(t), oracle.e2m1_encode_rn(t))
