@@ -2,8 +2,11 @@
 
 One step = the whole hot path on one batch of seeded synthetic input resident in HBM: every
 kernel a caller runs to turn a BF16 tensor into NVFP4 codes, E4M3 scales and FP32 global
-scales -- by default one nvfp4_quantize launch that computes the amax itself (fused_amax), or
-with --pipeline two_pass the amax kernel (nvfp4_amax) followed by the quantize kernel.
+scales. Grouped (MoE) workloads, the default: the per-expert amax pass (nvfp4_amax_grouped)
+then the grouped quantize kernel with those maxima (nvfp4_quantize_grouped), the two launches
+nvfp4_quantize_grouped makes on its own. Plain tensors: by default one nvfp4_quantize launch
+that computes the amax itself (fused_amax), or with --pipeline two_pass the amax kernel
+(nvfp4_amax) followed by the quantize kernel.
 Ideal bytes per step = one BF16 read + code writes + scale writes (the metric's roofline
 bytes). Between timed steps L2 holds none of the step's data: by default (--l2 rotate) the steps
 cycle through K input/output sets whose total is at least three times the L2 size (inputs
@@ -15,6 +18,7 @@ the flush, a pair around every step). Prints ONE JSON line (rank 0).
                   [--workload NAME] [--pipeline fused|two_pass] [--l2 rotate|flush]
 """
 import argparse
+import dataclasses
 import hashlib
 import re
 import json
@@ -33,7 +37,9 @@ sys.path.insert(0, ROOT)
 
 from nvfp4_block_scaled_quantize_gb300 import workloads  # noqa: E402
 
-DEFAULT_WORKLOAD = "activation_8192x4096_rowcol_rtne"
+# the largest configuration, and the pages' headline workload kind (grouped MoE row + col
+# RHT/SR quantization); the others through --workload
+DEFAULT_WORKLOAD = "moe_64experts_32768x7168_row_rtne_col_rht_sr"
 METRIC = "NVFP4 quantize GB/s (BF16 in) and fraction of GB300 HBM roofline, 1 GPU"
 FLUSH_BYTES = 256 << 20
 
@@ -380,11 +386,18 @@ def clear_l2(flush):
         flush.zero_()
 
 
+def workload_of(args):
+    """The named workload, or with --rows a smaller case of it (same distribution and options;
+    grouped inputs keep their expert count over fewer tokens), for profiling captures."""
+    w = workloads.WORKLOADS[args.workload]
+    return dataclasses.replace(w, rows=args.rows) if args.rows else w
+
+
 def run_ours(args, world, rank, local):
     from nvfp4_block_scaled_quantize_gb300 import api, _lib
     _lib.load()
     dev = torch.device("cuda", local)
-    w = workloads.WORKLOADS[args.workload]
+    w = workload_of(args)
     inp = workloads.make_input(w)
     x = inp["x"].to(dev)
     kw = quant_kwargs(w, inp)
@@ -407,15 +420,22 @@ def run_ours(args, world, rank, local):
         outs.append(alloc())
 
     if w.grouped:
+        # the two launches of nvfp4_quantize_grouped, made through the public calls so that
+        # events can sit between them: the per-expert amax pass, then the quantize kernel
         def step(j, ev=None):
             if ev:
                 ev[0].record(stream)
-            api.nvfp4_quantize_grouped(xs[j % n_sets], offsets, col_capacity=cap,
-                                       out=outs[j % n_sets], **kw)
+            xj = xs[j % n_sets]
+            a_row, a_col = api.nvfp4_amax_grouped(xj, offsets, rht_col=w.rht_col,
+                                                  sign_mask=kw["sign_mask"])
+            if ev:
+                ev[1].record(stream)
+            api.nvfp4_quantize_grouped(xj, offsets, col_capacity=cap, out=outs[j % n_sets],
+                                       amax_row=a_row, amax_col=a_col, **kw)
             if ev:
                 ev[2].record(stream)
         launches_per_step = 2
-        kernel_split = False
+        kernel_split = True
     else:
         rht_amax = w.rht_col
 
@@ -451,6 +471,7 @@ def run_ours(args, world, rank, local):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
         time.sleep(0.3)  # the sampler is up before the GPU work starts
+        clocks.mark_start()  # the record covers the warm-up and the timed region
         for j in range(args.warmup):
             clear_l2(flush)
             step(j)
@@ -460,7 +481,6 @@ def run_ours(args, world, rank, local):
             raise RuntimeError("device status %d (bits %#x) after warm-up" % (status, bits))
         barrier(world)
         torch.cuda.synchronize(dev)
-        clocks.mark_start()
         if per_step_timed:
             for i in range(args.steps):
                 clear_l2(flush)
@@ -483,7 +503,8 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status %d (bits %#x) after the timed steps" % (status, bits))
     step_ms = [e[0].elapsed_time(e[2]) for e in events]
     if kernel_split:
-        quant_ms = ([e[0].elapsed_time(e[2]) for e in events] if args.pipeline == "fused"
+        quant_ms = ([e[0].elapsed_time(e[2]) for e in events]
+                    if args.pipeline == "fused" and not w.grouped
                     else [e[1].elapsed_time(e[2]) for e in events])
     total_s = (sum(step_ms) if per_step_timed else t_start.elapsed_time(t_end)) / 1e3
     total_s = max_over_ranks(world, total_s)
@@ -510,7 +531,7 @@ def run_ours(args, world, rank, local):
         pipe = api.HostPipeline(w.rows, w.cols, depth=2, fused_amax=args.pipeline == "fused",
                                 **kw)
         host_out = pipe.alloc_host_outputs()
-        e2e_step = lambda: pipe.submit(x_host, host_out)
+        e2e_step = lambda: pipe.submit(x_host, host_out)  # noqa: E731
         e2e_join = pipe.join
 
     for _ in range(max(1, args.warmup)):
@@ -540,10 +561,12 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": [w.rows, w.cols],
+                   **({"rows_override": args.rows} if args.rows else {}),
                    "ideal_bytes_per_step": ideal,
                    "pipeline": ("one launch: amax phase, grid barrier, quantize phase"
                                 if args.pipeline == "fused" and not w.grouped else
-                                "amax pass + quantize pass (two launches)"),
+                                "per-expert amax pass + grouped quantize pass (two launches)"
+                                if w.grouped else "amax pass + quantize pass (two launches)"),
                    "math": "fast (rcp.approx multipliers%s)" % (
                        ", FP32 RHT" if w.rht_col else "") if args.fast_math and not w.block2d
                            else "exact",
@@ -564,7 +587,8 @@ def run_ours(args, world, rank, local):
     if kernel_split:
         # the single launch is the step, so its duration is the timed region's per-step time;
         # the two-pass pipeline's quantize kernel is timed alone by the events around it
-        qk = (total_s / args.steps if args.pipeline == "fused" and not per_step_timed
+        fused_step = args.pipeline == "fused" and not w.grouped
+        qk = (total_s / args.steps if fused_step and not per_step_timed
               else statistics.mean(quant_ms) / 1e3)
         achieved = ideal / qk / 1e9
         line["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -572,8 +596,9 @@ def run_ours(args, world, rank, local):
                             "kernel": "quantize_tiles_kernel",
                             "kernel_us": qk * 1e6,
                             "traffic": (None if args.fast_math
-                                        else kernel_traffic(w.name, args.pipeline))}
-        if args.pipeline != "fused" or w.grouped:
+                                        else kernel_traffic(w.name, "fused" if fused_step
+                                                            else "two_pass"))}
+        if not fused_step:
             line["amax_pass_us"] = statistics.mean([e[0].elapsed_time(e[1]) for e in events]) * 1e3
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp)
@@ -854,6 +879,9 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--rows", type=int, default=0,
+                   help="a smaller case of the workload (its first ROWS rows' shape and "
+                        "distribution; profiling captures), not a bench line")
     p.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                    help="between timed steps: rotate input/output sets totalling >= 3x L2 "
                         "(inputs larger than L2), or write a 256 MiB buffer before each step")

@@ -37,7 +37,7 @@
  *
  * Memory: the library allocates no memory on these calls except once per device, on the
  * first call that needs it: a small workspace (status word, the single-launch amax's counts,
- * maxima words and epoch; 16 KiB) allocated with cudaMalloc and kept until exit. Make that
+ * maxima words and claim bits; 16 KiB) allocated with cudaMalloc and kept until exit. Make that
  * first call outside CUDA-graph capture. Launches take no host-side state from call to call,
  * so a captured call replays correctly (the single-launch amax included). The host pipeline (end of this file) allocates its
  * device staging when it is created, and nothing when work is submitted.
@@ -92,27 +92,23 @@ typedef struct nvfp4_config {
   uint32_t rng_offset;    /* Philox counter word 3 (advance it to draw a new stream) */
   uint64_t rng_seed;      /* Philox key = (low 32 bits, high 32 bits) */
   int32_t fused_amax;     /* when the amax inputs are NULL: 0 = amax pass + quantize pass,
-                             1 = one launch: every CTA (one per SM) reduces the tiles it will
-                             quantize, folds its maxima into the workspace with an atomic max,
-                             counts its arrival and waits (bounded) for all CTAs, then
-                             quantizes (the re-read of x comes from L2 when x fits there).
-                             All CTAs must be resident at once: a device's calls are
-                             cooperative launches (which check that) until one with at least
-                             as large a grid has succeeded; later ones use programmatic
-                             dependent launch, so that a call may start on the SMs the previous
-                             single-launch call leaves. Such a launch waits for the previous
-                             kernel in the stream before it reads anything. A kernel launched
-                             after it with programmatic dependent launch may start before it
-                             ends and must wait for it before reading its outputs. On a device
-                             that cannot hold one CTA per SM for this call (e.g. a reduced
-                             MPS share), the wait gives up after about 2 s and reports
-                             NVFP4_DEVICE_TIMEOUT: use 0 there.
-                             Fused calls share the device workspace's counts, maxima and epoch
-                             (kept on the device: once every CTA has arrived, CTA 0 readies
-                             the count for the next launch and advances the epoch, so
-                             captured calls replay correctly): on one device they must not
-                             overlap in time (issue them on one stream).
-                             Plain tensors only. */
+                             1 = one launch: every CTA (one per SM) reduces its share of the
+                             tiles, folds the maxima into the workspace with an atomic max,
+                             counts the share as arrived and waits (bounded) for every share,
+                             then quantizes those tiles (the re-read of x comes from L2 when x
+                             fits there). No CTA waits for another to start: a CTA that has
+                             waited 20 us claims any share that no CTA has started and
+                             computes it itself, so the call also completes when some SMs are
+                             held by other work (another stream's kernels, a reduced MPS share,
+                             a green context), only more slowly. Launched with programmatic
+                             dependent launch: it waits for the previous kernel in the stream
+                             before it reads anything, and a kernel launched after it that way
+                             may start before it ends and must wait for it before reading its
+                             outputs. Fused calls share the device workspace's counts, maxima
+                             and claim bits (kept on the device: the last CTA to finish with
+                             them readies them for the next launch, so captured calls replay
+                             correctly): on one device they must not overlap in time (issue
+                             them on one stream). Plain tensors only. */
   int32_t fast_math;      /* 0 = exact (default). 1 = the fast variant of [PR4798] "Fast math":
                              the element multiplier is rcp.approx.ftz(float(s) * S_dec) instead
                              of the correctly rounded reciprocal, and the columnwise RHT output
@@ -182,6 +178,10 @@ nvfp4_status nvfp4_amax_grouped(const void* x, int64_t T, int64_t H, const int32
  *   offsets      (device) int32 [E], non-decreasing, offsets[E-1] <= T; expert e owns rows
  *                [offsets[e-1], offsets[e]) with offsets[-1] = 0 (empty experts allowed).
  *   E            1 <= E <= 256.
+ *   amax_row, amax_col  (device) float[E] each (per-expert amax, e.g. from
+ *                nvfp4_amax_grouped or a producer's epilogue), or NULL to compute them inside
+ *                this call (amax_col is the RHT amax when cfg->rht_col). With block2d both
+ *                orientations use amax_row.
  *   col_capacity columns of the columnwise outputs, a multiple of 16, >= sum_e pad16(n_e)
  *                (pad16 rounds a token count up to a multiple of 16). Expert e's columnwise
  *                block starts at column sum_{j<e} pad16(n_j); its last partial 16-token block
@@ -198,6 +198,7 @@ nvfp4_status nvfp4_amax_grouped(const void* x, int64_t T, int64_t H, const int32
 nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
                                     const int32_t* offsets, int32_t E, int64_t col_capacity,
                                     const nvfp4_config* cfg,
+                                    const float* amax_row, const float* amax_col,
                                     uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,
                                     uint8_t* col_codes, uint8_t* col_scales, float* col_gscale,
                                     void* stream);
@@ -230,25 +231,33 @@ nvfp4_status nvfp4_dequantize_ex(const uint8_t* codes, const uint8_t* scales, co
  * fixed memory budget. The pages have no counterpart of this entry point; it exists only so
  * that such callers get the single-launch path.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its scratch
- * -- a status word, the CTAs' counts, two maxima words and an epoch, 256 bytes in all -- is a
- * static device array that every GPU loading this library holds until exit. The caller still
- * passes x and every output.
+ * -- a status word, the single-launch amax's counts, two maxima words and one claim bit per
+ * CTA, 256 bytes in all -- is a static device array that every GPU loading this library holds
+ * until exit. The caller still passes x and every output.
  *   Arguments, layouts and shape rules as nvfp4_quantize with amax_row = amax_col = NULL and
  *   cfg->fused_amax = 1 (cfg->fused_amax itself is ignored); M and N must be positive.
  *   The first call on a device looks up the array's device address and prepares the kernels
  *   (no allocation): make that first call before any stream capture.
- *   A device whose launch would need more than 1024 CTAs is refused with
+ *   A device whose launch would need more than 1024 CTAs (one claim bit each) is refused with
  *   NVFP4_ERR_UNSUPPORTED (GB300 launches one CTA per SM, 152).
  *   Every call on a device shares the array: calls that overlap on the GPU race (issue them on
- *   one stream). The array is zero when the library loads; each launch tags its maxima with the
- *   epoch after the one it reads there, and once its CTAs have arrived CTA 0 readies the count
- *   for the next launch and advances the epoch, so nothing needs clearing between calls and a
- *   captured call replays correctly. A wait that gives up is recorded in the array's own
- *   status word, which nvfp4_get_status does not read. */
+ *   one stream). The array is zero when the library loads and the last CTA of each launch to
+ *   finish with the counts readies them for the next, so nothing needs clearing between calls
+ *   and a captured call replays correctly. A wait that gives up is recorded in the array's own
+ *   status word: read it with nvfp4_noalloc_get_status (nvfp4_get_status reads the regular
+ *   workspace's). */
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t N, const nvfp4_config* cfg,
                                     uint8_t* row_codes, uint8_t* row_scales, float* row_gscale,
                                     uint8_t* col_codes, uint8_t* col_scales, float* col_gscale,
                                     void* stream);
+
+/* The status word of nvfp4_quantize_noalloc's array on the current device, without allocating
+ * (the pages have no counterpart): synchronize `stream`, then read and clear the word with
+ * synchronous copies from and to the array itself. *device_status receives the NVFP4_DEVICE_*
+ * bits that the no-alloc calls recorded since the last read. Returns NVFP4_ERR_TIMEOUT when a
+ * wait of one of those calls gave up (its outputs are then incomplete), NVFP4_OK when no bit
+ * was set. Errors: NVFP4_ERR_INVALID_ARG (NULL device_status), NVFP4_ERR_CUDA. */
+nvfp4_status nvfp4_noalloc_get_status(void* stream, uint32_t* device_status);
 
 /* Scale bytes in the layout the tensor-core block-scaled (NVFP4) GEMMs read, e.g. cuBLASLt's
  * ([PR4798] "Config surface and AUTO": the reference's columnwise scale store is hardwired to
@@ -321,9 +330,9 @@ nvfp4_status nvfp4_mx_quantize(const void* x, int64_t M, int64_t N, int32_t form
 nvfp4_status nvfp4_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int32_t format,
                                  int64_t R, int64_t C, float* out, void* stream);
 
-/* The per-device workspace: the status word the kernels report to, and the counts, the
- * epoch-tagged maxima and the epoch of the single-launch amax. By default the library allocates it with
- * cudaMalloc (once per device, on the first call that needs it, zeroed) and never frees it. */
+/* The per-device workspace: the status word the kernels report to, and the counts, maxima and
+ * claim bits of the single-launch amax. By default the library allocates it with cudaMalloc
+ * (once per device, on the first call that needs it, zeroed) and never frees it. */
 #define NVFP4_WORKSPACE_BYTES 16384
 
 /* Use caller-owned device memory as the current device's workspace instead, e.g. memory from
@@ -342,14 +351,28 @@ nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes);
  * when bits were set, NVFP4_OK otherwise. */
 nvfp4_status nvfp4_get_status(void* stream, uint32_t* device_status);
 
-/* Test hook for the bounded wait of the single-launch amax: the next nvfp4_quantize call that
- * takes the single-launch path (on any device) waits for `extra` arrivals more than its grid
- * has CTAs. With extra > 0 no launch can reach that count, so every CTA gives up after its
- * bounded wait (about 2 s), stores nothing, sets NVFP4_DEVICE_TIMEOUT and exits; CTA 0 still
- * readies the workspace for the next launch, so the next call runs normally. The hook is consumed by
- * that one call (0 clears it). Not for production use.
- * Errors: NVFP4_ERR_INVALID_ARG (extra outside 0 .. 1024). */
+/* Test hook for the bounded wait of the single-launch amax: the next call that takes the
+ * single-launch path (nvfp4_quantize or nvfp4_quantize_noalloc, on any device) waits for
+ * `extra` arrivals more than its grid has shares. With extra > 0 no launch can reach that
+ * count, so every CTA gives up after its bounded wait (about 2 s), stores nothing, sets
+ * NVFP4_DEVICE_TIMEOUT and exits; the last CTA to finish still readies the counts for the next
+ * launch, so the next call runs normally. The hook is consumed by that one call (0 clears it).
+ * Not for production use. Errors: NVFP4_ERR_INVALID_ARG (extra outside 0 .. 1024). */
 nvfp4_status nvfp4_debug_fused_extra_arrivals(int32_t extra);
+
+/* Test hook for the take-over of shares: in the next single-launch call (as above), the last
+ * `count` CTAs of the grid hold back before they claim their own shares until every share has
+ * arrived (bounded, about 2 s), as if their SMs were busy with other work. The other CTAs then
+ * take those shares over after their 20 us wait, and the held-back CTAs find their shares
+ * taken. The outputs are those of a normal call. Consumed by that one call (0 clears it). Not
+ * for production use. Errors: NVFP4_ERR_INVALID_ARG (count outside 0 .. 1024). */
+nvfp4_status nvfp4_debug_fused_late_ctas(int32_t count);
+
+/* Synchronize `stream`, then read and clear the count of shares that single-launch calls on
+ * the current device's workspace have taken over from CTAs that had not claimed them yet
+ * (statistics for tests; nvfp4_quantize_noalloc's calls are not counted). Errors:
+ * NVFP4_ERR_INVALID_ARG (NULL count), NVFP4_ERR_CUDA. */
+nvfp4_status nvfp4_debug_fused_takeovers(void* stream, uint32_t* count);
 
 /* Test hook for launch failures: with on = 1, the next nvfp4_quantize or nvfp4_quantize_grouped
  * call (on any device) launches its quantize kernel with an empty grid, which the runtime

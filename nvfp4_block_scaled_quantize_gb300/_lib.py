@@ -26,7 +26,8 @@ EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quanti
             "nvfp4_mx_quantize", "nvfp4_mx_dequantize", "nvfp4_dequantize_ex",
             "nvfp4_rmsnorm_amax", "nvfp4_rmsnorm_quantize", "nvfp4_set_workspace",
             "nvfp4_amax_grouped", "nvfp4_debug_fused_extra_arrivals",
-            "nvfp4_debug_fail_next_launch"]
+            "nvfp4_debug_fail_next_launch", "nvfp4_noalloc_get_status",
+            "nvfp4_debug_fused_late_ctas", "nvfp4_debug_fused_takeovers"]
 
 
 class Config(ctypes.Structure):
@@ -82,7 +83,7 @@ def load(build_if_missing: bool = False):
     L.nvfp4_quantize.argtypes = [vp, i64, i64, cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.nvfp4_quantize_grouped.restype = ctypes.c_int
     L.nvfp4_quantize_grouped.argtypes = [vp, i64, i64, vp, i32, i64, cfgp, vp, vp, vp, vp, vp,
-                                         vp, vp]
+                                         vp, vp, vp, vp]
     L.nvfp4_dequantize.restype = ctypes.c_int
     L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     L.nvfp4_quantize_noalloc.restype = ctypes.c_int
@@ -119,5 +120,11 @@ def load(build_if_missing: bool = False):
     L.nvfp4_debug_fused_extra_arrivals.argtypes = [i32]
     L.nvfp4_debug_fail_next_launch.restype = ctypes.c_int
     L.nvfp4_debug_fail_next_launch.argtypes = [i32]
+    L.nvfp4_noalloc_get_status.restype = ctypes.c_int
+    L.nvfp4_noalloc_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.nvfp4_debug_fused_late_ctas.restype = ctypes.c_int
+    L.nvfp4_debug_fused_late_ctas.argtypes = [i32]
+    L.nvfp4_debug_fused_takeovers.restype = ctypes.c_int
+    L.nvfp4_debug_fused_takeovers.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     _lib = L
     return L

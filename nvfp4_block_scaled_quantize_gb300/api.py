@@ -114,10 +114,12 @@ def padded_capacity(counts) -> int:
 
 def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwise=True,
                            round_row="rn", round_col="rn", rht_col=False, sign_mask=0, seed=0,
-                           offset=0, out=None, fast_math=False, block2d=False):
+                           offset=0, out=None, fast_math=False, block2d=False, amax_row=None,
+                           amax_col=None):
     """Grouped quantization of a packed BF16 [T, H] tensor; `offsets` is an int32 [E] device
     tensor of cumulative expert ends. col_capacity defaults to T + 16 * E (always enough).
-    block2d: 16x16 tiles per expert (stacked expert weights), no RHT or SR."""
+    block2d: 16x16 tiles per expert (stacked expert weights), no RHT or SR. amax_row /
+    amax_col (float32 [E] device tensors, e.g. from nvfp4_amax_grouped) skip the amax pass."""
     _check_x(x)
     L = _lib.load()
     if offsets.dtype != torch.int32 or not offsets.is_cuda or offsets.dim() != 1:
@@ -132,8 +134,8 @@ def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwi
         out = alloc_outputs(T, H, x.device, rowwise, columnwise, col_ld=col_capacity, groups=E)
     g = out.get
     status = L.nvfp4_quantize_grouped(
-        _ptr(x), T, H, _ptr(offsets), E, col_capacity, ctypes.byref(cfg),
-        _ptr(g("row_codes")), _ptr(g("row_scales")), _ptr(g("row_gscale")),
+        _ptr(x), T, H, _ptr(offsets), E, col_capacity, ctypes.byref(cfg), _ptr(amax_row),
+        _ptr(amax_col), _ptr(g("row_codes")), _ptr(g("row_scales")), _ptr(g("row_gscale")),
         _ptr(g("col_codes")), _ptr(g("col_scales")), _ptr(g("col_gscale")), _stream(x.device))
     _raise_if(status, "nvfp4_quantize_grouped")
     return out
@@ -309,9 +311,36 @@ def nvfp4_get_status(device=None):
 
 def nvfp4_debug_fused_extra_arrivals(extra):
     """Test hook: the next single-launch amax call waits for `extra` arrivals more than its grid
-    has CTAs, so its bounded wait runs out (about 2 s) and it reports NVFP4_DEVICE_TIMEOUT."""
+    has shares, so its bounded wait runs out (about 2 s) and it reports NVFP4_DEVICE_TIMEOUT."""
     _raise_if(_lib.load().nvfp4_debug_fused_extra_arrivals(int(extra)),
               "nvfp4_debug_fused_extra_arrivals")
+
+
+def nvfp4_debug_fused_late_ctas(count):
+    """Test hook: in the next single-launch amax call the last `count` CTAs hold back until
+    every share has arrived, so the other CTAs take their shares over."""
+    _raise_if(_lib.load().nvfp4_debug_fused_late_ctas(int(count)), "nvfp4_debug_fused_late_ctas")
+
+
+def nvfp4_debug_fused_takeovers(device=None):
+    """Synchronize the current stream and return (and clear) the count of shares taken over by
+    single-launch calls on the device's workspace."""
+    L = _lib.load()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    n = ctypes.c_uint32(0)
+    _raise_if(L.nvfp4_debug_fused_takeovers(_stream(dev), ctypes.byref(n)),
+              "nvfp4_debug_fused_takeovers")
+    return n.value
+
+
+def nvfp4_noalloc_get_status(device=None):
+    """Synchronize the current stream and return (status, device status bits) of the no-alloc
+    entry point's own status word; clears it."""
+    L = _lib.load()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    bits = ctypes.c_uint32(0)
+    status = L.nvfp4_noalloc_get_status(_stream(dev), ctypes.byref(bits))
+    return status, bits.value
 
 
 def nvfp4_debug_fail_next_launch(on=True):

@@ -1,12 +1,33 @@
-// Single-launch amax for the quantize kernel: every CTA reduces the tiles it is about to
-// quantize (plain and, for the columnwise RHT, transformed maxima), folds them into two
-// launch-tagged maxima words with an atomic max, counts its arrival, and waits until every
-// CTA has arrived (a grid barrier that carries the result). These are the reduction and
-// exchange pieces; the tile walk is in the quantize kernel.
+// Single-launch amax for the quantize kernel: the amax of the whole tensor is needed before
+// any block can be quantized, so every CTA first reduces its share of the tiles, folds the
+// maxima into two workspace words with an atomic max and counts the share as arrived; once
+// every share has arrived the maxima are final. These are the reduction and exchange pieces;
+// the tile walk is in the quantize kernel.
 //
 // Page cited: "[nvfp4_training] Optimize CuteDSL kernels for NVFP4 training" (pytorch/ao pull
 // request #4798), "Performance": its pipelines are an amax kernel followed by a quantize
 // kernel; this folds the two into one launch.
+//
+// No CTA waits for another CTA to start. The tiles are split into G shares ("ranks", G = the
+// grid size; rank r is every G-th tile from tile r). CTA b claims rank b when it starts, but
+// a CTA that has waited a while for the arrivals claims any rank still unclaimed and does
+// that share's amax itself. A CTA that has not started yet (its SM held by another stream's
+// kernel, a reduced MPS share, a green context) thus never holds the others up: the waiters
+// take over its share, and when it starts it finds its rank taken and only quantizes. A CTA
+// quantizes every rank whose amax it computed, its own included even when its own rank was
+// taken meanwhile (both CTAs then write the same bytes).
+//
+// Workspace words (kFuseWsWords, zero before the first launch):
+//   [0] ranks arrived   [1] CTAs done with the words   [2] rowwise max   [3] columnwise max
+//   [4] ranks taken over from another CTA, ever (statistics; not reset)
+//   [8 .. 8 + kFuseMaxCtas / 32) one claim bit per rank
+// A CTA is done with the words once its wait has ended (passed or not); the last of the G to
+// get there zeroes words 0-3 and the claim bits, which readies them for the next launch. The
+// next launch on the stream reads them only after this launch has ended (it waits for it at
+// entry), so the reset needs no ordering beyond that, and no launch depends on host-side
+// state: launches can be captured in a CUDA graph and replayed, and a launch whose wait gave
+// up leaves the words ready for the next. Launches sharing a workspace must be ordered (one
+// stream): launches on unordered streams would use the words at the same time.
 #pragma once
 
 #include "nvfp4_device.cuh"
@@ -16,6 +37,18 @@ namespace nvfp4 {
 namespace qk {
 
 constexpr uint64_t kBarrierLimitNs = 2000000000ull;  // 2 s
+// A CTA that has waited this long for the arrivals starts claiming unclaimed ranks. Far above
+// the spread of CTA start times within one launch (a few microseconds), so that in an
+// undisturbed launch every CTA does its own rank.
+constexpr uint64_t kStealAfterNs = 20000ull;
+
+constexpr int kFuseArrived = 0;
+constexpr int kFuseDone = 1;
+constexpr int kFuseMaxRow = 2;
+constexpr int kFuseMaxCol = 3;
+constexpr int kFuseSteals = kFuseStatsWord;
+constexpr int kFuseClaims = 8;
+static_assert(kFuseClaims + kFuseMaxCtas / 32 <= kFuseWsWords, "claim bits outside the workspace");
 
 // Max over the CTA of a 16-bit magnitude held in a 32-bit word (every thread gets it).
 // red: 32 words of shared memory, free on entry.
@@ -30,70 +63,89 @@ __device__ __forceinline__ uint32_t cta_max(uint32_t v, volatile uint32_t* red) 
   return r;
 }
 
-// Workspace words of the single-launch amax (kFuseWsWords, 8-byte aligned): [0] and [1] the
-// arrival counts of launches with even and odd epochs, [2..3] and [4..5] the rowwise and
-// columnwise maxima as (epoch << 16) | 16-bit magnitude, [6..7] the epoch (64 bits, so tags
-// stay below 2^48 for longer than any process runs). A launch reads the epoch E when it starts,
-// counts its arrivals on word E & 1 and tags its maxima with E + 1; once CTA 0 has seen every
-// arrival (or given up) it zeroes the other count, which the next launch uses, and stores
-// E + 1. Every CTA has read E before it arrives, and the next launch on the stream reads the
-// words only once this one has ended (even when it starts early, it waits for this launch at
-// entry), so plain stores suffice and no launch depends on host-side state: launches can be
-// captured in a CUDA graph and replayed, and a launch whose barrier timed out leaves the words
-// ready for the next. Launches sharing a workspace must be ordered (one stream): launches on
-// unordered streams would use the words at the same time.
-
-// The epoch (one thread per CTA, at the start of the launch; the value is needed only at the
-// arrival, so the load's latency hides behind the amax phase).
-__device__ __forceinline__ uint64_t fuse_epoch(const uint32_t* ws) {
-  unsigned long long e;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(e) : "l"(ws + 6) : "memory");
-  return e;
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
-// Arrival of this CTA (one thread): fold its maxima (16-bit magnitudes) into the two maxima
-// words under the launch's tag, then count itself; the release orders the maxima before the
-// count. Tags grow from launch to launch, so the atomic max needs no clearing in between.
-__device__ __forceinline__ void fuse_arrive(uint32_t* ws, uint64_t epoch, uint32_t mr, uint32_t mc) {
-  unsigned long long* mx = reinterpret_cast<unsigned long long*>(ws + 2);
-  const unsigned long long tag = epoch + 1u;
-  const unsigned long long vr = (tag << 16) | mr, vc = (tag << 16) | mc;
-  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(mx), "l"(vr) : "memory");
-  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(mx + 1), "l"(vc) : "memory");
-  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws + (epoch & 1u)) : "memory");
+// Claim rank r (one thread): returns the claim word's previous value; the claim succeeded
+// when r's bit was clear in it.
+__device__ __forceinline__ uint32_t fuse_claim(uint32_t* ws, int r) {
+  return atomicOr(ws + kFuseClaims + (r >> 5), 1u << (r & 31));
 }
 
-// Wait (one thread, bounded) until `target` CTAs have arrived, then read the maxima of every
-// CTA. Returns false when the wait passed its limit or the maxima carry another tag.
-__device__ __forceinline__ bool fuse_wait(const uint32_t* ws, uint64_t epoch, uint32_t target,
-                                          uint32_t& mr, uint32_t& mc) {
-  const uint32_t* count = ws + (epoch & 1u);
-  uint32_t c;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(count) : "memory");
-  if (c < target) {
-    uint64_t t0, t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    do {
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-      if (t - t0 > kBarrierLimitNs) return false;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(count) : "memory");
-    } while (c < target);
+// One share's arrival (one thread): fold the CTA's maxima (16-bit magnitudes) into the maxima
+// words, then count `shares` ranks as arrived; the release orders the maxima before the count.
+__device__ __forceinline__ void fuse_arrive(uint32_t* ws, uint32_t mr, uint32_t mc, uint32_t shares) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(ws + kFuseMaxRow), "r"(mr) : "memory");
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(ws + kFuseMaxCol), "r"(mc) : "memory");
+  if (shares) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ws + kFuseArrived), "r"(shares) : "memory");
+}
+
+enum FuseWait { kFuseReady = 0, kFuseSteal = 1, kFuseTimedOut = 2 };
+
+// Wait (one thread, bounded) until `target` ranks have arrived, then read the maxima. After
+// kStealAfterNs (counted from t_start, when the CTA began waiting) the waiter looks for a rank
+// that no CTA has claimed among the G ranks; if it wins one it returns kFuseSteal with the
+// rank, to do that share's amax and come back. kFuseTimedOut after kBarrierLimitNs.
+// may_steal = false: only wait (the CTA holds as many ranks as it can).
+__device__ __forceinline__ FuseWait fuse_wait(uint32_t* ws, uint32_t target, int G, uint64_t t_start,
+                                              bool may_steal, uint32_t& mr, uint32_t& mc,
+                                              int& rank) {
+  const int words = (G + 31) >> 5;
+  uint64_t next_scan = t_start + kStealAfterNs;
+  while (ld_acquire(ws + kFuseArrived) < target) {
+    const uint64_t t = global_ns();
+    if (t - t_start > kBarrierLimitNs) return kFuseTimedOut;
+    if (!may_steal || t < next_scan) continue;
+    next_scan = t + kStealAfterNs / 4;
+    for (int i = 0; i < words; i++) {
+      const int w = ((int)(blockIdx.x >> 5) + i) % words;
+      const uint32_t valid = (w == words - 1 && (G & 31)) ? (1u << (G & 31)) - 1u : 0xFFFFFFFFu;
+      uint32_t taken = ld_relaxed(ws + kFuseClaims + w);
+      for (int tries = 0; tries < 32 && (~taken & valid); tries++) {
+        const int b = __ffs(~taken & valid) - 1;
+        const uint32_t before = atomicOr(ws + kFuseClaims + w, 1u << b);
+        if (!(before & (1u << b))) {
+          rank = 32 * w + b;
+          atomicAdd(ws + kFuseSteals, 1u);
+          return kFuseSteal;
+        }
+        taken = before | (1u << b);
+      }
+    }
   }
-  unsigned long long vr, vc;
-  const unsigned long long* mx = reinterpret_cast<const unsigned long long*>(ws + 2);
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(vr) : "l"(mx) : "memory");
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(vc) : "l"(mx + 1) : "memory");
-  if ((vr >> 16) != epoch + 1u || (vc >> 16) != epoch + 1u) return false;
-  mr = (uint32_t)vr & 0xFFFFu;
-  mc = (uint32_t)vc & 0xFFFFu;
-  return true;
+  mr = ld_acquire(ws + kFuseMaxRow);
+  mc = ld_acquire(ws + kFuseMaxCol);
+  return kFuseReady;
 }
 
-// CTA 0, once its wait has ended (passed or not): ready the words for the next launch.
-__device__ __forceinline__ void fuse_advance(uint32_t* ws, uint64_t epoch) {
-  const unsigned long long next = epoch + 1u;
-  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ws + (next & 1u)), "r"(0u) : "memory");
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(ws + 6), "l"(next) : "memory");
+// A CTA done with the words (one thread; after its wait has ended, passed or not): counts
+// itself and returns the count before it, to be handed to fuse_reset_if_last at the end.
+__device__ __forceinline__ uint32_t fuse_done(uint32_t* ws) {
+  return atomicAdd(ws + kFuseDone, 1u);
+}
+
+// The last of the G CTAs to be done with the words readies them for the next launch.
+__device__ __forceinline__ void fuse_reset_if_last(uint32_t* ws, uint32_t done_before, int G) {
+  if (done_before != (uint32_t)G - 1u) return;
+  volatile uint32_t* v = ws;
+  v[kFuseArrived] = 0u;
+  v[kFuseMaxRow] = 0u;
+  v[kFuseMaxCol] = 0u;
+  for (int w = 0; w < (G + 31) >> 5; w++) v[kFuseClaims + w] = 0u;
+  v[kFuseDone] = 0u;
 }
 
 }  // namespace qk

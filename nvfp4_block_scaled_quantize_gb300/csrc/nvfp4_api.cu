@@ -29,16 +29,15 @@ struct DeviceState {
   int sm_count = 0;
   uint32_t* workspace = nullptr;  // [0] status word; the library's own or the caller's
   uint32_t* own = nullptr;        // the library's own workspace, allocated on first need
-  // the largest grid of a cooperative single-launch call that has succeeded on this device:
-  // calls with a grid no larger are known to fit at once and use programmatic dependent
-  // launch instead (quantize_kernel.cuh, launch)
-  std::atomic<int> coop_checked_grid{0};
 };
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 // Arrivals the next single-launch amax awaits beyond its grid (nvfp4_debug_fused_extra_arrivals)
 std::atomic<int32_t> g_fuse_extra{0};
+// CTAs of the next single-launch amax that hold back until every rank has arrived
+// (nvfp4_debug_fused_late_ctas)
+std::atomic<int32_t> g_fuse_late{0};
 // Set: the next quantize call launches an empty grid, which the runtime rejects
 // (nvfp4_debug_fail_next_launch)
 std::atomic<int32_t> g_fail_next{0};
@@ -128,6 +127,11 @@ __global__ void gscale_fill_kernel(const float* amax, float* gscale, int n) {
 
 }  // namespace
 
+void take_fuse_debug(QuantArgs& q) {
+  q.fuse_extra = g_fuse_extra.exchange(0);
+  q.fuse_late = g_fuse_late.exchange(0);
+}
+
 cudaError_t launch_quantize(const QuantMode& m, const QuantArgs& args, int grid, cudaStream_t s) {
   if (m.two_d) return launch_quantize_2d(m, args, grid, s);
   if (m.row && m.col) return m.rht ? launch_quantize_rowcol_rht(m, args, grid, s)
@@ -153,13 +157,6 @@ namespace {
 // A failed launch or call is reported as NVFP4_ERR_CUDA; the runtime's last-error state is
 // cleared so that the caller's next, unrelated error check does not see it (a sticky error
 // stays sticky).
-// Raise the largest cooperatively checked grid to g (concurrent callers may race: keep the max).
-void note_checked_grid(std::atomic<int>& checked, int g) {
-  int cur = checked.load();
-  while (cur < g && !checked.compare_exchange_weak(cur, g)) {
-  }
-}
-
 nvfp4_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return NVFP4_OK;
   (void)cudaGetLastError();
@@ -347,20 +344,17 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
   const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};
-  // the barrier's counts and epoch live on the device (CTA 0 readies them for the next launch),
-  // so the launch depends on no host state and can be captured in a CUDA graph
-  if (fused) {
-    q.fuse_extra = g_fuse_extra.exchange(0);
-    q.coop_launch = grid > ds->coop_checked_grid.load() ? 1 : 0;
-  }
-  const cudaError_t e = launch_quantize(mode, q, launch_grid(grid), s);
-  if (e == cudaSuccess && fused && q.coop_launch) note_checked_grid(ds->coop_checked_grid, grid);
-  return cuda_status(e);
+  // the single-launch amax keeps its counts on the device (the last CTA to finish with them
+  // readies them for the next launch), so the launch depends on no host state and can be
+  // captured in a CUDA graph
+  if (fused) take_fuse_debug(q);
+  return cuda_status(launch_quantize(mode, q, launch_grid(grid), s));
 }
 
 NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64_t H,
                                                  const int32_t* offsets, int32_t E,
                                                  int64_t col_capacity, const nvfp4_config* cfg,
+                                                 const float* amax_row, const float* amax_col,
                                                  uint8_t* row_codes, uint8_t* row_scales,
                                                  float* row_gscale, uint8_t* col_codes,
                                                  uint8_t* col_scales, float* col_gscale,
@@ -386,7 +380,8 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
     return NVFP4_ERR_INVALID_ARG;
   if ((!empty && (x == nullptr || !aligned(x, 16))) || !aligned(offsets, 4) ||
       (row && (!aligned(row_codes, 16) || !aligned(row_scales, 16) || !aligned(row_gscale, 4))) ||
-      (col && (!aligned(col_codes, 16) || !aligned(col_scales, 16) || !aligned(col_gscale, 4))))
+      (col && (!aligned(col_codes, 16) || !aligned(col_scales, 16) || !aligned(col_gscale, 4))) ||
+      (amax_row && !aligned(amax_row, 4)) || (amax_col && !aligned(amax_col, 4)))
     return NVFP4_ERR_ALIGN;
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != NVFP4_OK) return st;
@@ -397,12 +392,20 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
     if (col) gscale_fill_kernel<<<1, 256, 0, s>>>(nullptr, col_gscale, E);
     return cuda_status(cudaGetLastError());
   }
-  // per-expert amax (and RHT amax) from one read, into the gscale outputs' amax slots
-  if (row && cudaMemsetAsync(row_gscale, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
-  if (col && cudaMemsetAsync(col_gscale, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
-  if ((st = amax_tiles(ds, x, T, H, offsets, E, cfg->rht_sign_mask, rht,
-                       row ? row_gscale : nullptr, col ? col_gscale : nullptr, 2, s)) != NVFP4_OK)
-    return st;
+  // per-expert amax (and RHT amax) of what the caller did not supply, from one read, into the
+  // gscale outputs' amax slots. 2D reads the one per-expert amax from the rowwise side (kept in
+  // col_gscale when only columnwise).
+  const bool need_row = (row || two_d) && amax_row == nullptr;
+  const bool need_col = col && !two_d && amax_col == nullptr;
+  float* row_slot = row ? row_gscale : col_gscale;
+  if (need_row || need_col) {
+    if (need_row && cudaMemsetAsync(row_slot, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (need_col && cudaMemsetAsync(col_gscale, 0, 8 * (size_t)E, s) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if ((st = amax_tiles(ds, x, T, H, offsets, E, cfg->rht_sign_mask, need_col && rht,
+                         need_row ? row_slot : nullptr, need_col ? col_gscale : nullptr, 2, s)) !=
+        NVFP4_OK)
+      return st;
+  }
 
   QuantArgs q;
   std::memset(&q, 0, sizeof q);
@@ -410,9 +413,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   q.rows = T; q.cols = H; q.offsets = offsets; q.segments = E;
   const int sr_row = cfg->round_row == NVFP4_ROUND_SR, sr_col = cfg->round_col == NVFP4_ROUND_SR;
   q.sign_mask = cfg->rht_sign_mask; q.col_ld = col ? col_capacity : 0;
-  // 2D reads the one per-expert amax from amax_row (kept in col_gscale when only columnwise)
-  q.amax_row = row ? row_gscale : (two_d ? col_gscale : nullptr); q.amax_col = col_gscale;
-  q.amax_row_stride = 2; q.amax_col_stride = 2;
+  q.amax_row = amax_row ? amax_row : ((row || two_d) ? row_slot : nullptr);
+  q.amax_col = amax_col ? amax_col : col_gscale;
+  q.amax_row_stride = amax_row ? 1 : 2; q.amax_col_stride = amax_col ? 1 : 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
   q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
@@ -629,6 +632,28 @@ NVFP4_EXPORT nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes) {
 NVFP4_EXPORT nvfp4_status nvfp4_debug_fused_extra_arrivals(int32_t extra) {
   if (extra < 0 || extra > kFuseMaxCtas) return NVFP4_ERR_INVALID_ARG;
   g_fuse_extra.store(extra);
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_debug_fused_late_ctas(int32_t count) {
+  if (count < 0 || count > kFuseMaxCtas) return NVFP4_ERR_INVALID_ARG;
+  g_fuse_late.store(count);
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_debug_fused_takeovers(void* stream, uint32_t* count) {
+  if (count == nullptr) return NVFP4_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  nvfp4_status st = device_state(&ds);
+  if (st != NVFP4_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_status(cudaErrorUnknown);
+  uint32_t* word = ds->workspace + kFuseWsOffset + kFuseStatsWord;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, word, 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(word, 0, 4) != cudaSuccess)
+    return cuda_status(cudaErrorUnknown);
+  *count = v;
   return NVFP4_OK;
 }
 

@@ -40,13 +40,19 @@ constexpr int kSmemBars = kSmemCoords + 32 * kStages;                 // full[kS
 constexpr int kSmemFlags = kSmemBars + 8 * kStages;                   // int32 [4]
 constexpr int kSmemIssued = kSmemFlags + 16;                          // int32 [kStages]
 constexpr int kSmemFused = kSmemIssued + 4 * kStages;            // uint32 [32 + 4]
-constexpr int kQuantSmemBytes = kSmemFused + 4 * 36;
+// single-launch amax: the ranks this CTA does the amax of, each with its first ring slot
+constexpr int kMaxHeld = 128;
+constexpr int kSmemHeld = kSmemFused + 4 * 36;                   // int32 [2][kMaxHeld]
+constexpr int kSmemFuseCtl = kSmemHeld + 8 * kMaxHeld;            // int32 [4]
+constexpr int kQuantSmemBytes = kSmemFuseCtl + 16;
 
-// Workspace of the single-launch (fused amax) path, 8-byte aligned, zeroed before first use:
-// the arrival and exit counts of the running launch, the rowwise and columnwise maxima tagged
-// with the launch's epoch, and the epoch itself, all kept on the device (fused_amax.cuh).
+// Workspace of the single-launch (fused amax) path, 4-byte aligned, zeroed before first use:
+// the count of ranks arrived, the count of CTAs done with the words, the rowwise and
+// columnwise maxima, a statistics counter and one claim bit per rank, all kept on the device
+// (fused_amax.cuh). At most kFuseMaxCtas CTAs (one claim bit each).
 constexpr int kFuseMaxCtas = 1024;
-constexpr int kFuseWsWords = 8;
+constexpr int kFuseWsWords = 8 + kFuseMaxCtas / 32;
+constexpr int kFuseStatsWord = 4;  // ranks taken over from another CTA (statistics)
 
 // Arguments of the quantize kernel: one BF16 tensor split into row segments (one segment for
 // a plain tensor, one per expert for the grouped case).
@@ -75,9 +81,10 @@ struct QuantArgs {
   int32_t fast;                     // 1: fast-math element multipliers (rcp.approx)
   int32_t fuse_extra;               // arrivals awaited beyond the grid's: 0 (> 0 only to make
                                     // the barrier time out on purpose, in tests)
-  uint32_t* fuse_ws;                // kFuseWsWords words, 8-byte aligned (fused_amax.cuh)
-  int32_t coop_launch;              // host side: 1 = cooperative launch (checks co-residency),
-                                    // 0 = programmatic dependent launch (fused only)
+  int32_t fuse_late;                // the last fuse_late CTAs start only once every rank has
+                                    // arrived (bounded): 0 (> 0 only in tests, so that the
+                                    // other CTAs take their ranks over)
+  uint32_t* fuse_ws;                // kFuseWsWords words, 4-byte aligned (fused_amax.cuh)
 };
 
 // Launch with programmatic dependent launch: the kernel may start before the previous kernel
@@ -118,6 +125,8 @@ struct QuantMode {
 };
 
 cudaError_t launch_quantize(const QuantMode& m, const QuantArgs& args, int grid, cudaStream_t s);
+// The single-launch amax's test hooks for the next launch (fuse_extra, fuse_late), taken once.
+void take_fuse_debug(QuantArgs& q);
 cudaError_t prepare_quantize_kernels();
 // The amax pass alone through the tile kernel (per segment; RHT amax when rht): atomic maxima
 // into args.amax_row / args.amax_col, which the caller zeroes.

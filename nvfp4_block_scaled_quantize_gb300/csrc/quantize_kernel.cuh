@@ -145,8 +145,8 @@ __device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int
   return true;
 }
 
-// FUSED: the amax is computed inside the launch (a.fused == 1; a cooperative launch of a
-// plain tensor). A template parameter, so that each path is compiled on its own.
+// FUSED: the amax is computed inside the launch (a.fused == 1; a plain tensor; fused_amax.cuh).
+// A template parameter, so that each path is compiled on its own.
 // AMAX_ONLY: the amax pass alone, through the same stage ring: per segment max |x| and, with
 // RHT, max |bf16(RHT)| over its zero-padded 16-row column blocks, atomically maxed into
 // a.amax_row / a.amax_col (zeroed by the caller); no codes. Instantiated with ROW and !COL (no
@@ -191,9 +191,26 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const bool plain = a.offsets == nullptr;
   int total = 0, n_local = 0;
 
-  // Load local tile i of this CTA into stage s.
-  auto issue = [&](int i, int s) {
-    const int tile = blockIdx.x + i * stride;
+  // Single-launch amax (fused_amax.cuh): the ranks this CTA computes the amax of, in order,
+  // each with the first slot of its amax round. Slots number the CTA's loads through the stage
+  // ring: slot k goes to stage k % kStages as that stage's load k / kStages. Rank r walks its
+  // tiles r, r + G, ... from the last to the first.
+  int32_t* held_rank = reinterpret_cast<int32_t*>(smem + kSmemHeld);
+  int32_t* held_first = held_rank + kMaxHeld;
+  // [0] ranks held, [1] the action after a wait (FuseWait), [2] the rank taken over
+  volatile int32_t* fctl = reinterpret_cast<volatile int32_t*>(smem + kSmemFuseCtl);
+  auto rank_tiles = [&](int r) -> int { return r < total ? (total - r + stride - 1) / stride : 0; };
+  auto tile_of_slot = [&](int k) -> int {
+    const int nh = fctl[0];
+    for (int h = 0; h < nh; h++) {
+      const int r = held_rank[h], n = rank_tiles(r), f = held_first[h];
+      if (k < f + n) return r + (n - 1 - (k - f)) * stride;
+    }
+    return -1;
+  };
+
+  // Load tile `tile` into stage s.
+  auto issue = [&](int tile, int s) {
     int lo = 0, hi = E;  // segment: largest e with seg_tile0[e] <= tile
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     tma_load_2d(smem + kSmemStages + s * kStageBytes, &a.tmap, c.n0, c.row0, &full[s]);
   };
   // The first kStages loads: the quantize phase's first tiles, or, with the single-launch
-  // amax, the amax phase's (it walks the local tiles from the last to the first, so that the
+  // amax, the amax phase's (its slots walk the tiles from the last to the first, so that the
   // quantize phase, walking forward, starts on the kStages tiles still in shared memory).
   auto first_loads = [&]() {
     prefetch_tensormap(&a.tmap);
@@ -227,7 +244,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       issued[s] = 0;
     }
     fence_barrier_init();
-    for (int k = 0; k < kStages && k < n_local; k++) issue(fused ? n_local - 1 - k : k, k);
+    for (int k = 0; k < kStages && k < n_local; k++)
+      issue(fused ? tile_of_slot(k) : (int)blockIdx.x + k * stride, k);
   };
 
   if (plain) {
@@ -241,6 +259,19 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       seg_col0[0] = 0;
       seg_tile0[0] = 0;
       seg_tile0[1] = total;
+      if (fused) {
+        // test hook: the last a.fuse_late CTAs hold back until every rank has arrived, so
+        // that the others must take their ranks over (bounded)
+        if (a.fuse_late > 0 && (int)blockIdx.x >= stride - a.fuse_late) {
+          const uint64_t t0 = global_ns();
+          while (ld_acquire(a.fuse_ws + kFuseArrived) < (uint32_t)(stride + a.fuse_extra) &&
+                 global_ns() - t0 < kBarrierLimitNs) {
+          }
+        }
+        fctl[0] = 1;
+        held_rank[0] = blockIdx.x;  // this CTA's own rank first
+        held_first[0] = 0;
+      }
       first_loads();
     }
     __syncthreads();
@@ -313,70 +344,104 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int rb = warp % kWarpsPerGroup;  // slab of the tile (rows 16 rb .. 16 rb + 15)
   const int gt = tid - g * 32 * kWarpsPerGroup;  // thread index inside the group
 
-  // ---- single-launch amax: stream the local tiles through the stage ring (last to first),
-  // reduce, fold into the workspace maxima, wait for every CTA's arrival ----
+  // ---- single-launch amax: rounds of amax slots, first this CTA's own rank, then any rank it
+  // takes over while waiting; fold the maxima into the workspace, count the rank as arrived,
+  // wait for every rank (fused_amax.cuh) ----
   float* fused_amax = reinterpret_cast<float*>(smem + kSmemFused) + 32;  // [0] row, [1] col
-  uint64_t fuse_e = 0u;  // thread 0: the workspace epoch at the start of this launch
+  int n_slots = n_local;  // amax slots of every round (the quantize phase walks them back)
+  uint32_t done_before = 0u;  // thread 0: the CTAs done with the workspace before this one
   if (fused) {
-    if (tid == 0) fuse_e = fuse_epoch(a.fuse_ws);
+    // claim the own rank (the result is needed only at the first arrival)
+    uint32_t own_before = 0u;
+    if (tid == 0) own_before = fuse_claim(a.fuse_ws, blockIdx.x);
     uint32_t m = 0u, mt = 0u;
     bool ok = true;
-    for (int k = g; k < n_local; k += kGroups) {
-      const int s = k % kStages, p = k / kStages;  // load p of stage s
-      const int i = n_local - 1 - k;
-      bool arrived = wait_issued(issued, s, p + 1);
-      arrived = arrived && mbar_wait_bounded(&full[s], (uint32_t)p & 1u, kWaitLimitNs);
-      if (!arrived || coords[s].tile != (int)blockIdx.x + i * stride) ok = false;
-      // rows and columns outside the tensor arrive as zeros: no masking for a maximum
-      uint4 v[16];
-      const uint32_t src = smem_u32(smem + kSmemStages + s * kStageBytes) +
-                           (16 * rb) * (kTileN * 2) + lane * 16;
+    int first = 0, round_end = n_local;
+    uint64_t t_wait = 0u;
+    volatile uint32_t* red = reinterpret_cast<volatile uint32_t*>(smem + kSmemFused);
+    while (true) {
+      for (int k = first + (g - first % kGroups + kGroups) % kGroups; k < round_end; k += kGroups) {
+        const int s = k % kStages, p = k / kStages;  // load p of stage s
+        bool arrived = wait_issued(issued, s, p + 1);
+        arrived = arrived && mbar_wait_bounded(&full[s], (uint32_t)p & 1u, kWaitLimitNs);
+        if (!arrived || coords[s].tile != tile_of_slot(k)) ok = false;
+        // rows and columns outside the tensor arrive as zeros: no masking for a maximum
+        uint4 v[16];
+        const uint32_t src = smem_u32(smem + kSmemStages + s * kStageBytes) +
+                             (16 * rb) * (kTileN * 2) + lane * 16;
 #pragma unroll
-      for (int r = 0; r < 16; r++) v[r] = lds128(src + r * (kTileN * 2));
-      named_bar_sync(1 + g, 32 * kWarpsPerGroup);
-      if (gt == 0 && k + kStages < n_local) {
-        fence_proxy_async();
-        issue(n_local - 1 - (k + kStages), s);
-      }
-      // max.xorsign.abs: the magnitude is exact, the sign bit is cleared at the end (inputs
-      // are finite, so no NaN takes part)
+        for (int r = 0; r < 16; r++) v[r] = lds128(src + r * (kTileN * 2));
+        named_bar_sync(1 + g, 32 * kWarpsPerGroup);
+        if (gt == 0 && k + kStages < round_end) {
+          fence_proxy_async();
+          issue(tile_of_slot(k + kStages), s);
+        }
+        // max.xorsign.abs: the magnitude is exact, the sign bit is cleared at the end (inputs
+        // are finite, so no NaN takes part)
 #pragma unroll
-      for (int r = 0; r < 16; r += 2)
-        m = hmax_abs2(m, hmax_abs2(hmax_abs2(hmax_abs2(v[r].x, v[r].y), hmax_abs2(v[r].z, v[r].w)),
-                                   hmax_abs2(hmax_abs2(v[r + 1].x, v[r + 1].y),
-                                             hmax_abs2(v[r + 1].z, v[r + 1].w))));
-      if (COL && RHT) {
+        for (int r = 0; r < 16; r += 2)
+          m = hmax_abs2(m, hmax_abs2(hmax_abs2(hmax_abs2(v[r].x, v[r].y), hmax_abs2(v[r].z, v[r].w)),
+                                     hmax_abs2(hmax_abs2(v[r + 1].x, v[r + 1].y),
+                                               hmax_abs2(v[r + 1].z, v[r + 1].w))));
+        if (COL && RHT) {
 #pragma unroll
-        for (int c4 = 0; c4 < 4; c4++) {
-          uint32_t w[16];
+          for (int c4 = 0; c4 < 4; c4++) {
+            uint32_t w[16];
 #pragma unroll
-          for (int r = 0; r < 16; r++) w[r] = comp(v[r], c4);
-          mt = vmax2(mt, rht16_pair_absmax(w, a.sign_mask));  // both sign-cleared
+            for (int r = 0; r < 16; r++) w[r] = comp(v[r], c4);
+            mt = vmax2(mt, rht16_pair_absmax(w, a.sign_mask));  // both sign-cleared
+          }
         }
       }
-    }
-    if (!ok) {
-      flags[3] = 1;  // this CTA stores nothing (below); the others still need its partials
-      if (lane == 0) atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
-    }
-    m &= 0x7FFF7FFFu;
-    volatile uint32_t* red = reinterpret_cast<volatile uint32_t*>(smem + kSmemFused);
-    uint32_t mr = cta_max(max(m & 0xFFFFu, m >> 16), red);
-    uint32_t mc = mr;
-    if (COL && RHT) mc = cta_max(max(mt & 0xFFFFu, mt >> 16), red);
-    if (tid == 0) {
-      fuse_arrive(a.fuse_ws, fuse_e, mr, mc);
-      uint32_t pr = 0u, pc = 0u;
-      if (!fuse_wait(a.fuse_ws, fuse_e, gridDim.x + (uint32_t)a.fuse_extra, pr, pc)) {
-        flags[3] = 1;
-        atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
+      m &= 0x7FFF7FFFu;
+      // the CTA's maxima over every round so far (cta_max's barriers also end the round: every
+      // group has read its last slot)
+      const uint32_t mr = cta_max(max(m & 0xFFFFu, m >> 16), red);
+      const uint32_t mc = (COL && RHT) ? cta_max(max(mt & 0xFFFFu, mt >> 16), red) : mr;
+      if (tid == 0) {
+        // the first round is the own rank: it counts only if the claim at the start won it
+        // (otherwise another CTA took it over and counts it)
+        const bool own_taken = ((own_before >> (blockIdx.x & 31)) & 1u) != 0u;
+        fuse_arrive(a.fuse_ws, mr, mc, (first == 0 && own_taken) ? 0u : 1u);
+        if (first == 0) t_wait = global_ns();
+        uint32_t pr = 0u, pc = 0u;
+        int r = -1;
+        const FuseWait w = fuse_wait(a.fuse_ws, (uint32_t)(stride + a.fuse_extra), stride, t_wait,
+                                     fctl[0] < kMaxHeld, pr, pc, r);
+        fctl[1] = w;
+        if (w == kFuseSteal) {
+          // take rank r over: its amax round follows in the ring (every stage is free: the
+          // round's last slots were read before cta_max's barriers)
+          const int h = fctl[0];
+          held_rank[h] = r;
+          held_first[h] = round_end;
+          fctl[0] = h + 1;
+          fctl[2] = r;
+          fence_proxy_async();
+          for (int k = round_end; k < round_end + kStages && k < round_end + rank_tiles(r); k++)
+            issue(tile_of_slot(k), k % kStages);
+        } else {
+          if (w == kFuseTimedOut) {
+            flags[3] = 1;
+            atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
+          }
+          done_before = fuse_done(a.fuse_ws);
+          // past the wait this CTA no longer uses the workspace: the next kernel in the stream
+          // may start on the SMs that finished CTAs leave
+          pdl_allow_next();
+          fused_amax[0] = __uint_as_float(pr << 16);
+          fused_amax[1] = __uint_as_float(pc << 16);
+        }
       }
-      if (blockIdx.x == 0) fuse_advance(a.fuse_ws, fuse_e);
-      // past the barrier this CTA no longer uses the workspace: the next kernel in the
-      // stream may start on the SMs that finished CTAs leave
-      pdl_allow_next();
-      fused_amax[0] = __uint_as_float(pr << 16);
-      fused_amax[1] = __uint_as_float(pc << 16);
+      __syncthreads();
+      if (fctl[1] != kFuseSteal) break;
+      first = round_end;
+      round_end += rank_tiles(fctl[2]);
+    }
+    n_slots = round_end;
+    if (!ok) {
+      flags[3] = 1;  // this CTA stores nothing (below); the others still need its maxima
+      if (lane == 0) atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
     }
     __syncthreads();
     if (flags[3]) flags[0] = flags[1] = flags[2] = 1;  // every group leaves without storing
@@ -494,18 +559,25 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   bool have_prev = false;
   int buf = 0;
 
-  if (!AMAX_ONLY && plain && n_local > g) set_segment(0);  // overlaps the first loads (or follows the amax)
+  // Quantize position i: the tile of local index i; after the single-launch amax, the tile of
+  // amax slot n_slots - 1 - i (the amax rounds walked back, so that the first kStages
+  // positions are the tiles still in the stages).
+  auto position_tile = [&](int i) -> int {
+    return fused ? tile_of_slot(n_slots - 1 - i) : (int)blockIdx.x + i * stride;
+  };
+  if (!AMAX_ONLY && plain && n_slots > g) set_segment(0);  // overlaps the first loads (or follows the amax)
 
-  for (int i = g; i < n_local; i += kGroups) {
-    const int tile = blockIdx.x + i * stride;
-    // Stage and load number of local tile i. Plain: stage i % kStages, its load i / kStages.
-    // After the single-launch amax phase (loads a_s into stage s, last tiles first) the first
-    // kStages tiles are still in the stages; tile i >= kStages goes where tile i - kStages was.
+  for (int i = g; i < n_slots; i += kGroups) {
+    const int tile = position_tile(i);
+    // Stage and load number of position i. Plain: stage i % kStages, its load i / kStages.
+    // After the single-launch amax phase (a_s loads into stage s, slot k in stage k % kStages)
+    // the first kStages positions are still in the stages; position i >= kStages goes where
+    // position i - kStages was.
     int s, p;
     bool resident = false;
     if (fused) {
-      s = (n_local - 1 - i) % kStages;
-      const int a_s = n_local > s ? (n_local - 1 - s) / kStages + 1 : 0;
+      s = (n_slots - 1 - i) % kStages;
+      const int a_s = n_slots > s ? (n_slots - 1 - s) / kStages + 1 : 0;
       p = a_s + i / kStages - 1;
       resident = i < kStages;
     } else {
@@ -542,9 +614,9 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     // written out, and the group's abort flag is settled.
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     if (flags[g]) break;
-    if (gt == 0 && i + kStages < n_local) {
+    if (gt == 0 && i + kStages < n_slots) {
       fence_proxy_async();
-      issue(i + kStages, s);
+      issue(position_tile(i + kStages), s);
     }
 
     if constexpr (AMAX_ONLY) {
@@ -803,35 +875,18 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       const int loads = issued[s];
       if (loads > 0) mbar_wait_bounded(&full[s], (uint32_t)(loads - 1) & 1u, kWaitLimitNs);
     }
+    if (fused) fuse_reset_if_last(a.fuse_ws, done_before, stride);
   }
 }
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
 cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
   if (args.fused) {
-    // Every CTA waits for all the others, so all must be resident at once (one per SM). A
-    // cooperative launch checks that; the host uses it for a device's first single-launch
-    // call. Later calls use programmatic dependent launch instead (the two do not combine):
-    // their CTAs may start on SMs that the previous single-launch kernel's CTAs leave, and
-    // wait for that kernel at entry.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kQuantThreads);
-    cfg.dynamicSmemBytes = kQuantSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    if (args.coop_launch) {
-      attr[0].id = cudaLaunchAttributeCooperative;
-      attr[0].val.cooperative = 1;
-    } else {
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(
-        &cfg, quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT>,
-        args);
+    // No CTA waits for another to start (fused_amax.cuh), so the CTAs need not be resident at
+    // once: a plain launch with programmatic dependent launch, whose CTAs may start on the SMs
+    // that the previous kernel's CTAs leave and wait for that kernel at entry.
+    return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT>,
+                      dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
   }
   return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT>,
                     dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);

@@ -3,8 +3,10 @@
 // real-time path that must never reach cudaMalloc (which can synchronize the device), or a
 // host that hands this library a fixed memory budget. The regular entry points allocate a
 // small per-device workspace on their first call; this one keeps its scratch (a status word,
-// the CTAs' counts, the launch-tagged maxima words and the epoch) in a file-scope device array
+// the single-launch amax's counts, maxima and claim bits) in a file-scope device array
 // instead, so it calls no cudaMalloc, cudaFree or other allocating routine.
+// nvfp4_noalloc_get_status reads (and clears) the array's status word, also without
+// allocating.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -22,8 +24,8 @@ namespace nvfp4 {
 namespace {
 
 // Scratch of every nvfp4_quantize_noalloc call on a device (64 words, 256 bytes): word 0 the
-// device status word, words 4 .. 4 + kFuseWsWords the counts, maxima and epoch of the
-// single-launch amax. Zero when the library is loaded and kept until exit.
+// device status word, words 4 .. 4 + kFuseWsWords the counts, maxima and claim bits of the
+// single-launch amax (fused_amax.cuh). Zero when the library is loaded and kept until exit.
 constexpr int kScratchStatus = 0;
 constexpr int kScratchFuse = 4;
 constexpr int kScratchWords = 64;
@@ -36,9 +38,6 @@ struct NoAllocDevice {
   bool ready = false;
   int sm_count = 0;
   uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-  // the largest grid of a cooperative launch that has succeeded here: launches with a grid
-  // no larger use programmatic dependent launch (quantize_kernel.cuh, launch)
-  std::atomic<int> coop_checked_grid{0};
 };
 
 std::mutex g_mutex;
@@ -120,7 +119,8 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   if (st != NVFP4_OK) return st;
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < d->sm_count ? tiles : d->sm_count);
-  if (grid > kFuseMaxCtas) return NVFP4_ERR_UNSUPPORTED;  // partials would not fit the array
+  // one claim bit per CTA in the array (GB300 launches one CTA per SM, 152)
+  if (grid > kFuseMaxCtas) return NVFP4_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   QuantArgs q;
@@ -145,20 +145,37 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   q.fused = 1;
   q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
   q.fuse_ws = d->scratch + kScratchFuse;
-  q.fuse_extra = 0;
-  // the barrier's counts and epoch live in the scratch (zero-initialised; CTA 0 readies them for
-  // the next launch), so nothing is cleared before the launch and it can be captured in a graph
+  take_fuse_debug(q);  // the test hooks of the single-launch amax apply here too
+  // the single-launch amax keeps its counts in the array (zero when loaded; the last CTA to
+  // finish with them readies them for the next launch), so nothing is cleared before a launch
   const QuantMode mode{row, col, rht, two_d, cfg->round_row == NVFP4_ROUND_SR,
                        cfg->round_col == NVFP4_ROUND_SR, q.fast && rht};
-  q.coop_launch = grid > d->coop_checked_grid.load() ? 1 : 0;
   if (launch_quantize(mode, q, grid, s) != cudaSuccess) {
     (void)cudaGetLastError();  // leave no error behind for the caller's next check
     return NVFP4_ERR_CUDA;
   }
-  if (q.coop_launch) {
-    int cur = d->coop_checked_grid.load();
-    while (cur < grid && !d->coop_checked_grid.compare_exchange_weak(cur, grid)) {
-    }
+  return NVFP4_OK;
+}
+
+NVFP4_EXPORT nvfp4_status nvfp4_noalloc_get_status(void* stream, uint32_t* device_status) {
+  if (device_status == nullptr) return NVFP4_ERR_INVALID_ARG;
+  NoAllocDevice* d = nullptr;
+  nvfp4_status st = setup(&d);
+  if (st != NVFP4_OK) return st;
+  // the status word is read and cleared by synchronous copies to and from the array itself:
+  // nothing is allocated
+  const uint32_t zero = 0u;
+  uint32_t v = 0u;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&v, g_noalloc_scratch, 4, 4 * kScratchStatus, cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemcpyToSymbol(g_noalloc_scratch, &zero, 4, 4 * kScratchStatus, cudaMemcpyHostToDevice) !=
+          cudaSuccess) {
+    (void)cudaGetLastError();
+    return NVFP4_ERR_CUDA;
   }
+  *device_status = v;
+  if (v & NVFP4_DEVICE_TIMEOUT) return NVFP4_ERR_TIMEOUT;
+  if (v) return NVFP4_ERR_DEVICE_STATUS;
   return NVFP4_OK;
 }

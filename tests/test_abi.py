@@ -81,14 +81,17 @@ def test_grouped_and_dequant_argument_checks(L):
     cfg = _cfg(columnwise=1)
 
     def grouped(T, H, offs, E, cap, c=cfg):
-        return L.nvfp4_quantize_grouped(p(FAKE), T, H, offs, E, cap, ctypes.byref(c), p(FAKE),
-                                        p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None)
+        return L.nvfp4_quantize_grouped(p(FAKE), T, H, offs, E, cap, ctypes.byref(c), None, None,
+                                        p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), None)
     assert grouped(64, 32, p(FAKE), 0, 64) == 1     # no experts
     assert grouped(64, 32, p(FAKE), 257, 64) == 1   # too many experts
     assert grouped(64, 32, None, 2, 64) == 1        # no offsets
     assert grouped(64, 24, p(FAKE), 2, 64) == 2     # H % 16
     assert grouped(64, 32, p(FAKE), 2, 40) == 2     # capacity % 16
     assert grouped(64, 32, p(FAKE + 2), 2, 64) == 3
+    assert L.nvfp4_quantize_grouped(p(FAKE), 64, 32, p(FAKE), 2, 64, ctypes.byref(cfg), None,
+                                    p(FAKE + 2), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                                    p(FAKE), None) == 3   # misaligned supplied amax
     # grouped 2D has no RHT or SR, and no grouped call takes the single-launch amax
     assert grouped(64, 32, p(FAKE), 2, 64, _cfg(columnwise=1, block2d=1, rht_col=1)) == 4
     assert grouped(64, 32, p(FAKE), 2, 64, _cfg(columnwise=1, block2d=1, round_col=1)) == 4

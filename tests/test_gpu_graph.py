@@ -5,9 +5,13 @@ match the oracle on that data bit for bit. The data's amax falls from replay to 
 barrier that kept its maxima from an earlier replay (or counted arrivals against a target fixed
 at capture) would show up as a wrong global scale.
 
-The timeout test asks the next single-launch call to wait for one CTA more than its grid has:
-every CTA gives up after its bounded wait, records NVFP4_DEVICE_TIMEOUT and exits, and the call
-after it runs normally on the same workspace. Nothing faults or hangs: the wait has a limit.
+The timeout test asks the next single-launch call to wait for one share more than its grid
+has: every CTA gives up after its bounded wait, records NVFP4_DEVICE_TIMEOUT and exits, and the
+call after it runs normally on the same workspace. Nothing faults or hangs: the wait has a
+limit. The take-over tests hold the last CTAs of a launch back (a test hook, bounded) until
+every share has arrived: the other CTAs must take their shares over, the outputs must be the
+oracle's, and a launch whose held-back CTAs start only after the others have given up must
+leave the workspace ready for the next call.
 The launch-failure test has the next call launch an empty grid, which the runtime rejects
 before anything reaches the GPU: the call reports NVFP4_ERR_CUDA, leaves no error behind for
 the next CUDA call, and the call after it is correct."""
@@ -142,7 +146,7 @@ def test_barrier_wait_runs_out_then_next_call_is_correct(shape):
     status, bits = api.nvfp4_get_status(dev)  # waits for the launch (about 2 s)
     assert _lib.STATUS_NAMES[status] == "NVFP4_ERR_TIMEOUT" and bits & _lib.DEVICE_TIMEOUT, \
         (status, bits)
-    # the hook was consumed and CTA 0 readied the barrier: a normal call again
+    # the hook was consumed and the last CTA readied the counts: a normal call again
     out = api.nvfp4_quantize(x.to(dev), **cfg)
     torch.cuda.synchronize()
     _same(out, oracle.quantize(x, _oracle_cfg(cfg)), "after timeout")
@@ -198,3 +202,62 @@ def test_back_to_back_single_launch_calls(mode):
         _same(o, r, "%s call %d" % (mode, k))
     _same(shared, refs[-1], "%s reused outputs" % mode)
     assert api.nvfp4_get_status(dev) == (0, 0)
+
+
+TAKEOVER_MODES = ["fused_rowcol", "fused_rht_sr", "fused_2d"]
+
+
+@pytest.mark.parametrize("mode", TAKEOVER_MODES)
+@pytest.mark.parametrize("late", [1, 40, 120])
+def test_held_back_ctas_have_their_shares_taken_over(mode, late):
+    """The last `late` CTAs of a full grid (one per SM) start their shares only after every
+    share has arrived, so the other CTAs take them over; the held-back CTAs then find their
+    shares taken and quantize them again (the same bytes)."""
+    dev = _cuda()
+    M, N = 4096, 4096
+    cfg = MODES[mode]
+    x = workloads.normal_with_outliers(M, N, seed=500 + late, fraction=0.01, gain=25.0)
+    xd = x.to(dev)
+    api.nvfp4_quantize(xd, **cfg)
+    torch.cuda.synchronize()
+    api.nvfp4_debug_fused_takeovers(dev)  # clear the count
+    api.nvfp4_debug_fused_late_ctas(late)
+    out = api.nvfp4_quantize(xd, **cfg)
+    torch.cuda.synchronize()
+    assert api.nvfp4_get_status(dev) == (0, 0)
+    taken = api.nvfp4_debug_fused_takeovers(dev)
+    assert taken == late, (taken, late)
+    ref = oracle.quantize(x, _oracle_cfg(cfg))
+    _same(out, ref, "%s with %d held-back CTAs" % (mode, late))
+    # and the next call, on the counts the last CTA readied
+    out = api.nvfp4_quantize(xd, **cfg)
+    torch.cuda.synchronize()
+    _same(out, ref, "%s after the take-over" % mode)
+    assert api.nvfp4_get_status(dev) == (0, 0)
+    assert api.nvfp4_debug_fused_takeovers(dev) == 0
+
+
+def test_ctas_starting_after_a_timeout_leave_the_next_call_correct():
+    """A launch that times out (one share more awaited than exists) while its last CTAs are
+    held back until that count is reached (which never happens: they give up their hold after
+    the bounded wait, about 2 s, and only then claim their shares, long after the others gave
+    up): it reports NVFP4_DEVICE_TIMEOUT, and the next call must match the oracle bit for bit
+    and report nothing (no count or maximum of the timed-out launch survives)."""
+    dev = _cuda()
+    M, N = 4096, 4096
+    cfg = MODES["fused_rowcol"]
+    xs = [workloads.normal_with_outliers(M, N, seed=600 + k, fraction=0.01, gain=g)
+          for k, g in enumerate((80.0, 3.0))]
+    api.nvfp4_quantize(xs[0].to(dev), **cfg)
+    torch.cuda.synchronize()
+    api.nvfp4_debug_fused_extra_arrivals(1)
+    api.nvfp4_debug_fused_late_ctas(20)
+    api.nvfp4_quantize(xs[0].to(dev), **cfg)  # larger amax than the next call's data
+    status, bits = api.nvfp4_get_status(dev)  # about 4 s: the hold, then the wait
+    assert _lib.STATUS_NAMES[status] == "NVFP4_ERR_TIMEOUT" and bits & _lib.DEVICE_TIMEOUT
+    api.nvfp4_debug_fused_takeovers(dev)
+    out = api.nvfp4_quantize(xs[1].to(dev), **cfg)
+    torch.cuda.synchronize()
+    _same(out, oracle.quantize(xs[1], _oracle_cfg(cfg)), "after a timeout with late CTAs")
+    assert api.nvfp4_get_status(dev) == (0, 0)
+    assert api.nvfp4_debug_fused_takeovers(dev) == 0

@@ -307,6 +307,44 @@ def test_grouped_matches_oracle(case, mode):
     assert_same(out, ref, "%s/%s" % (name, mode))
 
 
+@pytest.mark.parametrize("case", GROUPED_CASES[1:3], ids=lambda c: c[0])
+@pytest.mark.parametrize("mode", ["rn", "rht_sr", "col_only_rht", "2d_rowcol", "2d_col"])
+def test_grouped_with_supplied_amax_matches_oracle(case, mode):
+    """Per-expert maxima from nvfp4_amax_grouped passed in (no amax pass inside the call):
+    every output equals the oracle's, as with the maxima computed inside."""
+    name, T, H, offs = case
+    cfg = {
+        "rn": dict(rowwise=True, columnwise=True),
+        "rht_sr": dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x6A5C,
+                       round_col="sr", seed=5, offset=2),
+        "col_only_rht": dict(rowwise=False, columnwise=True, rht_col=True, sign_mask=0xFFFF),
+        "2d_rowcol": dict(rowwise=True, columnwise=True, block2d=True),
+        "2d_col": dict(rowwise=False, columnwise=True, block2d=True),
+    }[mode]
+    dev = _cuda()
+    x = workloads.normal_with_outliers(T, H, seed=T * 3 + H, fraction=0.01, gain=30.0)
+    off = torch.from_numpy(np.asarray(offs, dtype=np.int32)).to(dev)
+    xd = x.to(dev)
+    a_row, a_col = api.nvfp4_amax_grouped(xd, off, rht_col=cfg.get("rht_col", False),
+                                          sign_mask=cfg.get("sign_mask", 0))
+    cap = oracle.padded_capacity(offs)
+    _, ref = run_grouped_both(x, offs, **cfg)
+    out = api.nvfp4_quantize_grouped(xd, off, col_capacity=cap, amax_row=a_row,
+                                     amax_col=None if cfg.get("block2d") else a_col, **cfg)
+    torch.cuda.synchronize()
+    # regions the call does not write hold whatever the allocation held: compare written parts
+    rows = int(offs[-1])
+    for k in list(ref):
+        if k.startswith("row_") and k != "row_gscale":
+            ref[k] = ref[k][:rows]
+            out[k] = out[k][:rows]
+        if k.startswith("col_") and k != "col_gscale":
+            w = cap // 2 if k == "col_codes" else cap // 16
+            ref[k] = ref[k][:, :w]
+            out[k] = out[k][:, :w]
+    assert_same(out, ref, "%s/%s with supplied maxima" % (name, mode))
+
+
 def test_grouped_extra_capacity_left_untouched():
     x = workloads.normal(100, 48, 1.0, seed=61)
     offs = [30, 30, 64, 99]

@@ -7,6 +7,11 @@ Called directly through the C ABI (ctypes) and compared with the regular nvfp4_q
 same input, bit for bit (the tolerance of every parity test here), twice in a row so that the
 second call runs on the scratch the first one left behind. Kept in a file of its own that
 pytest collects last; it passes alone in a fresh process and after the other tests.
+
+A call whose bounded wait gives up (forced with the test hook that makes the wait expect one
+share more than exists) must be visible through nvfp4_noalloc_get_status, which reads the
+array's own status word without allocating; the next call must be correct again. A call whose
+last CTAs are held back (another test hook) has their shares taken over and is still correct.
 """
 import ctypes
 
@@ -78,3 +83,59 @@ def test_noalloc_rejects_bad_arguments_before_launching():
                                     None) == 2          # N % 16
     assert L.nvfp4_quantize_noalloc(ctypes.c_void_p(0x10008), 32, 32, ctypes.byref(cfg), p, p,
                                     p, None, None, None, None) == 3  # misaligned input
+
+
+def _noalloc_status():
+    L = _lib.load()
+    bits = ctypes.c_uint32(0)
+    st = L.nvfp4_noalloc_get_status(
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def _same_as_regular(x, kw, what):
+    cfg = api.make_config(**kw)
+    M, N = x.shape
+    ref = api.nvfp4_quantize(x, **kw)
+    out = api.alloc_outputs(M, N, x.device, kw.get("rowwise", True), kw.get("columnwise", False))
+    status = _noalloc(x, out, cfg)
+    assert status == 0, _lib.load().nvfp4_status_string(status).decode()
+    torch.cuda.synchronize()
+    for k in KEYS:
+        if k in ref:
+            a, b = out[k].cpu().numpy(), ref[k].cpu().numpy()
+            if a.dtype == np.float32:
+                a, b = a.view(np.uint32), b.view(np.uint32)
+            assert np.array_equal(a, b), "%s: %s differs" % (what, k)
+
+
+def test_noalloc_timeout_is_reported_by_its_status_query():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda")
+    kw = dict(rowwise=True, columnwise=True)
+    x = workloads.normal_with_outliers(2048, 4096, seed=31, fraction=0.002, gain=40.0).to(dev)
+    _same_as_regular(x, kw, "before")
+    assert _noalloc_status() == (0, 0)
+    api.nvfp4_debug_fused_extra_arrivals(1)  # the next single-launch call cannot complete
+    out = api.alloc_outputs(2048, 4096, dev, True, True)
+    assert _noalloc(x, out, api.make_config(**kw)) == 0  # the launch itself succeeds
+    status, bits = _noalloc_status()  # waits for the call (about 2 s)
+    assert _lib.STATUS_NAMES[status] == "NVFP4_ERR_TIMEOUT" and bits & _lib.DEVICE_TIMEOUT
+    assert _noalloc_status() == (0, 0)  # read and cleared
+    assert api.nvfp4_get_status(dev) == (0, 0)  # the regular workspace saw nothing
+    _same_as_regular(x, kw, "after the timeout")
+    assert _noalloc_status() == (0, 0)
+
+
+def test_noalloc_held_back_ctas_are_taken_over():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda")
+    kw = dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x0FF0, round_col="sr",
+              seed=5)
+    x = workloads.normal_with_outliers(4096, 4096, seed=32, fraction=0.002, gain=40.0).to(dev)
+    _same_as_regular(x, kw, "before")
+    api.nvfp4_debug_fused_late_ctas(30)
+    _same_as_regular(x, kw, "with 30 held-back CTAs")
+    assert _noalloc_status() == (0, 0)
