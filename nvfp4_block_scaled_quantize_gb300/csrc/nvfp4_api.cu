@@ -104,6 +104,22 @@ nvfp4_status make_tensor_map(CUtensorMap* map, const void* x, int64_t rows, int6
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// TMA descriptor of the columnwise codes [cols][col_ld / 2] bytes as a 3D tensor
+// {col_ld / 2, cols / 8, 8} (column 8y + z), box {kTileM / 2, kTileN / 8, 8} with the 32-byte
+// swizzle: one quantize tile's codes. Returns false (thread stores are used) when the row pitch
+// is not a multiple of 16 bytes or cols not of 8.
+bool make_col_codes_map(CUtensorMap* map, uint8_t* col_codes, int64_t cols, int64_t col_ld) {
+  const int64_t pitch = col_ld / 2;
+  if (col_codes == nullptr || pitch % 16 != 0 || cols % 8 != 0 || cols == 0 || pitch == 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)pitch, (cuuint64_t)(cols / 8), 8};
+  cuuint64_t strides[2] = {(cuuint64_t)(8 * pitch), (cuuint64_t)pitch};
+  cuuint32_t box[3] = {(cuuint32_t)(kTileM / 2), (cuuint32_t)(kTileN / 8), 8};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, col_codes, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 nvfp4_status check_config(const nvfp4_config* cfg) {
   if (cfg == nullptr) return NVFP4_ERR_INVALID_ARG;
   if (cfg->fast_math != 0 && cfg->fast_math != 1) return NVFP4_ERR_INVALID_ARG;
@@ -189,7 +205,7 @@ nvfp4_status amax_tiles(const DeviceState* ds, const void* x, int64_t rows, int6
   nvfp4_status st = make_tensor_map(&q.tmap, x, rows, cols);
   if (st != NVFP4_OK) return st;
   q.x = x; q.rows = rows; q.cols = cols; q.offsets = offsets; q.segments = segments;
-  q.sign_mask = sign_mask;
+  set_rht_flips(q, sign_mask);
   q.amax_row = amax_row; q.amax_col = amax_col;
   q.amax_row_stride = stride; q.amax_col_stride = stride;
   q.status = ds->workspace;
@@ -330,12 +346,13 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   if ((st = make_tensor_map(&q.tmap, x, M, N)) != NVFP4_OK) return st;
   q.rows = M; q.cols = N; q.offsets = nullptr; q.segments = 1;
   const int sr_row = cfg->round_row == NVFP4_ROUND_SR, sr_col = cfg->round_col == NVFP4_ROUND_SR;
-  q.sign_mask = cfg->rht_sign_mask; q.col_ld = M;
+  set_rht_flips(q, cfg->rht_sign_mask); q.col_ld = M;
   q.amax_row = amax_row ? amax_row : row_amax_slot;
   q.amax_col = amax_col ? amax_col : col_gscale;
   q.amax_row_stride = 2; q.amax_col_stride = 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
+  q.col_tma = col && make_col_codes_map(&q.tmap_colc, col_codes, q.cols, q.col_ld) ? 1 : 0;
   q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
   q.x = x;
   q.fused = fused ? 1 : 0;
@@ -412,12 +429,13 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   if ((st = make_tensor_map(&q.tmap, x, T, H)) != NVFP4_OK) return st;
   q.rows = T; q.cols = H; q.offsets = offsets; q.segments = E;
   const int sr_row = cfg->round_row == NVFP4_ROUND_SR, sr_col = cfg->round_col == NVFP4_ROUND_SR;
-  q.sign_mask = cfg->rht_sign_mask; q.col_ld = col ? col_capacity : 0;
+  set_rht_flips(q, cfg->rht_sign_mask); q.col_ld = col ? col_capacity : 0;
   q.amax_row = amax_row ? amax_row : ((row || two_d) ? row_slot : nullptr);
   q.amax_col = amax_col ? amax_col : col_gscale;
   q.amax_row_stride = amax_row ? 1 : 2; q.amax_col_stride = amax_col ? 1 : 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
+  q.col_tma = col && make_col_codes_map(&q.tmap_colc, col_codes, q.cols, q.col_ld) ? 1 : 0;
   q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset; q.status = ds->workspace;
   q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
   const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};

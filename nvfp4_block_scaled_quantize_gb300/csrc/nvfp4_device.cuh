@@ -80,6 +80,12 @@ __device__ __forceinline__ uint32_t hmax_abs2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) {
   return f2_pack(bf16_lo(w), bf16_hi(w));
 }
+// A packed BF16 pair widened to binary32 with the sign of both halves flipped when f (0 or
+// 0x80000000) is set: the low half by one multiply-add (w * 2^16 + f, the addition of bit 31
+// being its flip), the high half by one three-input logic operation.
+__device__ __forceinline__ uint64_t f2_from_bf16x2_flip(uint32_t w, uint32_t f) {
+  return f2_pack(__uint_as_float(w * 65536u + f), __uint_as_float((w & 0xFFFF0000u) ^ f));
+}
 
 // ------------------------------------------------------------------------------------------
 // Scales
@@ -142,13 +148,10 @@ __device__ __forceinline__ float element_multiplier(float s, float s_dec) {
 
 // rht16_pair without the BF16 round-through (the fast-math variant): x[i] receives the FP32
 // pair 0.25 * (H16 (d . v))_i of the two columns.
-__device__ __forceinline__ void rht16_pair_f32(const uint32_t (&w)[16], uint32_t sign_mask,
+__device__ __forceinline__ void rht16_pair_f32(const uint32_t (&w)[16], const uint32_t (&flip)[16],
                                                uint64_t (&x)[16]) {
 #pragma unroll
-  for (int i = 0; i < 16; i++) {
-    uint32_t flip = ((sign_mask >> i) & 1u) ? 0x80008000u : 0u;
-    x[i] = f2_from_bf16x2(w[i] ^ flip);
-  }
+  for (int i = 0; i < 16; i++) x[i] = f2_from_bf16x2_flip(w[i], flip[i]);
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
@@ -179,13 +182,10 @@ __device__ __forceinline__ float element_multiplier_fast(float s, float s_dec) {
 // and rounding to BF16 are both monotone, so the maximum of the rounded outputs is the rounded
 // maximum of the unrounded ones: the maximum is taken in FP32 straight after the last
 // butterfly stage, and only it is scaled and rounded.
-__device__ __forceinline__ uint32_t rht16_pair_absmax(const uint32_t (&w)[16], uint32_t sign_mask) {
+__device__ __forceinline__ uint32_t rht16_pair_absmax(const uint32_t (&w)[16], const uint32_t (&flip)[16]) {
   uint64_t x[16];
 #pragma unroll
-  for (int i = 0; i < 16; i++) {
-    uint32_t flip = ((sign_mask >> i) & 1u) ? 0x80008000u : 0u;
-    x[i] = f2_from_bf16x2(w[i] ^ flip);
-  }
+  for (int i = 0; i < 16; i++) x[i] = f2_from_bf16x2_flip(w[i], flip[i]);
 #pragma unroll
   for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
@@ -321,16 +321,14 @@ __device__ __forceinline__ uint4 block_random_rk(const uint32_t (&k)[2][10], uin
 // items 2 and 5; "Fast math": an FP32 accumulator rounded through BF16 in exact mode).
 // w[i] holds rows i of the two columns as a BF16 pair. In place: w[i] <- bf16(0.25 * (H16 (d .
 // v))_i) for each column, H16 the natural-order Sylvester matrix computed by butterflies in
-// stages 1, 2, 4, 8 ((a, b) -> (a + b, a - b), a the lower index), d_i = -1 where bit i of
-// sign_mask is set.
+// stages 1, 2, 4, 8 ((a, b) -> (a + b, a - b), a the lower index), d_i = -1 where flip[i] is
+// 0x80000000 (flip[i] is 0 or that word: the sign vector as the kernels' parameters hold it, so
+// that the sign flips cost nothing beyond the widening to binary32).
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ void rht16_pair(uint32_t (&w)[16], uint32_t sign_mask) {
+__device__ __forceinline__ void rht16_pair(uint32_t (&w)[16], const uint32_t (&flip)[16]) {
   uint64_t x[16];
 #pragma unroll
-  for (int i = 0; i < 16; i++) {
-    uint32_t flip = ((sign_mask >> i) & 1u) ? 0x80008000u : 0u;
-    x[i] = f2_from_bf16x2(w[i] ^ flip);
-  }
+  for (int i = 0; i < 16; i++) x[i] = f2_from_bf16x2_flip(w[i], flip[i]);
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
@@ -441,6 +439,20 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tensor_m
       "l"(tensor_map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+
+// 3D tiled TMA store of the box at (x, y, z) from shared memory (bulk async group); the
+// parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const void* tensor_map, const void* smem_src, int32_t x,
+                                             int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(tensor_map), "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the bulk stores committed by this thread have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until they have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const void* tensor_map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tensor_map) : "memory");

@@ -58,11 +58,15 @@ constexpr int kFuseStatsWord = 4;  // ranks taken over from another CTA (statist
 // a plain tensor, one per expert for the grouped case).
 struct QuantArgs {
   CUtensorMap tmap;                 // x as BF16 [rows][cols], box {kTileN, kTileM}
+  CUtensorMap tmap_colc;            // col_codes as bytes {col_ld / 2, cols / 8, 8} (column 8y + z),
+                                    // box {kTileM / 2, kTileN / 8, 8}, 32-byte swizzle
+  int32_t col_tma;                  // 1: whole tiles' columnwise codes leave by TMA (tmap_colc)
   const void* x;                    // the same tensor, for the fused amax phase
   int64_t rows, cols;
   const int32_t* offsets;           // cumulative segment ends, or nullptr: one segment
   int32_t segments;
   uint32_t sign_mask;
+  uint32_t rht_flip[16];            // 0x80000000 where bit i of sign_mask is set (set_rht_flips)
   int64_t col_ld;                   // columnwise output row length (elements)
   const float* amax_row;            // amax of segment e at amax_row[e * amax_row_stride]
   const float* amax_col;
@@ -116,6 +120,13 @@ inline void set_philox_keys(QuantArgs& a, uint64_t seed) {
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
+}
+
+// The RHT's sign flips as words (the sign bit of a binary32), so that the kernels take them
+// from their parameters.
+inline void set_rht_flips(QuantArgs& a, uint32_t sign_mask) {
+  a.sign_mask = sign_mask;
+  for (int i = 0; i < 16; i++) a.rht_flip[i] = ((sign_mask >> i) & 1u) ? 0x80000000u : 0u;
 }
 
 // What one quantize launch produces.

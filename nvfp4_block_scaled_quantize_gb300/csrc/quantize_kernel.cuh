@@ -15,9 +15,11 @@
 //     (thread-local maximum, RHT butterflies and conversion);
 //   * scale reciprocals come from a per-group 128-entry table indexed by the E4M3 code, built
 //     once per segment with the exact (div_rn) reciprocal ("Fast math");
-//   * columnwise codes/scales of the four slabs are staged in shared memory (XOR-swizzled,
-//     conflict-free) and leave as whole 32-byte column runs ("Optimization" item 5); grouped
-//     segments start their tiles on 64-row column boundaries so that this holds for them too;
+//   * columnwise codes of the four slabs are staged in shared memory in the layout of a TMA
+//     store's box and leave by one tensor store per tile (a 3D view of the output in which the
+//     tile's 256 columns are one box), the scales as one 4-byte store per column
+//     ("Optimization" item 5); grouped segments start their tiles on 64-row column boundaries
+//     so that whole tiles stay whole for them too;
 //   * 2D row+col: the columnwise codes are the rowwise codes transposed in registers;
 //   * stochastic rounding uses one Philox4x32-10 draw per 16-element block, all four words
 //     consumed by cvt.rs.satfinite.e2m1x4 ("Optimization" item 3).
@@ -48,8 +50,13 @@ struct Coord {
   int32_t pad;
 };
 
-// XOR swizzle of 16-byte chunks inside each 128-byte row of the columnwise code staging.
-__device__ __forceinline__ int swz(int chunk) { return (chunk & ~7) | ((chunk ^ (chunk >> 3)) & 7); }
+// Columnwise code staging in the layout of the TMA store's box: column 8 y + z of the tile
+// (y = 0..31, z = 0..7) at z * 1024 + y * 32, its 32 bytes the four slabs' 8 bytes in order,
+// the two 16-byte halves swapped where bit 2 of y is set (the 32-byte swizzle). Lane l's
+// column 8 l + z, slab sl:
+__device__ __forceinline__ int col_stage_off(int l, int z, int sl) {
+  return z * 1024 + l * 32 + ((((sl >> 1) ^ (l >> 2)) & 1) << 4) + ((sl & 1) << 3);
+}
 
 __device__ __forceinline__ uint32_t comp(const uint4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
             uint32_t w[16];
 #pragma unroll
             for (int r = 0; r < 16; r++) w[r] = comp(v[r], c4);
-            mt = vmax2(mt, rht16_pair_absmax(w, a.sign_mask));  // both sign-cleared
+            mt = vmax2(mt, rht16_pair_absmax(w, a.rht_flip));  // both sign-cleared
           }
         }
       }
@@ -501,35 +508,49 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     cur_seg = e;
   };
-  // Write-out of a tile's staged columnwise codes and scales by the whole group: thread gt owns
-  // the column pair 2 gt, 2 gt + 1, and a column's 64 codes leave as one 32-byte store.
+  // Write-out of a tile's staged columnwise codes and scales by the whole group. Whole tiles'
+  // codes leave by one TMA store (issued by thread 0 of the group); otherwise thread gt owns
+  // the column pair 2 gt, 2 gt + 1 and a column's codes leave as one 32-byte store (or as its
+  // slabs' 8-byte pieces). The scales always leave from the threads.
   auto write_out = [&](const Coord& wc, const uint8_t* ccs, const uint8_t* css) {
     const int nrb = (wc.nrows + 15) >> 4;
+    const bool whole = nrb == kWarpsPerGroup && wc.skip == 0;  // all four slabs are ours
+    if (a.col_tma && whole) {
+      if (gt == 0) {
+        tma_store_3d(&a.tmap_colc, ccs, wc.colpos / 2, wc.n0 / 8, 0);
+        bulk_commit();
+      }
+    }
     const int64_t col0 = (int64_t)wc.n0 + 2 * gt;   // this thread's column pair
     if (col0 < N) {
-      uint4 d[kWarpsPerGroup];
+      if (!(a.col_tma && whole)) {
+        const int l = gt >> 2, z0 = (2 * gt) & 7;   // lane of origin, columns z0 and z0 + 1
+        const uint8_t* p0 = ccs + z0 * 1024 + l * 32;
+        const uint8_t* p1 = p0 + 1024;
+        const int sw = ((l >> 2) & 1) << 4;  // the 32-byte swizzle of this y
+        uint4 c0a = *reinterpret_cast<const uint4*>(p0 + sw), c0b = *reinterpret_cast<const uint4*>(p0 + (16 ^ sw));
+        uint4 c1a = *reinterpret_cast<const uint4*>(p1 + sw), c1b = *reinterpret_cast<const uint4*>(p1 + (16 ^ sw));
+        // c?a: slabs 0, 1; c?b: slabs 2, 3
+        uint8_t* dst0 = a.col_codes + col0 * (a.col_ld / 2) + wc.colpos / 2;
+        uint8_t* dst1 = dst0 + a.col_ld / 2;
+        const uintptr_t dbits = reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1);
+        if (whole && (dbits & 31) == 0) {
+          stg256(dst0, c0a, c0b);
+          stg256(dst1, c1a, c1b);
+        } else if (whole && (dbits & 15) == 0) {
+          reinterpret_cast<uint4*>(dst0)[0] = c0a;
+          reinterpret_cast<uint4*>(dst0)[1] = c0b;
+          reinterpret_cast<uint4*>(dst1)[0] = c1a;
+          reinterpret_cast<uint4*>(dst1)[1] = c1b;
+        } else {
+          const uint2 q0[4] = {make_uint2(c0a.x, c0a.y), make_uint2(c0a.z, c0a.w), make_uint2(c0b.x, c0b.y), make_uint2(c0b.z, c0b.w)};
+          const uint2 q1[4] = {make_uint2(c1a.x, c1a.y), make_uint2(c1a.z, c1a.w), make_uint2(c1b.x, c1b.y), make_uint2(c1b.z, c1b.w)};
 #pragma unroll
-      for (int r = 0; r < kWarpsPerGroup; r++)
-        if (r < nrb) d[r] = *reinterpret_cast<const uint4*>(ccs + r * (kTileN * 8) + swz(gt) * 16);
-      uint8_t* dst0 = a.col_codes + col0 * (a.col_ld / 2) + wc.colpos / 2;
-      uint8_t* dst1 = dst0 + a.col_ld / 2;
-      const uintptr_t dbits = reinterpret_cast<uintptr_t>(dst0) | reinterpret_cast<uintptr_t>(dst1);
-      const bool whole = nrb == kWarpsPerGroup && wc.skip == 0;  // all four slabs are ours
-      if (whole && (dbits & 31) == 0) {
-        // each column's 64 codes are one full 32-byte sector: one store per column
-        stg256(dst0, make_uint4(d[0].x, d[0].y, d[1].x, d[1].y), make_uint4(d[2].x, d[2].y, d[3].x, d[3].y));
-        stg256(dst1, make_uint4(d[0].z, d[0].w, d[1].z, d[1].w), make_uint4(d[2].z, d[2].w, d[3].z, d[3].w));
-      } else if (whole && (dbits & 15) == 0) {
-        reinterpret_cast<uint4*>(dst0)[0] = make_uint4(d[0].x, d[0].y, d[1].x, d[1].y);
-        reinterpret_cast<uint4*>(dst0)[1] = make_uint4(d[2].x, d[2].y, d[3].x, d[3].y);
-        reinterpret_cast<uint4*>(dst1)[0] = make_uint4(d[0].z, d[0].w, d[1].z, d[1].w);
-        reinterpret_cast<uint4*>(dst1)[1] = make_uint4(d[2].z, d[2].w, d[3].z, d[3].w);
-      } else {
-#pragma unroll
-        for (int r = 0; r < kWarpsPerGroup; r++) {
-          if (r >= wc.skip && r < nrb) {
-            *reinterpret_cast<uint2*>(dst0 + 8 * r) = make_uint2(d[r].x, d[r].y);
-            *reinterpret_cast<uint2*>(dst1 + 8 * r) = make_uint2(d[r].z, d[r].w);
+          for (int r = 0; r < kWarpsPerGroup; r++) {
+            if (r >= wc.skip && r < nrb) {
+              *reinterpret_cast<uint2*>(dst0 + 8 * r) = q0[r];
+              *reinterpret_cast<uint2*>(dst1 + 8 * r) = q1[r];
+            }
           }
         }
       }
@@ -612,6 +633,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     // All four slabs are in registers: the stage can be refilled, the previous tile's staging
     // is complete (every warp staged it before arriving here), the buffer before it was
     // written out, and the group's abort flag is settled.
+    if (COL && !AMAX_ONLY) {
+      fence_proxy_async();             // this thread's staging, for the TMA store
+      if (gt == 0) bulk_wait_read();   // the store that read the buffer about to be staged
+    }
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     if (flags[g]) break;
     if (gt == 0 && i + kStages < n_slots) {
@@ -638,7 +663,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
             uint32_t w[16];
 #pragma unroll
             for (int r = 0; r < 16; r++) w[r] = comp(v[r], k);
-            mt = vmax2(mt, rht16_pair_absmax(w, a.sign_mask));
+            mt = vmax2(mt, rht16_pair_absmax(w, a.rht_flip));
           }
           mc = max(mt & 0xFFFFu, mt >> 16);
         }
@@ -784,9 +809,12 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         transpose_nibbles8(tcode);
         transpose_nibbles8(tcode + 8);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          *reinterpret_cast<uint4*>(cc_stage + rb * (kTileN * 8) + swz(4 * lane + k) * 16) =
-              make_uint4(tcode[2 * k], tcode[8 + 2 * k], tcode[2 * k + 1], tcode[8 + 2 * k + 1]);
+        for (int k = 0; k < 4; k++) {
+          *reinterpret_cast<uint2*>(cc_stage + col_stage_off(lane, 2 * k, rb)) =
+              make_uint2(tcode[2 * k], tcode[8 + 2 * k]);
+          *reinterpret_cast<uint2*>(cc_stage + col_stage_off(lane, 2 * k + 1, rb)) =
+              make_uint2(tcode[2 * k + 1], tcode[8 + 2 * k + 1]);
+        }
         const uint32_t s4 = tile_s * 0x01010101u;  // the tile scale for all four column pairs
         *reinterpret_cast<uint2*>(cs_stage + rb * kTileN + lane * 8) = make_uint2(s4, s4);
       }
@@ -798,8 +826,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
 #pragma unroll
           for (int r = 0; r < 16; r++) w[r] = comp(v[r], k);
           uint64_t xs[16];  // fast math: the FP32 transform, not rounded (unused otherwise)
-          if (FAST_RHT) rht16_pair_f32(w, a.sign_mask, xs);
-          else if (RHT) rht16_pair(w, a.sign_mask);
+          if (FAST_RHT) rht16_pair_f32(w, a.rht_flip, xs);
+          else if (RHT) rht16_pair(w, a.rht_flip);
           uint32_t s2;
           uint64_t rc2;
           if (FAST_RHT) {
@@ -841,8 +869,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
             code[1][o] = e2m1x8<SR_COL>(t[0].y, t[1].y, t[2].y, t[3].y, t[4].y, t[5].y, t[6].y,
                                         t[7].y, comp(W1, 2 * o), comp(W1, 2 * o + 1));
           }
-          *reinterpret_cast<uint4*>(cc_stage + rb * (kTileN * 8) + swz(4 * lane + k) * 16) =
-              make_uint4(code[0][0], code[0][1], code[1][0], code[1][1]);
+          *reinterpret_cast<uint2*>(cc_stage + col_stage_off(lane, 2 * k, rb)) =
+              make_uint2(code[0][0], code[0][1]);
+          *reinterpret_cast<uint2*>(cc_stage + col_stage_off(lane, 2 * k + 1, rb)) =
+              make_uint2(code[1][0], code[1][1]);
         }
         *reinterpret_cast<uint2*>(cs_stage + rb * kTileN + lane * 8) = make_uint2(csc[0], csc[1]);
       }
@@ -854,9 +884,11 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     buf ^= 1;
   }
   if (COL && !AMAX_ONLY && have_prev && !flags[g]) {
+    fence_proxy_async();
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     write_out(prev, cc_base + (buf ^ 1) * kColCodeStage, cs_base + (buf ^ 1) * kColScaleStage);
   }
+  if (COL && !AMAX_ONLY && gt == 0) bulk_wait_all();  // the last store has left shared memory
 
   // Every load issued into a stage is waited for by the group that owns its tile, unless that
   // group gave up: let the last load of each stage land before the CTA leaves.

@@ -135,11 +135,21 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
     return NVFP4_ERR_CUDA;
   q.x = x;
   q.rows = M; q.cols = N; q.offsets = nullptr; q.segments = 1;
-  q.sign_mask = cfg->rht_sign_mask; q.col_ld = M;
+  set_rht_flips(q, cfg->rht_sign_mask); q.col_ld = M;
   q.amax_row = nullptr; q.amax_col = nullptr;  // computed in the launch (fused)
   q.amax_row_stride = 2; q.amax_col_stride = 2;
   q.row_codes = row_codes; q.row_scales = row_scales; q.row_gscale = row_gscale;
   q.col_codes = col_codes; q.col_scales = col_scales; q.col_gscale = col_gscale;
+  if (col && (M / 2) % 16 == 0 && N % 8 == 0) {
+    cuuint64_t cdims[3] = {(cuuint64_t)(M / 2), (cuuint64_t)(N / 8), 8};
+    cuuint64_t cstrides[2] = {(cuuint64_t)(8 * (M / 2)), (cuuint64_t)(M / 2)};
+    cuuint32_t cbox[3] = {(cuuint32_t)(kTileM / 2), (cuuint32_t)(kTileN / 8), 8};
+    cuuint32_t cestr[3] = {1, 1, 1};
+    q.col_tma = g_encode(&q.tmap_colc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, col_codes, cdims, cstrides,
+                         cbox, cestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS ? 1 : 0;
+  }
   q.seed = cfg->rng_seed; set_philox_keys(q, cfg->rng_seed); q.rng_offset = cfg->rng_offset;
   q.status = d->scratch + kScratchStatus;
   q.fused = 1;
