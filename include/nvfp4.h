@@ -119,6 +119,18 @@ typedef struct nvfp4_config {
                              step. The amax, the global scales and 2D (block2d) quantization
                              stay exact. Other values:
                              NVFP4_ERR_INVALID_ARG. */
+  int32_t swizzle_scales; /* 0 = row-major scale outputs (default). 1 = both scale outputs in the
+                             128 x 4 tiled layout the tensor-core block-scaled (NVFP4) GEMMs
+                             read, the one nvfp4_swizzle_scales writes (see there), written by
+                             the quantize kernel itself ([PR4798] "Config surface and AUTO":
+                             the reference's columnwise scale store is hardwired to it): the
+                             scale matrix [R][C] (rowwise R = M, C = N/16; columnwise R = N,
+                             C = M/16) zero-padded to whole 128 x 4 tiles, so the buffers hold
+                             ceil(R/128) * ceil(C/4) * 512 bytes. nvfp4_quantize and
+                             nvfp4_quantize_noalloc only (grouped calls and the host pipeline:
+                             NVFP4_ERR_UNSUPPORTED). When R or C is not a multiple of 128 or 4
+                             the call first zeroes the buffers (one memset each). Other values:
+                             NVFP4_ERR_INVALID_ARG. */
 } nvfp4_config;
 
 /* Stochastic rounding ([PR4798] "Optimization" item 3 and "Correctness"): one Philox4x32-10

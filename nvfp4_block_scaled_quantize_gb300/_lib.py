@@ -44,6 +44,7 @@ class Config(ctypes.Structure):
         ("rng_seed", ctypes.c_uint64),
         ("fused_amax", ctypes.c_int32),
         ("fast_math", ctypes.c_int32),
+        ("swizzle_scales", ctypes.c_int32),
     ]
 
 

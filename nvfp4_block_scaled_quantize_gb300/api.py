@@ -44,12 +44,13 @@ def _round(v):
 
 def make_config(rowwise=True, columnwise=False, block2d=False, round_row="rn", round_col="rn",
                 rht_col=False, sign_mask=0, seed=0, offset=0, fused_amax=False,
-                fast_math=False) -> Config:
+                fast_math=False, swizzle_scales=False) -> Config:
     return Config(rowwise=int(bool(rowwise)), columnwise=int(bool(columnwise)),
                   block2d=int(bool(block2d)), round_row=_round(round_row),
                   round_col=_round(round_col), rht_col=int(bool(rht_col)),
                   rht_sign_mask=int(sign_mask), rng_offset=int(offset), rng_seed=int(seed),
-                  fused_amax=int(bool(fused_amax)), fast_math=int(bool(fast_math)))
+                  fused_amax=int(bool(fused_amax)), fast_math=int(bool(fast_math)),
+                  swizzle_scales=int(bool(swizzle_scales)))
 
 
 def _raise_if(status, where):
@@ -71,34 +72,48 @@ def nvfp4_amax(x, rht_col=False, sign_mask=0):
     return a_row, a_col
 
 
-def alloc_outputs(M, N, device, rowwise=True, columnwise=False, col_ld=None, groups=None):
+def swizzled_scale_bytes(R, C) -> int:
+    """Bytes of an [R][C] scale matrix in the 128 x 4 tiled layout (zero-padded tiles)."""
+    return ((R + 127) // 128) * ((C + 3) // 4) * 512
+
+
+def alloc_outputs(M, N, device, rowwise=True, columnwise=False, col_ld=None, groups=None,
+                  swizzled=False):
+    """Output buffers of one quantization; swizzled: scale buffers in the 128 x 4 tiled layout
+    (flat uint8 tensors, see nvfp4_config.swizzle_scales)."""
     out = {}
     g = () if groups is None else (groups,)
     if rowwise:
         out["row_codes"] = torch.empty((M, N // 2), dtype=torch.uint8, device=device)
-        out["row_scales"] = torch.empty((M, N // 16), dtype=torch.uint8, device=device)
+        out["row_scales"] = (torch.empty(swizzled_scale_bytes(M, N // 16), dtype=torch.uint8,
+                                         device=device) if swizzled else
+                             torch.empty((M, N // 16), dtype=torch.uint8, device=device))
         out["row_gscale"] = torch.empty(g + (2,), dtype=torch.float32, device=device)
     if columnwise:
         ld = M if col_ld is None else col_ld
         out["col_codes"] = torch.empty((N, ld // 2), dtype=torch.uint8, device=device)
-        out["col_scales"] = torch.empty((N, ld // 16), dtype=torch.uint8, device=device)
+        out["col_scales"] = (torch.empty(swizzled_scale_bytes(N, ld // 16), dtype=torch.uint8,
+                                         device=device) if swizzled else
+                             torch.empty((N, ld // 16), dtype=torch.uint8, device=device))
         out["col_gscale"] = torch.empty(g + (2,), dtype=torch.float32, device=device)
     return out
 
 
 def nvfp4_quantize(x, rowwise=True, columnwise=False, block2d=False, round_row="rn",
                    round_col="rn", rht_col=False, sign_mask=0, seed=0, offset=0,
-                   fused_amax=False, amax_row=None, amax_col=None, out=None, fast_math=False):
+                   fused_amax=False, amax_row=None, amax_col=None, out=None, fast_math=False,
+                   swizzle_scales=False):
     """Quantize a BF16 [M, N] CUDA tensor. amax_row / amax_col (float32[1] device tensors)
     skip the amax pass; `out` reuses preallocated outputs (see alloc_outputs); fast_math
-    selects the approximate variant (see nvfp4_config.fast_math)."""
+    selects the approximate variant (see nvfp4_config.fast_math); swizzle_scales writes both
+    scale outputs in the GEMMs' 128 x 4 tiled layout (see nvfp4_config.swizzle_scales)."""
     _check_x(x)
     L = _lib.load()
     M, N = x.shape
     cfg = make_config(rowwise, columnwise, block2d, round_row, round_col, rht_col, sign_mask,
-                      seed, offset, fused_amax, fast_math)
+                      seed, offset, fused_amax, fast_math, swizzle_scales)
     if out is None:
-        out = alloc_outputs(M, N, x.device, rowwise, columnwise)
+        out = alloc_outputs(M, N, x.device, rowwise, columnwise, swizzled=swizzle_scales)
     g = out.get
     status = L.nvfp4_quantize(_ptr(x), M, N, ctypes.byref(cfg), _ptr(amax_row), _ptr(amax_col),
                               _ptr(g("row_codes")), _ptr(g("row_scales")), _ptr(g("row_gscale")),
@@ -182,13 +197,14 @@ def nvfp4_dequantize_ex(codes, scales, gscale, inverse_rht=False, sign_mask=0, b
     return out
 
 
-def nvfp4_swizzle_scales(scales):
-    """uint8 [R, C] E4M3 scales -> the flat 128 x 4 tiled layout of the block-scaled GEMMs."""
+def nvfp4_swizzle_scales(scales, out=None):
+    """uint8 [R, C] E4M3 scales -> the flat 128 x 4 tiled layout of the block-scaled GEMMs
+    (into `out` when given)."""
     L = _lib.load()
     src = scales.contiguous()
     R, C = src.shape
-    out = torch.empty(((R + 127) // 128) * ((C + 3) // 4) * 512, dtype=torch.uint8,
-                      device=src.device)
+    if out is None:
+        out = torch.empty(swizzled_scale_bytes(R, C), dtype=torch.uint8, device=src.device)
     _raise_if(L.nvfp4_swizzle_scales(_ptr(src), R, C, _ptr(out), _stream(src.device)),
               "nvfp4_swizzle_scales")
     return out

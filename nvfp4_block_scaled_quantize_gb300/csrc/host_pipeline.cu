@@ -95,6 +95,7 @@ bool alloc(T** out, size_t bytes) {
 NVFP4_EXPORT nvfp4_status nvfp4_host_pipeline_create(int64_t M, int64_t N,
                                                      const nvfp4_config* cfg, int32_t depth,
                                                      nvfp4_host_pipeline** out) {
+  if (cfg != nullptr && cfg->swizzle_scales != 0) return NVFP4_ERR_UNSUPPORTED;
   if (out == nullptr || cfg == nullptr || (cfg->fast_math != 0 && cfg->fast_math != 1))
     return NVFP4_ERR_INVALID_ARG;
   *out = nullptr;

@@ -123,6 +123,7 @@ bool make_col_codes_map(CUtensorMap* map, uint8_t* col_codes, int64_t cols, int6
 nvfp4_status check_config(const nvfp4_config* cfg) {
   if (cfg == nullptr) return NVFP4_ERR_INVALID_ARG;
   if (cfg->fast_math != 0 && cfg->fast_math != 1) return NVFP4_ERR_INVALID_ARG;
+  if (cfg->swizzle_scales != 0 && cfg->swizzle_scales != 1) return NVFP4_ERR_INVALID_ARG;
   if ((cfg->round_row != NVFP4_ROUND_RN && cfg->round_row != NVFP4_ROUND_SR) ||
       (cfg->round_col != NVFP4_ROUND_RN && cfg->round_col != NVFP4_ROUND_SR))
     return NVFP4_ERR_INVALID_ARG;
@@ -358,6 +359,12 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t N,
   q.fused = fused ? 1 : 0;
   q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
   q.fuse_ws = ds->workspace + kFuseWsOffset;
+  if (cfg->swizzle_scales) {
+    const bool row_scales_out = row, col_scales_out = col;
+    if (prepare_swizzled_scales(q, row_scales_out ? row_scales : nullptr,
+                                col_scales_out ? col_scales : nullptr, M, N, s) != cudaSuccess)
+      return cuda_status(cudaErrorUnknown);
+  }
   const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
   const int grid = (int)(tiles < ds->sm_count ? tiles : ds->sm_count);
   const QuantMode mode{row, col, rht, two_d, sr_row != 0, sr_col != 0, q.fast && rht};
@@ -383,7 +390,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   const bool rht = cfg->rht_col != 0 && col;
   if (!row && !col) return NVFP4_ERR_UNSUPPORTED;
   const bool two_d = cfg->block2d != 0;
-  if (cfg->fused_amax) return NVFP4_ERR_UNSUPPORTED;
+  if (cfg->fused_amax || cfg->swizzle_scales) return NVFP4_ERR_UNSUPPORTED;
   if (two_d && (cfg->rht_col || cfg->round_row == NVFP4_ROUND_SR || cfg->round_col == NVFP4_ROUND_SR))
     return NVFP4_ERR_UNSUPPORTED;
   if (T < 0 || H < 0 || E < 1 || E > kMaxSegments || offsets == nullptr) return NVFP4_ERR_INVALID_ARG;

@@ -61,6 +61,8 @@ struct QuantArgs {
   CUtensorMap tmap_colc;            // col_codes as bytes {col_ld / 2, cols / 8, 8} (column 8y + z),
                                     // box {kTileM / 2, kTileN / 8, 8}, 32-byte swizzle
   int32_t col_tma;                  // 1: whole tiles' columnwise codes leave by TMA (tmap_colc)
+  int32_t swz_scales;               // 1: both scale outputs in the 128 x 4 tiled layout
+  int64_t row_swz_tc, col_swz_tc;   // tiles per tile row of that layout: ceil(scale columns / 4)
   const void* x;                    // the same tensor, for the fused amax phase
   int64_t rows, cols;
   const int32_t* offsets;           // cumulative segment ends, or nullptr: one segment
@@ -127,6 +129,22 @@ inline void set_philox_keys(QuantArgs& a, uint64_t seed) {
 inline void set_rht_flips(QuantArgs& a, uint32_t sign_mask) {
   a.sign_mask = sign_mask;
   for (int i = 0; i < 16; i++) a.rht_flip[i] = ((sign_mask >> i) & 1u) ? 0x80000000u : 0u;
+}
+
+// Scale outputs in the 128 x 4 tiled layout (nvfp4_config.swizzle_scales): the tiles per tile
+// row for the kernel, and the buffers zeroed first when the scale matrix does not fill whole
+// tiles (the padding of that layout is zero). A NULL buffer: that side is not produced.
+inline cudaError_t prepare_swizzled_scales(QuantArgs& q, uint8_t* row_scales, uint8_t* col_scales,
+                                           int64_t M, int64_t N, cudaStream_t s) {
+  q.swz_scales = 1;
+  q.row_swz_tc = (N / 16 + 3) / 4;
+  q.col_swz_tc = (M / 16 + 3) / 4;
+  cudaError_t e = cudaSuccess;
+  if (row_scales && (M % 128 != 0 || (N / 16) % 4 != 0))
+    e = cudaMemsetAsync(row_scales, 0, (size_t)((M + 127) / 128) * q.row_swz_tc * 512, s);
+  if (e == cudaSuccess && col_scales && (N % 128 != 0 || (M / 16) % 4 != 0))
+    e = cudaMemsetAsync(col_scales, 0, (size_t)((N + 127) / 128) * q.col_swz_tc * 512, s);
+  return e;
 }
 
 // What one quantize launch produces.

@@ -50,6 +50,14 @@ struct Coord {
   int32_t pad;
 };
 
+// Byte offset of scale (r, c) in the 128 x 4 tiled layout of the block-scaled GEMMs' scale
+// factors (the scale matrix zero-padded to whole 128 x 4 tiles, tiles_c tiles per tile row, 512
+// bytes each in row-major tile order; inside a tile, row r % 128 = 32 i + q and column j sit at
+// 16 q + 4 i + j).
+__device__ __forceinline__ int64_t swz_scale_off(int64_t r, int64_t c, int64_t tiles_c) {
+  return ((r >> 7) * tiles_c + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
 // Columnwise code staging in the layout of the TMA store's box: column 8 y + z of the tile
 // (y = 0..31, z = 0..7) at z * 1024 + y * 32, its 32 bytes the four slabs' 8 bytes in order,
 // the two 16-byte halves swapped where bit 2 of y is set (the 32-byte swizzle). Lane l's
@@ -563,16 +571,46 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           sc1 |= (pr >> 8) << (8 * r);
         }
       }
-      uint8_t* sd0 = a.col_scales + col0 * col_nb + wc.colpos / 16;
-      uint8_t* sd1 = sd0 + col_nb;
-      if (whole && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
-        *reinterpret_cast<uint32_t*>(sd0) = sc0;
-        *reinterpret_cast<uint32_t*>(sd1) = sc1;
-      } else {
-        for (int r = wc.skip; r < nrb; r++) {
-          sd0[r] = (uint8_t)(sc0 >> (8 * r));
-          sd1[r] = (uint8_t)(sc1 >> (8 * r));
+      if (!a.swz_scales) {
+        uint8_t* sd0 = a.col_scales + col0 * col_nb + wc.colpos / 16;
+        uint8_t* sd1 = sd0 + col_nb;
+        if (whole && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
+          *reinterpret_cast<uint32_t*>(sd0) = sc0;
+          *reinterpret_cast<uint32_t*>(sd1) = sc1;
+        } else {
+          for (int r = wc.skip; r < nrb; r++) {
+            sd0[r] = (uint8_t)(sc0 >> (8 * r));
+            sd1[r] = (uint8_t)(sc1 >> (8 * r));
+          }
         }
+      } else if (!whole) {  // the tiled layout, a partial tile: byte by byte
+        for (int r = wc.skip; r < nrb; r++) {
+          a.col_scales[swz_scale_off(col0, wc.colpos / 16 + r, a.col_swz_tc)] = (uint8_t)(sc0 >> (8 * r));
+          if (col0 + 1 < N)
+            a.col_scales[swz_scale_off(col0 + 1, wc.colpos / 16 + r, a.col_swz_tc)] = (uint8_t)(sc1 >> (8 * r));
+        }
+      }
+    }
+    // The tiled layout, a whole tile: its 256 columns x 4 scales (colpos / 16 is a multiple of
+    // four, n0 of 256) are two whole 128 x 4 tiles of 512 contiguous bytes; thread gt < 64
+    // writes the 16 bytes of row q = gt % 32 of tile half gt / 32 (columns 32 i + q, i = 0..3).
+    if (a.swz_scales && whole && gt < 64) {
+      const int h = gt >> 5, q = gt & 31;
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const int cc = 128 * h + 32 * i + q;
+        w[i] = (uint32_t)css[cc] | ((uint32_t)css[kTileN + cc] << 8) |
+               ((uint32_t)css[2 * kTileN + cc] << 16) | ((uint32_t)css[3 * kTileN + cc] << 24);
+      }
+      const int64_t row = (int64_t)wc.n0 + 128 * h;
+      uint8_t* dst = a.col_scales + swz_scale_off(row, wc.colpos / 16, a.col_swz_tc) + 16 * q;
+      if (row + 128 <= N) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+          if (row + 32 * i + q < N) *reinterpret_cast<uint32_t*>(dst + 4 * i) = w[i];
       }
     }
   };
@@ -773,7 +811,13 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
                                 SR_ROW ? wr[r][0] : 0u, SR_ROW ? wr[r][1] : 0u);
         };
         uint8_t* rowp = a.row_codes + row_g0 * (N / 2) + c.n0 / 2 + lane * 4;
-        uint8_t* rsp = a.row_scales + row_g0 * row_nb + c.n0 / 16 + kb + (odd ? 2 : 0) * row_nb;
+        // the lane's scale bytes: rows row_g0 + 4q (+ 2 on the odd lane) and the next, column
+        // c.n0 / 16 + kb, row-major or in the tiled layout (rows 16 bytes apart there: no row
+        // of the slab crosses a 32-row boundary)
+        const int64_t rcol = c.n0 / 16 + kb, rrow = row_g0 + (odd ? 2 : 0);
+        uint8_t* rsp = a.row_scales + (a.swz_scales ? swz_scale_off(rrow, rcol, a.row_swz_tc)
+                                                    : rrow * row_nb + rcol);
+        const int64_t rstride = a.swz_scales ? 16 : row_nb;
         if (kRowCol2D) {
           // 2D: the columnwise codes are these codes transposed (one multiplier per 16x16
           // tile, the same in both orientations), so keep all 16 rows
@@ -786,8 +830,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
             *reinterpret_cast<uint32_t*>(rowp + (int64_t)r * (N / 2)) = kRowCol2D ? tcode[r] : row_code(r);
 #pragma unroll
           for (int q = 0; q < 4; q++) {
-            rsp[(int64_t)(4 * q) * row_nb] = (uint8_t)(own_s[q] & 0xFFu);
-            rsp[(int64_t)(4 * q + 1) * row_nb] = (uint8_t)(own_s[q] >> 8);
+            rsp[(int64_t)(4 * q) * rstride] = (uint8_t)(own_s[q] & 0xFFu);
+            rsp[(int64_t)(4 * q + 1) * rstride] = (uint8_t)(own_s[q] >> 8);
           }
         } else if (lane_cols) {
 #pragma unroll
@@ -797,8 +841,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; q++) {
             const int r0 = 4 * q + (odd ? 2 : 0);
-            if (r0 < slab_rows) rsp[(int64_t)(4 * q) * row_nb] = (uint8_t)(own_s[q] & 0xFFu);
-            if (r0 + 1 < slab_rows) rsp[(int64_t)(4 * q + 1) * row_nb] = (uint8_t)(own_s[q] >> 8);
+            if (r0 < slab_rows) rsp[(int64_t)(4 * q) * rstride] = (uint8_t)(own_s[q] & 0xFFu);
+            if (r0 + 1 < slab_rows) rsp[(int64_t)(4 * q + 1) * rstride] = (uint8_t)(own_s[q] >> 8);
           }
         }
       }

@@ -91,7 +91,9 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
                                                  uint8_t* row_scales, float* row_gscale,
                                                  uint8_t* col_codes, uint8_t* col_scales,
                                                  float* col_gscale, void* stream) {
-  if (cfg == nullptr || (cfg->fast_math != 0 && cfg->fast_math != 1)) return NVFP4_ERR_INVALID_ARG;
+  if (cfg == nullptr || (cfg->fast_math != 0 && cfg->fast_math != 1) ||
+      (cfg->swizzle_scales != 0 && cfg->swizzle_scales != 1))
+    return NVFP4_ERR_INVALID_ARG;
   if ((cfg->round_row != NVFP4_ROUND_RN && cfg->round_row != NVFP4_ROUND_SR) ||
       (cfg->round_col != NVFP4_ROUND_RN && cfg->round_col != NVFP4_ROUND_SR) ||
       cfg->rht_sign_mask > 0xFFFFu)
@@ -156,6 +158,12 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64
   q.fast = (cfg->fast_math && !two_d) ? 1 : 0;  // weights (2D blocks) have no fast variant
   q.fuse_ws = d->scratch + kScratchFuse;
   take_fuse_debug(q);  // the test hooks of the single-launch amax apply here too
+  if (cfg->swizzle_scales &&
+      prepare_swizzled_scales(q, row ? row_scales : nullptr, col ? col_scales : nullptr, M, N, s) !=
+          cudaSuccess) {
+    (void)cudaGetLastError();
+    return NVFP4_ERR_CUDA;
+  }
   // the single-launch amax keeps its counts in the array (zero when loaded; the last CTA to
   // finish with them readies them for the next launch), so nothing is cleared before a launch
   const QuantMode mode{row, col, rht, two_d, cfg->round_row == NVFP4_ROUND_SR,

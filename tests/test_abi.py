@@ -33,9 +33,11 @@ def test_header_and_library_agree(L):
 
 
 def test_config_struct_layout():
-    # int32 x 6, uint32 x 2, uint64, int32 x 2 -> 48 bytes, rng_seed at offset 32
-    assert ctypes.sizeof(_lib.Config) == 48
+    # int32 x 6, uint32 x 2, uint64, int32 x 3 -> 52 bytes of fields, padded to 56 (the uint64's
+    # alignment), rng_seed at offset 32, swizzle_scales at 48
+    assert ctypes.sizeof(_lib.Config) == 56
     assert _lib.Config.rng_seed.offset == 32
+    assert _lib.Config.swizzle_scales.offset == 48
 
 
 def test_status_strings(L):
