@@ -15,6 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libnvfp4.so")
 SOURCES = ["quantize_row.cu", "quantize_col.cu", "quantize_rowcol.cu", "quantize_rowcol_rht.cu",
+           "quantize_rowcol_rht_fast.cu",
            "quantize_2d.cu", "amax_dequant.cu", "nvfp4_api.cu", "quantize_noalloc.cu",
            "host_pipeline.cu", "amax_pass.cu", "mx_kernel.cu", "producer.cu"]
 HEADERS = ["nvfp4_device.cuh", "nvfp4_internal.h", "aux_internal.h", "quantize_kernel.cuh",

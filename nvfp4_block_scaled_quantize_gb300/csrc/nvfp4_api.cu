@@ -151,8 +151,10 @@ void take_fuse_debug(QuantArgs& q) {
 
 cudaError_t launch_quantize(const QuantMode& m, const QuantArgs& args, int grid, cudaStream_t s) {
   if (m.two_d) return launch_quantize_2d(m, args, grid, s);
-  if (m.row && m.col) return m.rht ? launch_quantize_rowcol_rht(m, args, grid, s)
-                                   : launch_quantize_rowcol(m, args, grid, s);
+  if (m.row && m.col && m.rht)
+    return m.fast ? launch_quantize_rowcol_rht_fast(m, args, grid, s)
+                  : launch_quantize_rowcol_rht(m, args, grid, s);
+  if (m.row && m.col) return launch_quantize_rowcol(m, args, grid, s);
   if (m.row) return launch_quantize_row(m, args, grid, s);
   return launch_quantize_col(m, args, grid, s);
 }
@@ -163,6 +165,7 @@ cudaError_t prepare_quantize_kernels() {
   if ((r = prepare_quantize_col()) != cudaSuccess) e = r;
   if ((r = prepare_quantize_rowcol()) != cudaSuccess) e = r;
   if ((r = prepare_quantize_rowcol_rht()) != cudaSuccess) e = r;
+  if ((r = prepare_quantize_rowcol_rht_fast()) != cudaSuccess) e = r;
   if ((r = prepare_quantize_2d()) != cudaSuccess) e = r;
   if ((r = prepare_amax_tiles()) != cudaSuccess) e = r;
   if ((r = prepare_mx_kernels()) != cudaSuccess) e = r;

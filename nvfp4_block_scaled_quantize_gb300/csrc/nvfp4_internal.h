@@ -167,11 +167,14 @@ cudaError_t launch_quantize_col(const QuantMode& m, const QuantArgs& a, int grid
 cudaError_t launch_quantize_rowcol(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_quantize_rowcol_rht(const QuantMode& m, const QuantArgs& a, int grid,
                                        cudaStream_t s);
+cudaError_t launch_quantize_rowcol_rht_fast(const QuantMode& m, const QuantArgs& a, int grid,
+                                            cudaStream_t s);
 cudaError_t launch_quantize_2d(const QuantMode& m, const QuantArgs& a, int grid, cudaStream_t s);
 cudaError_t prepare_quantize_row();
 cudaError_t prepare_quantize_col();
 cudaError_t prepare_quantize_rowcol();
 cudaError_t prepare_quantize_rowcol_rht();
+cudaError_t prepare_quantize_rowcol_rht_fast();
 cudaError_t prepare_quantize_2d();
 
 }  // namespace nvfp4

@@ -169,7 +169,7 @@ __device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int
 // FAST_RHT: fast math with the RHT (columnwise codes from the FP32 transform, no BF16
 // round-through).
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FUSED,
-          bool AMAX_ONLY = false, bool FAST_RHT = false>
+          bool AMAX_ONLY = false, bool FAST_RHT = false, bool SWZ = false>
 __global__ void __launch_bounds__(kQuantThreads, 1)
     quantize_tiles_kernel(const __grid_constant__ QuantArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           sc1 |= (pr >> 8) << (8 * r);
         }
       }
-      if (!a.swz_scales) {
+      if (!SWZ) {
         uint8_t* sd0 = a.col_scales + col0 * col_nb + wc.colpos / 16;
         uint8_t* sd1 = sd0 + col_nb;
         if (whole && ((reinterpret_cast<uintptr_t>(sd0) | reinterpret_cast<uintptr_t>(sd1)) & 3) == 0) {
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     // The tiled layout, a whole tile: its 256 columns x 4 scales (colpos / 16 is a multiple of
     // four, n0 of 256) are two whole 128 x 4 tiles of 512 contiguous bytes; thread gt < 64
     // writes the 16 bytes of row q = gt % 32 of tile half gt / 32 (columns 32 i + q, i = 0..3).
-    if (a.swz_scales && whole && gt < 64) {
+    if (SWZ && whole && gt < 64) {
       const int h = gt >> 5, q = gt & 31;
       uint32_t w[4];
 #pragma unroll
@@ -815,9 +815,9 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         // c.n0 / 16 + kb, row-major or in the tiled layout (rows 16 bytes apart there: no row
         // of the slab crosses a 32-row boundary)
         const int64_t rcol = c.n0 / 16 + kb, rrow = row_g0 + (odd ? 2 : 0);
-        uint8_t* rsp = a.row_scales + (a.swz_scales ? swz_scale_off(rrow, rcol, a.row_swz_tc)
-                                                    : rrow * row_nb + rcol);
-        const int64_t rstride = a.swz_scales ? 16 : row_nb;
+        uint8_t* rsp = a.row_scales + (SWZ ? swz_scale_off(rrow, rcol, a.row_swz_tc)
+                                           : rrow * row_nb + rcol);
+        const int64_t rstride = SWZ ? 16 : row_nb;
         if (kRowCol2D) {
           // 2D: the columnwise codes are these codes transposed (one multiplier per 16x16
           // tile, the same in both orientations), so keep all 16 rows
@@ -955,17 +955,25 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   }
 }
 
-template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
-cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
+// One variant: SWZ writes both scale outputs in the GEMMs' tiled layout (a.swz_scales).
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT, bool SWZ>
+cudaError_t launch_variant(const QuantArgs& args, int grid, cudaStream_t s) {
   if (args.fused) {
     // No CTA waits for another to start (fused_amax.cuh), so the CTAs need not be resident at
     // once: a plain launch with programmatic dependent launch, whose CTAs may start on the SMs
     // that the previous kernel's CTAs leave and wait for that kernel at entry.
-    return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT>,
+    return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT, SWZ>,
                       dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
   }
-  return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT>,
+  return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT, SWZ>,
                     dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
+}
+
+template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
+cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
+  return args.swz_scales
+             ? launch_variant<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, FAST_RHT, true>(args, grid, s)
+             : launch_variant<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, FAST_RHT, false>(args, grid, s);
 }
 
 // The amax pass (AMAX_ONLY) of a plain or grouped tensor.
@@ -982,13 +990,17 @@ cudaError_t prepare_amax_pass() {
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
 cudaError_t prepare() {
-  cudaError_t e = cudaFuncSetAttribute(
-      quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT>,
-      cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(
-      quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT>,
-      cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+  cudaError_t e = cudaSuccess, r;
+  auto set = [&](auto kernel) {
+    if ((r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kQuantSmemBytes)) != cudaSuccess)
+      e = r;
+  };
+  set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT, false>);
+  set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT, false>);
+  set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT, true>);
+  set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT, true>);
+  return e;
 }
 
 }  // namespace qk
