@@ -90,12 +90,13 @@ nvfp4_status device_state(DeviceState** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// TMA descriptor of a BF16 [rows][cols] row-major tensor, box {kTileN, kTileM}; reads outside
-// the tensor return zeros.
-nvfp4_status make_tensor_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols) {
+// TMA descriptor of a BF16 [rows][cols] row-major tensor, box {kTileN, box_rows} (a tile, or
+// one 16-row slab of it); reads outside the tensor return zeros.
+nvfp4_status make_tensor_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols,
+                             int box_rows = kTileM) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kTileN, (cuuint32_t)kTileM};
+  cuuint32_t box[2] = {(cuuint32_t)kTileN, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -208,6 +209,7 @@ nvfp4_status amax_tiles(const DeviceState* ds, const void* x, int64_t rows, int6
   std::memset(&q, 0, sizeof q);
   nvfp4_status st = make_tensor_map(&q.tmap, x, rows, cols);
   if (st != NVFP4_OK) return st;
+  if (offsets && (st = make_tensor_map(&q.tmap_slab, x, rows, cols, 16)) != NVFP4_OK) return st;
   q.x = x; q.rows = rows; q.cols = cols; q.offsets = offsets; q.segments = segments;
   set_rht_flips(q, sign_mask);
   q.amax_row = amax_row; q.amax_col = amax_col;
@@ -437,6 +439,7 @@ NVFP4_EXPORT nvfp4_status nvfp4_quantize_grouped(const void* x, int64_t T, int64
   QuantArgs q;
   std::memset(&q, 0, sizeof q);
   if ((st = make_tensor_map(&q.tmap, x, T, H)) != NVFP4_OK) return st;
+  if ((st = make_tensor_map(&q.tmap_slab, x, T, H, 16)) != NVFP4_OK) return st;
   q.rows = T; q.cols = H; q.offsets = offsets; q.segments = E;
   const int sr_row = cfg->round_row == NVFP4_ROUND_SR, sr_col = cfg->round_col == NVFP4_ROUND_SR;
   set_rht_flips(q, cfg->rht_sign_mask); q.col_ld = col ? col_capacity : 0;

@@ -8,10 +8,10 @@
 namespace nvfp4 {
 
 // ---- the quantize kernel's geometry ----
-// A tile is kTileM rows x kTileN BF16 columns (one TMA box, one pipeline stage). A warp owns
-// one 16-row slab of a tile; four warps (a group) share a tile; kGroups groups work on
-// different tiles at once, and each group refills the stage it has just drained, so kStages
-// tiles stay in flight.
+// A tile is kTileM rows x kTileN BF16 columns (one pipeline stage: one TMA box, or one box per
+// 16-row slab where a grouped tile's slabs are not consecutive rows of x). A warp owns one
+// slab of a tile; four warps (a group) share a tile; kGroups groups work on different tiles at
+// once, and each group refills the stage it has just drained, so kStages tiles stay in flight.
 constexpr int kTileM = 64;
 constexpr int kTileN = 256;
 constexpr int kStages = 4;
@@ -20,8 +20,12 @@ constexpr int kWarpsPerGroup = kTileM / 16;
 constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
 constexpr int kQuantThreads = 32 * kConsumerWarps;
 constexpr int kStageBytes = kTileM * kTileN * 2;
+constexpr int kSlabBytes = 16 * kTileN * 2;
 constexpr int kMaxSegments = 256;
 constexpr int kTableEntries = 128;  // E4M3 codes of non-negative scales
+// A segment's scale block: the rowwise and columnwise reciprocal tables (f32 [2][128]), then
+// {S_enc row, S_enc col} and 8 bytes of padding.
+constexpr int kTableBlock = 2 * kTableEntries * 4 + 16;
 
 // Shared-memory layout of the quantize kernel (byte offsets).
 constexpr int kColCodeStage = kWarpsPerGroup * kTileN * 8;   // [4 slabs][128 chunks][16 B]
@@ -30,21 +34,27 @@ constexpr int kSmemStages = 0;
 constexpr int kSmemColCodes = kSmemStages + kStages * kStageBytes;
 constexpr int kColStageBufs = 2;                             // per group (double-buffered)
 constexpr int kSmemColScales = kSmemColCodes + kGroups * kColStageBufs * kColCodeStage;
-constexpr int kSmemTables = kSmemColScales + kGroups * kColStageBufs * kColScaleStage;  // per group: 2 x 128 f32
-constexpr int kSmemSegStart = kSmemTables + kGroups * 2 * kTableEntries * 4;
-constexpr int kSmemSegEnd = kSmemSegStart + 4 * kMaxSegments;
-constexpr int kSmemSegCol0 = kSmemSegEnd + 4 * kMaxSegments;
-constexpr int kSmemSegTile0 = kSmemSegCol0 + 4 * kMaxSegments;        // [kMaxSegments + 4]
-constexpr int kSmemCoords = kSmemSegTile0 + 4 * (kMaxSegments + 4);   // [kStages][8] int32
-constexpr int kSmemBars = kSmemCoords + 32 * kStages;                 // full[kStages]
+constexpr int kSmemTables = kSmemColScales + kGroups * kColStageBufs * kColScaleStage;  // per group: a scale block
+// per segment {first slab, first row, end row, next segment's first slab}, [kMaxSegments + 1]
+constexpr int kSmemSegRec = kSmemTables + kGroups * kTableBlock;
+// per segment {S_enc row, S_dec row, S_enc col, S_dec col}, [kMaxSegments]
+constexpr int kSmemSegScale = kSmemSegRec + 16 * (kMaxSegments + 1);
+constexpr int kSmemCoords = kSmemSegScale + 16 * kMaxSegments;      // [kStages][16] int32
+constexpr int kSmemBars = kSmemCoords + 64 * kStages;                 // full[kStages]
 constexpr int kSmemFlags = kSmemBars + 8 * kStages;                   // int32 [4]
-constexpr int kSmemIssued = kSmemFlags + 16;                          // int32 [kStages]
+constexpr int kSmemSegHint = kSmemFlags + 16;                         // int32 [kConsumerWarps]
+constexpr int kSmemIssued = kSmemSegHint + 4 * kConsumerWarps;        // int32 [kStages]
 constexpr int kSmemFused = kSmemIssued + 4 * kStages;            // uint32 [32 + 4]
 // single-launch amax: the ranks this CTA does the amax of, each with its first ring slot
 constexpr int kMaxHeld = 128;
 constexpr int kSmemHeld = kSmemFused + 4 * 36;                   // int32 [2][kMaxHeld]
 constexpr int kSmemFuseCtl = kSmemHeld + 8 * kMaxHeld;            // int32 [4]
-constexpr int kQuantSmemBytes = kSmemFuseCtl + 16;
+// per warp: a scale block for a slab of another segment than its group's
+constexpr int kSmemWarpTables = kSmemFuseCtl + 16;
+constexpr int kQuantSmemBytes = kSmemWarpTables + kConsumerWarps * kTableBlock;
+static_assert(kSmemSegRec % 16 == 0 && kSmemSegScale % 16 == 0 && kSmemCoords % 16 == 0 &&
+                  kSmemBars % 8 == 0 && kSmemWarpTables % 16 == 0,
+              "shared-memory record alignment");
 
 // Workspace of the single-launch (fused amax) path, 4-byte aligned, zeroed before first use:
 // the count of ranks arrived, the count of CTAs done with the words, the rowwise and
@@ -58,6 +68,7 @@ constexpr int kFuseStatsWord = 4;  // ranks taken over from another CTA (statist
 // a plain tensor, one per expert for the grouped case).
 struct QuantArgs {
   CUtensorMap tmap;                 // x as BF16 [rows][cols], box {kTileN, kTileM}
+  CUtensorMap tmap_slab;            // the same, box {kTileN, 16} (grouped tensors only)
   CUtensorMap tmap_colc;            // col_codes as bytes {col_ld / 2, cols / 8, 8} (column 8y + z),
                                     // box {kTileM / 2, kTileN / 8, 8}, 32-byte swizzle
   int32_t col_tma;                  // 1: whole tiles' columnwise codes leave by TMA (tmap_colc)

@@ -18,8 +18,12 @@
 //   * columnwise codes of the four slabs are staged in shared memory in the layout of a TMA
 //     store's box and leave by one tensor store per tile (a 3D view of the output in which the
 //     tile's 256 columns are one box), the scales as one 4-byte store per column
-//     ("Optimization" item 5); grouped segments start their tiles on 64-row column boundaries
-//     so that whole tiles stay whole for them too;
+//     ("Optimization" item 5);
+//   * a grouped tensor is tiled in the space of its columnwise outputs, where each segment's
+//     rows sit padded to whole 16-row slabs, back to back: a tile is four consecutive slabs,
+//     from one segment or from several, loaded as one box when they are consecutive rows of x
+//     and slab by slab otherwise. No tile is partly empty except the last, and every tile's
+//     columnwise codes are whole 32-byte column runs;
 //   * 2D row+col: the columnwise codes are the rowwise codes transposed in registers;
 //   * stochastic rounding uses one Philox4x32-10 draw per 16-element block, all four words
 //     consumed by cvt.rs.satfinite.e2m1x4 ("Optimization" item 3).
@@ -40,14 +44,19 @@ namespace qk {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: no TMA load takes this long
 
 struct Coord {
-  int32_t row0;    // first row of the tile in x (negative rows read as zeros)
-  int32_t nrows;   // rows from row0 to the end of the tile's segment, at most kTileM
   int32_t n0;      // first column
   int32_t colpos;  // first column of the tile in the columnwise outputs (a multiple of kTileM)
-  int32_t seg;
   int32_t tile;    // the tile these coordinates belong to (checked by the consumers)
-  int32_t skip;    // leading 16-row slabs that lie before the segment (its first tile only)
-  int32_t pad;
+  int32_t nvalid;  // slabs that hold rows of a segment (the first nvalid of the four)
+  int32_t row0[kWarpsPerGroup];   // first row of each 16-row slab in x
+  int32_t nrows[kWarpsPerGroup];  // rows of each slab inside its segment (0: no slab)
+  int32_t seg[kWarpsPerGroup];    // segment of each slab (slab 0's where there is no slab)
+};
+static_assert(sizeof(Coord) == 64, "coordinate record size");
+
+// What the column write-out of a tile needs after its coordinates' stage has been refilled.
+struct OutPos {
+  int32_t n0, colpos, nvalid;
 };
 
 // Byte offset of scale (r, c) in the 128 x 4 tiled layout of the block-scaled GEMMs' scale
@@ -144,6 +153,25 @@ __device__ __forceinline__ void transpose_nibbles8(uint32_t* w) {
   }
 }
 
+// A warp's own scale block (kTableBlock) for segment scales q = {S_enc row, S_dec row, S_enc
+// col, S_dec col}: the rowwise and columnwise reciprocal tables and the two encode scales.
+// Out of line: it runs only for a slab whose segment is not its group's, and kept out of the
+// tile loop's code it leaves that loop's register allocation alone.
+static __device__ __noinline__ void build_scale_block(float* blk, float4 q, int lane, int fast) {
+  __syncwarp();  // every lane is done with the block's previous contents
+#pragma unroll 1
+  for (int c = lane; c < kTableEntries; c += 32) {
+    const float sv = e4m3x2_to_float2((uint16_t)c).x;
+    blk[c] = fast ? element_multiplier_fast(sv, q.y) : element_multiplier(sv, q.y);
+    blk[kTableEntries + c] = fast ? element_multiplier_fast(sv, q.w) : element_multiplier(sv, q.w);
+  }
+  if (lane == 0) {
+    blk[2 * kTableEntries] = q.x;
+    blk[2 * kTableEntries + 1] = q.z;
+  }
+  __syncwarp();
+}
+
 // Bounded wait until at least `count` loads have been issued into stage s (a monotonic
 // per-stage count). Only then does the mbarrier parity of load count - 1 name its phase
 // unambiguously: the previous load of the stage has been consumed, so its phase is complete.
@@ -167,9 +195,10 @@ __device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int
 // a.amax_row / a.amax_col (zeroed by the caller); no codes. Instantiated with ROW and !COL (no
 // lead rows: tiles start on the segments' 16-row blocks).
 // FAST_RHT: fast math with the RHT (columnwise codes from the FP32 transform, no BF16
-// round-through).
+// round-through). SWZ: both scale outputs in the GEMMs' tiled layout (a.swz_scales).
+// GROUPED: a tensor split into segments (a.offsets); never FUSED or SWZ.
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FUSED,
-          bool AMAX_ONLY = false, bool FAST_RHT = false, bool SWZ = false>
+          bool AMAX_ONLY = false, bool FAST_RHT = false, bool SWZ = false, bool GROUPED = false>
 __global__ void __launch_bounds__(kQuantThreads, 1)
     quantize_tiles_kernel(const __grid_constant__ QuantArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -186,24 +215,28 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   pdl_wait();
   if (!FUSED) pdl_allow_next();
 
-  int32_t* seg_start = reinterpret_cast<int32_t*>(smem + kSmemSegStart);
-  int32_t* seg_end = reinterpret_cast<int32_t*>(smem + kSmemSegEnd);
-  int32_t* seg_col0 = reinterpret_cast<int32_t*>(smem + kSmemSegCol0);
-  int32_t* seg_tile0 = reinterpret_cast<int32_t*>(smem + kSmemSegTile0);
+  // grouped: per segment {first slab in the padded columnwise space, first row, end row, the
+  // next segment's first slab}; [E] = {slab count, rows, rows, INT_MAX}
+  int4* seg_rec = reinterpret_cast<int4*>(smem + kSmemSegRec);
+  float4* seg_scale = reinterpret_cast<float4*>(smem + kSmemSegScale);
   Coord* coords = reinterpret_cast<Coord*>(smem + kSmemCoords);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemBars);
   volatile int32_t* flags = reinterpret_cast<volatile int32_t*>(smem + kSmemFlags);
   volatile int32_t* issued = reinterpret_cast<volatile int32_t*>(smem + kSmemIssued);
+  // grouped: per warp, the segment its last issue_slab() found (any index is a valid start)
+  int32_t* seg_hint = reinterpret_cast<int32_t*>(smem + kSmemSegHint);
 
   const int E = a.segments;
   const int tiles_n = (int)((a.cols + kTileN - 1) / kTileN);
   const int64_t N = a.cols;
 
   const int stride = gridDim.x;
+  int n_slabs = 0;  // grouped: slabs of all segments
   constexpr bool fused = FUSED;
   // A plain tensor is one segment: the first loads leave at once, before anything else
   // (the grouped path first needs the segment table below).
-  const bool plain = a.offsets == nullptr;
+  constexpr bool plain = !GROUPED;
+  static_assert(!GROUPED || (!FUSED && !SWZ), "grouped tensors: no single-launch amax, no tiled scales");
   int total = 0, n_local = 0;
 
   // Single-launch amax (fused_amax.cuh): the ranks this CTA computes the amax of, in order,
@@ -224,38 +257,89 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     return -1;
   };
 
-  // Load tile `tile` into stage s.
-  auto issue = [&](int tile, int s) {
-    int lo = 0, hi = E;  // segment: largest e with seg_tile0[e] <= tile
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (seg_tile0[mid] <= tile) lo = mid; else hi = mid;
+  // Load tile `tile` into stage s. Tile (mt, nt) is columns nt * kTileN.. and slabs 4 mt..
+  // 4 mt + 3: rows 64 mt.. of a plain tensor (one box, one arrival on the stage's mbarrier);
+  // for a grouped tensor, slabs of the padded columnwise space (segment e's slabs are
+  // seg_rec[e].x.., its rows 16 at a time), each loaded as a box of its own, with one arrival
+  // per slab (issue_slab). The consumers read the coordinate record after their wait on the
+  // stage's mbarrier, whose phase completes only after these arrivals (release; the wait
+  // acquires).
+  auto issue_slab = [&](int tile, int s, int k) {  // grouped: slab k of the tile
+    Coord* cp = coords + s;
+    const int mt = tile / tiles_n;
+    const int n0 = (tile - mt * tiles_n) * kTileN;
+    const int j = 4 * mt + k;
+    if (k == 0) {
+      cp->n0 = n0;
+      cp->colpos = mt * kTileM;
+      cp->tile = tile;
+      cp->nvalid = min(kWarpsPerGroup, n_slabs - 4 * mt);
     }
-    const int local = tile - seg_tile0[lo];
-    const int mt = local / tiles_n;
-    const int lead = COL ? (seg_col0[lo] & (kTileM - 1)) : 0;  // see the segment table
-    Coord c;
-    c.n0 = (local - mt * tiles_n) * kTileN;
-    c.row0 = seg_start[lo] - lead + mt * kTileM;
-    c.nrows = min(kTileM, seg_end[lo] - c.row0);
-    c.colpos = seg_col0[lo] - lead + mt * kTileM;
-    c.seg = lo;
-    c.tile = tile;
-    c.skip = mt == 0 ? lead / 16 : 0;
-    c.pad = 0;
-    coords[s] = c;
-    __threadfence_block();
+    if (j < n_slabs) {
+      // The segment of slab j: the one this warp's last call found, where it still holds j
+      // (tiles are walked forward), else a binary search for the largest e whose first slab
+      // is at most j (never an empty segment: the next one starts at the same slab).
+      int e = seg_hint[warp];
+      int4 r = seg_rec[e];
+      if (j < r.x || j >= r.w) {
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (seg_rec[mid].x <= j) lo = mid; else hi = mid;
+        }
+        e = lo;
+        r = seg_rec[e];
+        seg_hint[warp] = e;
+      }
+      const int row0 = r.y + 16 * (j - r.x);
+      cp->row0[k] = row0;
+      cp->nrows[k] = min(16, r.z - row0);
+      cp->seg[k] = e;
+      if (k == 0) issued[s] = issued[s] + 1;  // the stage's next mbarrier phase is this load's
+      mbar_expect_tx(&full[s], kSlabBytes);
+      tma_load_2d(smem + kSmemStages + s * kStageBytes + k * kSlabBytes, &a.tmap_slab, n0, row0,
+                  &full[s]);
+    } else {  // past the last slab (the last tile row only; never slab 0)
+      cp->row0[k] = 0;
+      cp->nrows[k] = 0;
+      cp->seg[k] = -1;
+      mbar_arrive(&full[s]);
+    }
+  };
+  auto issue = [&](int tile, int s) {
+    if (GROUPED) {
+      for (int k = 0; k < kWarpsPerGroup; k++) issue_slab(tile, s, k);
+      return;
+    }
+    Coord* cp = coords + s;
+    const int mt = tile / tiles_n;
+    const int n0 = (tile - mt * tiles_n) * kTileN;
+    cp->n0 = n0;
+    cp->colpos = mt * kTileM;
+    cp->tile = tile;
+    const int64_t rem = a.rows - (int64_t)mt * kTileM;  // rows from the tile's first on
+    int nvalid = 0;
+#pragma unroll
+    for (int k = 0; k < kWarpsPerGroup; k++) {
+      const int64_t rk = rem - 16 * k;
+      cp->row0[k] = mt * kTileM + 16 * k;
+      cp->nrows[k] = rk >= 16 ? 16 : (rk > 0 ? (int)rk : 0);
+      cp->seg[k] = 0;
+      nvalid += rk > 0 ? 1 : 0;
+    }
+    cp->nvalid = nvalid;
     issued[s] = issued[s] + 1;  // the stage's next mbarrier phase is this load's
     mbar_expect_tx(&full[s], kStageBytes);
-    tma_load_2d(smem + kSmemStages + s * kStageBytes, &a.tmap, c.n0, c.row0, &full[s]);
+    tma_load_2d(smem + kSmemStages + s * kStageBytes, &a.tmap, n0, mt * kTileM, &full[s]);
   };
   // The first kStages loads: the quantize phase's first tiles, or, with the single-launch
   // amax, the amax phase's (its slots walk the tiles from the last to the first, so that the
   // quantize phase, walking forward, starts on the kStages tiles still in shared memory).
   auto first_loads = [&]() {
     prefetch_tensormap(&a.tmap);
+    if (!plain) prefetch_tensormap(&a.tmap_slab);
     for (int s = 0; s < kStages; s++) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], GROUPED ? kWarpsPerGroup : 1);  // grouped: one arrival per slab
       issued[s] = 0;
     }
     fence_barrier_init();
@@ -269,11 +353,6 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     n_local = (int)blockIdx.x < total ? (total - (int)blockIdx.x + stride - 1) / stride : 0;
     if (tid == 0) {
       flags[0] = flags[1] = flags[2] = flags[3] = 0;
-      seg_start[0] = 0;
-      seg_end[0] = (int32_t)a.rows;
-      seg_col0[0] = 0;
-      seg_tile0[0] = 0;
-      seg_tile0[1] = total;
       if (fused) {
         // test hook: the last a.fuse_late CTAs hold back until every rank has arrived, so
         // that the others must take their ranks over (bounded)
@@ -291,51 +370,36 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     }
     __syncthreads();
   } else {
-    // ---- segment table: starts, ends, padded column starts, tile prefix sums ----
+    // ---- segment table: starts, ends, first slabs in the padded columnwise space ----
     if (tid < 4) flags[tid] = 0;
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) {
       const int32_t start = e == 0 ? 0 : a.offsets[e - 1];
       const int32_t end = a.offsets[e];
       if (start < 0 || end < start || (int64_t)end > a.rows) flags[3] = 1;
-      seg_start[e] = start;
-      seg_end[e] = end;
+      seg_rec[e].y = start;
+      seg_rec[e].z = end;
     }
+    if (tid < kConsumerWarps) seg_hint[tid] = 0;
     __syncthreads();
     if (warp == 0) {
-      int32_t tile_base = 0, col_base = 0;
+      int32_t slab_base = 0;
       for (int c0 = 0; c0 < E; c0 += 32) {
         const int e = c0 + lane;
-        const int32_t n = (e < E && !flags[3]) ? seg_end[e] - seg_start[e] : 0;
-        const int32_t p0 = ((n + 15) / 16) * 16;
+        const int32_t n = (e < E && !flags[3]) ? seg_rec[e].z - seg_rec[e].y : 0;
+        const int32_t p0 = (n + 15) / 16;  // the segment's slabs (its rows padded to 16)
         int32_t p = p0;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
           const int32_t pu = __shfl_up_sync(0xFFFFFFFFu, p, d);
           if (lane >= d) p += pu;
         }
-        const int32_t col0 = col_base + p - p0;
-        // With columnwise outputs a segment's tiles start lead = col0 % kTileM rows before it,
-        // so that every tile's columnwise position is a multiple of kTileM (whole 32-byte
-        // column runs); the lead rows are whole slabs, skipped by the consumers.
-        const int32_t lead = COL ? (col0 & (kTileM - 1)) : 0;
-        const int32_t t0 = n > 0 ? ((n + lead + kTileM - 1) / kTileM) * tiles_n : 0;
-        int32_t t = t0;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const int32_t tu = __shfl_up_sync(0xFFFFFFFFu, t, d);
-          if (lane >= d) t += tu;
-        }
-        if (e < E) {
-          seg_tile0[e] = tile_base + t - t0;
-          seg_col0[e] = col0;
-        }
-        tile_base += __shfl_sync(0xFFFFFFFFu, t, 31);
-        col_base += __shfl_sync(0xFFFFFFFFu, p, 31);
+        if (e < E) seg_rec[e].x = slab_base + p - p0;
+        slab_base += __shfl_sync(0xFFFFFFFFu, p, 31);
       }
       if (lane == 0) {
-        seg_tile0[E] = tile_base;
-        if (COL && (int64_t)col_base > a.col_ld) flags[3] = 1;
+        seg_rec[E] = make_int4(slab_base, (int32_t)a.rows, (int32_t)a.rows, 0x7FFFFFFF);
+        if (COL && (int64_t)slab_base * 16 > a.col_ld) flags[3] = 1;
       }
     }
     __syncthreads();
@@ -343,7 +407,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       if (blockIdx.x == 0 && tid == 0) atomicOr(a.status, 1u);  // NVFP4_DEVICE_BAD_OFFSETS
       return;
     }
-    total = seg_tile0[E];
+    for (int e = tid; e < E; e += blockDim.x) seg_rec[e].w = seg_rec[e + 1].x;
+    n_slabs = seg_rec[E].x;
+    __syncthreads();
+    total = ((n_slabs + kWarpsPerGroup - 1) / kWarpsPerGroup) * tiles_n;
     n_local = (int)blockIdx.x < total ? (total - (int)blockIdx.x + stride - 1) / stride : 0;
     if (tid == 0) first_loads();
     __syncthreads();
@@ -486,12 +553,26 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     }
   }
 
+  // Every segment's encode and decode scales, once per CTA (the single-launch amax computes its
+  // one segment's where the maxima are known, in set_segment)
+  if (!FUSED && !AMAX_ONLY) {
+    for (int e = tid; e < E; e += blockDim.x) {
+      float4 q = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+      if (ROW || TWO_D) global_scale(amax_row_of(e), q.x, q.y);
+      if (COL && !TWO_D) global_scale(amax_col_of(e), q.z, q.w);
+      if (TWO_D) { q.z = q.x; q.w = q.y; }
+      seg_scale[e] = q;
+    }
+    __syncthreads();
+  }
+
   // =========================================================================================
   // Groups of four warps, one tile at a time.
   // =========================================================================================
   const bool odd = (lane & 1) != 0;
   const int kb = lane >> 1;              // rowwise block of the tile row (lane pair)
-  float* tab_row = reinterpret_cast<float*>(smem + kSmemTables) + g * 2 * kTableEntries;
+  // the group's scale block (kTableBlock): tables [2][128], then {S_enc row, S_enc col}
+  float* tab_row = reinterpret_cast<float*>(smem + kSmemTables + g * kTableBlock);
   float* tab_col = tab_row + kTableEntries;
   // columnwise staging, two buffers per group: a tile's codes and scales are staged in one
   // while the previous tile's leave from the other
@@ -500,29 +581,45 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
   const int64_t row_nb = N / 16;
   const int64_t col_nb = a.col_ld / 16;
   int cur_seg = -1;
-  float s_enc_r = 1.0f, s_enc_c = 1.0f;
+  // Encode scales of segment e and the decode scales its reciprocal tables are built from.
+  auto seg_scales = [&](int e, float& enc_r, float& dec_r, float& enc_c, float& dec_c) {
+    if (FUSED) {
+      enc_r = enc_c = dec_r = dec_c = 1.0f;
+      if (ROW || TWO_D) global_scale(amax_row_of(e), enc_r, dec_r);
+      if (COL && !TWO_D) global_scale(amax_col_of(e), enc_c, dec_c);
+      if (TWO_D) { enc_c = enc_r; dec_c = dec_r; }
+    } else {
+      const float4 q = seg_scale[e];
+      enc_r = q.x; dec_r = q.y; enc_c = q.z; dec_c = q.w;
+    }
+  };
+  auto multiplier = [&](int code, float dec) -> float {
+    const float sv = e4m3x2_to_float2((uint16_t)code).x;
+    return a.fast ? element_multiplier_fast(sv, dec) : element_multiplier(sv, dec);
+  };
   // Global scales of segment e and the group's reciprocal tables for them: one entry of each
   // table per thread of the group. Called by the whole group, between tiles (no warp of the
   // group is still reading the previous tables).
   auto set_segment = [&](int e) {
-    float dec_r = 1.0f, dec_c = 1.0f;
-    if (ROW || TWO_D) global_scale(amax_row_of(e), s_enc_r, dec_r);
-    if (COL && !TWO_D) global_scale(amax_col_of(e), s_enc_c, dec_c);
-    if (TWO_D) { s_enc_c = s_enc_r; dec_c = dec_r; }
+    float enc_r, dec_r, enc_c, dec_c;
+    seg_scales(e, enc_r, dec_r, enc_c, dec_c);
     static_assert(kTableEntries == 32 * kWarpsPerGroup, "one table entry per group thread");
-    const float sv = e4m3x2_to_float2((uint16_t)gt).x;
-    tab_row[gt] = a.fast ? element_multiplier_fast(sv, dec_r) : element_multiplier(sv, dec_r);
-    tab_col[gt] = a.fast ? element_multiplier_fast(sv, dec_c) : element_multiplier(sv, dec_c);
+    tab_row[gt] = multiplier(gt, dec_r);
+    tab_col[gt] = multiplier(gt, dec_c);
+    if (gt == 0) { tab_row[2 * kTableEntries] = enc_r; tab_row[2 * kTableEntries + 1] = enc_c; }
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     cur_seg = e;
   };
+  // A grouped tile's slabs can belong to several segments; the group's scale block is its
+  // first slab's, and a warp whose slab lies in another segment builds a block of its own.
+  float* tab_warp = reinterpret_cast<float*>(smem + kSmemWarpTables + warp * kTableBlock);
   // Write-out of a tile's staged columnwise codes and scales by the whole group. Whole tiles'
   // codes leave by one TMA store (issued by thread 0 of the group); otherwise thread gt owns
   // the column pair 2 gt, 2 gt + 1 and a column's codes leave as one 32-byte store (or as its
   // slabs' 8-byte pieces). The scales always leave from the threads.
-  auto write_out = [&](const Coord& wc, const uint8_t* ccs, const uint8_t* css) {
-    const int nrb = (wc.nrows + 15) >> 4;
-    const bool whole = nrb == kWarpsPerGroup && wc.skip == 0;  // all four slabs are ours
+  auto write_out = [&](const OutPos& wc, const uint8_t* ccs, const uint8_t* css) {
+    const int nrb = wc.nvalid;
+    const bool whole = nrb == kWarpsPerGroup;  // all four slabs hold rows
     if (a.col_tma && whole) {
       if (gt == 0) {
         tma_store_3d(&a.tmap_colc, ccs, wc.colpos / 2, wc.n0 / 8, 0);
@@ -555,7 +652,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           const uint2 q1[4] = {make_uint2(c1a.x, c1a.y), make_uint2(c1a.z, c1a.w), make_uint2(c1b.x, c1b.y), make_uint2(c1b.z, c1b.w)};
 #pragma unroll
           for (int r = 0; r < kWarpsPerGroup; r++) {
-            if (r >= wc.skip && r < nrb) {
+            if (r < nrb) {
               *reinterpret_cast<uint2*>(dst0 + 8 * r) = q0[r];
               *reinterpret_cast<uint2*>(dst1 + 8 * r) = q1[r];
             }
@@ -578,13 +675,13 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           *reinterpret_cast<uint32_t*>(sd0) = sc0;
           *reinterpret_cast<uint32_t*>(sd1) = sc1;
         } else {
-          for (int r = wc.skip; r < nrb; r++) {
+          for (int r = 0; r < nrb; r++) {
             sd0[r] = (uint8_t)(sc0 >> (8 * r));
             sd1[r] = (uint8_t)(sc1 >> (8 * r));
           }
         }
       } else if (!whole) {  // the tiled layout, a partial tile: byte by byte
-        for (int r = wc.skip; r < nrb; r++) {
+        for (int r = 0; r < nrb; r++) {
           a.col_scales[swz_scale_off(col0, wc.colpos / 16 + r, a.col_swz_tc)] = (uint8_t)(sc0 >> (8 * r));
           if (col0 + 1 < N)
             a.col_scales[swz_scale_off(col0 + 1, wc.colpos / 16 + r, a.col_swz_tc)] = (uint8_t)(sc1 >> (8 * r));
@@ -614,7 +711,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       }
     }
   };
-  Coord prev{};           // the group's previous tile, staged in buffer buf ^ 1
+  OutPos prev{};          // the group's previous tile, staged in buffer buf ^ 1
   bool have_prev = false;
   int buf = 0;
 
@@ -648,14 +745,23 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     // then does the phase parity name its phase unambiguously.
     bool arrived = resident || wait_issued(issued, s, p + 1);
     arrived = arrived && (resident || mbar_wait_bounded(&full[s], (uint32_t)p & 1u, kWaitLimitNs));
-    const Coord c = coords[s];
-    if (!arrived || c.tile != tile) {
+    // this warp's slab and what the group needs of the tile, read before the stage is refilled
+    const Coord& cs = coords[s];
+    const OutPos c = {cs.n0, cs.colpos, cs.nvalid};
+    const int slab_rows = cs.nrows[rb];
+    const int64_t row_g0 = cs.row0[rb];
+    const int seg_w = cs.seg[rb], seg_g = cs.seg[0];
+    // a slab of another segment than the tile's first: this warp's own scale block, built
+    // before the tile's data take up registers (the warp is done with its previous block)
+    const bool foreign = GROUPED && arrived && cs.tile == tile && seg_w != seg_g && slab_rows > 0;
+    if (foreign) build_scale_block(tab_warp, seg_scale[seg_w], lane, a.fast);
+    const float* trow = foreign ? tab_warp : tab_row;  // the slab's scale block
+    if (!arrived || cs.tile != tile) {
       // the data never arrived (or the stage holds another tile): record it; the loads below
       // read stale shared memory and the group leaves at its next barrier without storing
       flags[g] = 1;
       if (lane == 0) atomicOr(a.status, 2u);  // NVFP4_DEVICE_TIMEOUT
     }
-    const int slab_rows = rb < c.skip ? 0 : min(16, c.nrows - 16 * rb);
     uint4 v[16];
     if (slab_rows > 0) {
       const uint32_t src = smem_u32(smem + kSmemStages + s * kStageBytes) +
@@ -677,7 +783,12 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     }
     named_bar_sync(1 + g, 32 * kWarpsPerGroup);
     if (flags[g]) break;
-    if (gt == 0 && i + kStages < n_slots) {
+    if (GROUPED) {  // each warp loads its own slab of the stage's next tile
+      if (lane == 0 && i + kStages < n_slots) {
+        fence_proxy_async();
+        issue_slab(position_tile(i + kStages), s, rb);
+      }
+    } else if (gt == 0 && i + kStages < n_slots) {
       fence_proxy_async();
       issue(position_tile(i + kStages), s);
     }
@@ -708,8 +819,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         mr = __reduce_max_sync(0xFFFFFFFFu, mr);
         mc = __reduce_max_sync(0xFFFFFFFFu, mc);
         if (lane == 0) {
-          atomicMax(&seg_amax[c.seg], mr);
-          atomicMax(&seg_amax[kMaxSegments + c.seg], mc);
+          atomicMax(&seg_amax[seg_w], mr);
+          atomicMax(&seg_amax[kMaxSegments + seg_w], mc);
         }
       }
       continue;
@@ -719,12 +830,12 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       write_out(prev, cc_base + (buf ^ 1) * kColCodeStage, cs_base + (buf ^ 1) * kColScaleStage);
     uint8_t* cc_stage = cc_base + buf * kColCodeStage;
     uint8_t* cs_stage = cs_base + buf * kColScaleStage;
-    if (c.seg != cur_seg) set_segment(c.seg);  // uniform across the group
+    if (seg_g != cur_seg) set_segment(seg_g);  // uniform across the group
+    const float* tcol = trow + kTableEntries;
 
     const bool lane_cols = (int64_t)c.n0 + lane * 8 < N;  // all 8 of the lane's columns exist
     // every row of the slab and every column of the tile exist (uniform across the warp)
     const bool full_slab = slab_rows == 16 && (int64_t)c.n0 + kTileN <= N;
-    const int64_t row_g0 = (int64_t)c.row0 + 16 * rb;
     if (slab_rows > 0) {
       // ---------------- 2D: one scale per 16x16 tile (the lane pair's 16 columns) ----------------
       float tile_r = 0.0f;
@@ -741,8 +852,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         const uint32_t m = vmax2(vmax2(cm[0], cm[1]), vmax2(cm[2], cm[3]));
         uint32_t tm = max(m & 0xFFFFu, m >> 16);
         tm = max(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 1));
-        tile_s = block_scales2(__uint_as_float(tm << 16), 0.0f, s_enc_r) & 0xFFu;
-        tile_r = tab_row[tile_s];
+        tile_s = block_scales2(__uint_as_float(tm << 16), 0.0f, trow[2 * kTableEntries]) & 0xFFu;
+        tile_r = trow[tile_s];
       }
 
       uint32_t tcode[kRowCol2D ? 16 : 1];  // 2D row+col: the slab's row codes, then transposed
@@ -766,12 +877,13 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
           for (int q = 0; q < 4; q++)
             recv[q] = __shfl_xor_sync(0xFFFFFFFFu, odd ? P[2 * q] : P[2 * q + 1], 1);
           float r_own[8];
+          const float enc_r = trow[2 * kTableEntries];
 #pragma unroll
           for (int q = 0; q < 4; q++) {
             const uint32_t bm = vmax2(odd ? P[2 * q + 1] : P[2 * q], recv[q]);
-            own_s[q] = block_scales2(mag_lo(bm), mag_hi(bm), s_enc_r);
-            r_own[2 * q] = tab_row[own_s[q] & 0xFFu];
-            r_own[2 * q + 1] = tab_row[own_s[q] >> 8];
+            own_s[q] = block_scales2(mag_lo(bm), mag_hi(bm), enc_r);
+            r_own[2 * q] = trow[own_s[q] & 0xFFu];
+            r_own[2 * q + 1] = trow[own_s[q] >> 8];
           }
 #pragma unroll
           for (int q = 0; q < 4; q++) {
@@ -882,15 +994,15 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
               m0 = fmaxf(m0, fabsf(y.x));
               m1 = fmaxf(m1, fabsf(y.y));
             }
-            s2 = block_scales2(m0, m1, s_enc_c);
-            rc2 = f2_pack(tab_col[s2 & 0xFFu], tab_col[s2 >> 8]);
+            s2 = block_scales2(m0, m1, trow[2 * kTableEntries + 1]);
+            rc2 = f2_pack(tcol[s2 & 0xFFu], tcol[s2 >> 8]);
           } else if (TWO_D) {
             s2 = tile_s | (tile_s << 8);
             rc2 = f2_pack(tile_r, tile_r);
           } else {
             const uint32_t m = tree_max16(w);
-            s2 = block_scales2(mag_lo(m), mag_hi(m), s_enc_c);
-            rc2 = f2_pack(tab_col[s2 & 0xFFu], tab_col[s2 >> 8]);
+            s2 = block_scales2(mag_lo(m), mag_hi(m), trow[2 * kTableEntries + 1]);
+            rc2 = f2_pack(tcol[s2 & 0xFFu], tcol[s2 >> 8]);
           }
           csc[k >> 1] |= s2 << (16 * (k & 1));
           uint4 W0 = make_uint4(0u, 0u, 0u, 0u), W1 = W0;
@@ -922,7 +1034,6 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       }
     }
 
-    // the staged codes leave after the next tile's barrier (or after the loop)
     prev = c;
     have_prev = true;
     buf ^= 1;
@@ -958,6 +1069,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
 // One variant: SWZ writes both scale outputs in the GEMMs' tiled layout (a.swz_scales).
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT, bool SWZ>
 cudaError_t launch_variant(const QuantArgs& args, int grid, cudaStream_t s) {
+  if (args.offsets != nullptr) {  // grouped (the host rejects the single launch and SWZ there)
+    return launch_pdl(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT, false, true>,
+                      dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
+  }
   if (args.fused) {
     // No CTA waits for another to start (fused_amax.cuh), so the CTAs need not be resident at
     // once: a plain launch with programmatic dependent launch, whose CTAs may start on the SMs
@@ -979,13 +1094,20 @@ cudaError_t launch(const QuantArgs& args, int grid, cudaStream_t s) {
 // The amax pass (AMAX_ONLY) of a plain or grouped tensor.
 template <bool RHT>
 cudaError_t launch_amax_pass(const QuantArgs& args, int grid, cudaStream_t s) {
+  if (args.offsets != nullptr)
+    return launch_pdl(quantize_tiles_kernel<true, false, RHT, false, false, false, false, true, false, false, true>,
+                      dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
   return launch_pdl(quantize_tiles_kernel<true, false, RHT, false, false, false, false, true>,
                     dim3(grid), dim3(kQuantThreads), kQuantSmemBytes, s, args);
 }
 template <bool RHT>
 cudaError_t prepare_amax_pass() {
-  return cudaFuncSetAttribute(quantize_tiles_kernel<true, false, RHT, false, false, false, false, true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(quantize_tiles_kernel<true, false, RHT, false, false, false, false, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+  cudaError_t e2 = cudaFuncSetAttribute(
+      quantize_tiles_kernel<true, false, RHT, false, false, false, false, true, false, false, true>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+  return e != cudaSuccess ? e : e2;
 }
 
 template <bool ROW, bool COL, bool RHT, bool TWO_D, bool SR_ROW, bool SR_COL, bool FAST_RHT = false>
@@ -1000,6 +1122,7 @@ cudaError_t prepare() {
   set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT, false>);
   set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT, true>);
   set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, true, false, FAST_RHT, true>);
+  set(quantize_tiles_kernel<ROW, COL, RHT, TWO_D, SR_ROW, SR_COL, false, false, FAST_RHT, false, true>);
   return e;
 }
 
