@@ -281,6 +281,10 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
       // is at most j (never an empty segment: the next one starts at the same slab).
       int e = seg_hint[warp];
       int4 r = seg_rec[e];
+      if (AMAX_ONLY) {  // a few steps forward first (each warp walks its tiles forward)
+#pragma unroll 1
+        for (int step = 0; step < 4 && j >= r.w; step++) r = seg_rec[++e];
+      }
       if (j < r.x || j >= r.w) {
         int lo = 0, hi = E;
         while (hi - lo > 1) {
@@ -289,8 +293,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
         }
         e = lo;
         r = seg_rec[e];
-        seg_hint[warp] = e;
       }
+      seg_hint[warp] = e;
       const int row0 = r.y + 16 * (j - r.x);
       cp->row0[k] = row0;
       cp->nrows[k] = min(16, r.z - row0);
@@ -753,7 +757,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1)
     const int seg_w = cs.seg[rb], seg_g = cs.seg[0];
     // a slab of another segment than the tile's first: this warp's own scale block, built
     // before the tile's data take up registers (the warp is done with its previous block)
-    const bool foreign = GROUPED && arrived && cs.tile == tile && seg_w != seg_g && slab_rows > 0;
+    const bool foreign =
+        GROUPED && !AMAX_ONLY && arrived && cs.tile == tile && seg_w != seg_g && slab_rows > 0;
     if (foreign) build_scale_block(tab_warp, seg_scale[seg_w], lane, a.fast);
     const float* trow = foreign ? tab_warp : tab_row;  // the slab's scale block
     if (!arrived || cs.tile != tile) {

@@ -263,8 +263,8 @@ GROUPED_CASES = [
     ("odd_counts", 203, 272, [5, 5, 37, 37, 70, 150, 203]),
     ("zero_experts_and_tail", 300, 64, [0, 0, 17, 17, 129, 250]),
     ("many_small", 260, 32, list(np.cumsum([1, 2, 3, 15, 16, 17, 31, 33, 0, 64, 65, 13]))),
-    # column starts 16, 48, 96 (lead slabs of 16, 48, 32 rows before the next expert's tiles)
-    # followed by experts long enough for whole, aligned 64-row tiles
+    # column starts 16, 48, 96: segments that begin inside a 64-row tile of the columnwise
+    # space (tiles shared by two or three segments), then experts long enough for whole tiles
     ("lead_slabs", 700, 512, list(np.cumsum([16, 200, 32, 150, 48, 200, 1, 53]))),
 ]
 
@@ -305,6 +305,31 @@ def test_grouped_matches_oracle(case, mode):
     x = workloads.normal(T, H, 1.0, seed=T + H)
     out, ref = run_grouped_both(x, offs, **cfg)
     assert_same(out, ref, "%s/%s" % (name, mode))
+
+
+@pytest.mark.parametrize("mode", ["rn", "rht_sr", "row_only_sr", "col_only_rht", "2d_rowcol"])
+def test_grouped_many_tiles_per_cta_matches_oracle(mode):
+    """Enough tiles that every CTA refills each stage of its ring several times (about ten
+    tiles per CTA), with 40 experts of seeded random sizes (empty and tiny ones included), so
+    that tiles shared by segments, the per-warp loads of the refills and the amax pass's
+    refills all run; the per-expert maxima are computed inside the call."""
+    rng = np.random.default_rng(0x5EED_0040)
+    counts = rng.integers(0, 300, size=40)
+    counts[[3, 17, 18]] = 0
+    counts[[5, 9]] = [1, 15]
+    offs = list(np.cumsum(counts))
+    T, H = int(offs[-1]), 4096
+    cfg = {
+        "rn": dict(rowwise=True, columnwise=True),
+        "rht_sr": dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x3A5C,
+                       round_col="sr", seed=11, offset=3),
+        "row_only_sr": dict(rowwise=True, columnwise=False, round_row="sr", seed=12),
+        "col_only_rht": dict(rowwise=False, columnwise=True, rht_col=True, sign_mask=0x8001),
+        "2d_rowcol": dict(rowwise=True, columnwise=True, block2d=True),
+    }[mode]
+    x = workloads.normal_with_outliers(T, H, seed=T + 7, fraction=0.002, gain=40.0)
+    out, ref = run_grouped_both(x, offs, **cfg)
+    assert_same(out, ref, "many tiles/%s" % mode)
 
 
 @pytest.mark.parametrize("case", GROUPED_CASES[1:3], ids=lambda c: c[0])
