@@ -139,3 +139,29 @@ def test_noalloc_held_back_ctas_are_taken_over():
     api.nvfp4_debug_fused_late_ctas(30)
     _same_as_regular(x, kw, "with 30 held-back CTAs")
     assert _noalloc_status() == (0, 0)
+
+
+def test_noalloc_matches_the_oracle():
+    """The entry point's outputs against the oracle itself (not only against the regular
+    entry point), with RHT + stochastic rounding columnwise and a ragged shape."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    dev = torch.device("cuda")
+    M, N = 1040, 784
+    kw = dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x6C39, round_col="sr",
+              seed=17, offset=4)
+    x = workloads.normal_with_outliers(M, N, seed=61, fraction=0.003, gain=40.0)
+    out = api.alloc_outputs(M, N, dev, True, True)
+    for v in out.values():
+        v.fill_(0x5A if v.dtype == torch.uint8 else float("nan"))
+    assert _noalloc(x.to(dev), out, api.make_config(**kw)) == 0
+    torch.cuda.synchronize()
+    ref = oracle.quantize(x, oracle.Config(rowwise=True, columnwise=True, rht_col=True,
+                                           sign_mask=0x6C39, round_col_sr=True, seed=17,
+                                           offset=4))
+    for k, r in ref.items():
+        a, b = out[k].cpu().numpy(), np.asarray(r)
+        if a.dtype == np.float32:
+            a, b = a.view(np.uint32), b.astype(np.float32).view(np.uint32)
+        assert a.shape == b.shape and np.array_equal(a, b), "noalloc vs oracle: %s differs" % k
