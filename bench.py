@@ -512,21 +512,18 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API: pinned host input -> device -> quantize -> pinned host.
     # Plain tensors go through the host pipeline (the copy in of one step overlaps the copy out
-    # of the previous one); grouped ones through nvfp4_quantize_grouped on the current stream.
+    # of the previous one), grouped ones through its grouped form (the expert offsets copied in
+    # with x).
     x_host = inp["x"].pin_memory()
     h2d = x_host.numel() * 2
     d2h = sum(v.numel() * v.element_size() for v in out.values())
     if w.grouped:
-        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
-
-        def e2e_step():
-            xd = x_host.to(dev, non_blocking=True)
-            o = api.nvfp4_quantize_grouped(xd, offsets, col_capacity=cap,
-                                           **kw)
-            for k, v in o.items():
-                host_out[k].copy_(v, non_blocking=True)
-
-        e2e_join = lambda: None
+        offsets_host = torch.from_numpy(np.ascontiguousarray(inp["offsets"], dtype=np.int32))
+        h2d += offsets_host.numel() * 4
+        pipe = api.GroupedHostPipeline(w.rows, w.cols, w.experts, cap, depth=2, **kw)
+        host_out = pipe.alloc_host_outputs()
+        e2e_step = lambda: pipe.submit(x_host, offsets_host, host_out)  # noqa: E731
+        e2e_join = pipe.join
     else:
         pipe = api.HostPipeline(w.rows, w.cols, depth=2, fused_amax=args.pipeline == "fused",
                                 **kw)
@@ -548,8 +545,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(world, e0.elapsed_time(e1) / 1e3)
     e2e_value = ideal * e2e_steps * world / e2e_s / 1e9
-    if not w.grouped:
-        pipe.close()
+    pipe.close()
 
     if rank != 0:
         return
@@ -575,8 +571,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": ("nvfp4_quantize_grouped, copies on the current stream" if w.grouped
-                         else "nvfp4_host_pipeline depth 2 (copies of consecutive steps overlap)")},
+                "path": ("nvfp4_host_pipeline_*_grouped" if w.grouped else "nvfp4_host_pipeline")
+                        + " depth 2 (copies of consecutive steps overlap)"},
         "clocks": clocks.summary(),
     }
     line["step_us"] = {"min": min(step_ms) * 1e3, "median": statistics.median(step_ms) * 1e3,

@@ -422,6 +422,26 @@ nvfp4_status nvfp4_host_pipeline_submit(nvfp4_host_pipeline* p, const void* x_ho
                                         float* row_gscale, uint8_t* col_codes,
                                         uint8_t* col_scales, float* col_gscale, void* stream);
 
+/* The same for grouped tensors: BF16 [T][H] with E experts (1 <= E <= 256), quantized by
+ * nvfp4_quantize_grouped with *cfg (fused_amax 0: NVFP4_ERR_UNSUPPORTED otherwise) and
+ * col_capacity columns of columnwise outputs (a multiple of 16 when cfg->columnwise); each
+ * slot also stages the submission's E offsets. Shape rules as nvfp4_quantize_grouped. */
+nvfp4_status nvfp4_host_pipeline_create_grouped(int64_t T, int64_t H, int32_t E,
+                                                int64_t col_capacity, const nvfp4_config* cfg,
+                                                int32_t depth, nvfp4_host_pipeline** out);
+
+/* Enqueue one grouped tensor: x_host (host) BF16 [T][H], offsets_host (host) int32 [E] (the
+ * expert ends, rules as nvfp4_quantize_grouped's; copied in with x), outputs (host) as
+ * nvfp4_quantize_grouped's. A pipeline created by nvfp4_host_pipeline_create takes only
+ * nvfp4_host_pipeline_submit, one created by nvfp4_host_pipeline_create_grouped only this
+ * call (NVFP4_ERR_INVALID_ARG otherwise). */
+nvfp4_status nvfp4_host_pipeline_submit_grouped(nvfp4_host_pipeline* p, const void* x_host,
+                                                const int32_t* offsets_host,
+                                                uint8_t* row_codes, uint8_t* row_scales,
+                                                float* row_gscale, uint8_t* col_codes,
+                                                uint8_t* col_scales, float* col_gscale,
+                                                void* stream);
+
 /* Make `stream` wait (on the device) until every submitted tensor's outputs are in host
  * memory. Synchronize `stream` (or an event recorded after this call) before reading them. */
 nvfp4_status nvfp4_host_pipeline_join(nvfp4_host_pipeline* p, void* stream);

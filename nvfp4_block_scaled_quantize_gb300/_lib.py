@@ -22,6 +22,7 @@ DEVICE_TIMEOUT = 0x2
 EXPORTED = ["nvfp4_status_string", "nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_grouped",
             "nvfp4_dequantize", "nvfp4_get_status", "nvfp4_quantize_noalloc",
             "nvfp4_host_pipeline_create", "nvfp4_host_pipeline_submit",
+            "nvfp4_host_pipeline_create_grouped", "nvfp4_host_pipeline_submit_grouped",
             "nvfp4_host_pipeline_join", "nvfp4_host_pipeline_destroy", "nvfp4_swizzle_scales",
             "nvfp4_mx_quantize", "nvfp4_mx_dequantize", "nvfp4_dequantize_ex",
             "nvfp4_rmsnorm_amax", "nvfp4_rmsnorm_quantize", "nvfp4_set_workspace",
@@ -93,6 +94,11 @@ def load(build_if_missing: bool = False):
     L.nvfp4_host_pipeline_create.argtypes = [i64, i64, cfgp, i32, ctypes.POINTER(vp)]
     L.nvfp4_host_pipeline_submit.restype = ctypes.c_int
     L.nvfp4_host_pipeline_submit.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.nvfp4_host_pipeline_create_grouped.restype = ctypes.c_int
+    L.nvfp4_host_pipeline_create_grouped.argtypes = [i64, i64, i32, i64, cfgp, i32,
+                                                     ctypes.POINTER(vp)]
+    L.nvfp4_host_pipeline_submit_grouped.restype = ctypes.c_int
+    L.nvfp4_host_pipeline_submit_grouped.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.nvfp4_host_pipeline_join.restype = ctypes.c_int
     L.nvfp4_host_pipeline_join.argtypes = [vp, vp]
     L.nvfp4_host_pipeline_destroy.restype = ctypes.c_int

@@ -438,3 +438,54 @@ class HostPipeline:
             self.close()
         except Exception:
             pass
+
+
+class GroupedHostPipeline(HostPipeline):
+    """nvfp4_host_pipeline_create_grouped / _submit_grouped: grouped BF16 [T, H] host tensors
+    with E experts (offsets given per submission as a host int32 [E] array of expert ends),
+    quantized by nvfp4_quantize_grouped with col_capacity columns of columnwise outputs."""
+
+    def __init__(self, T, H, E, col_capacity, depth=2, **kw):
+        L = _lib.load()
+        self.M, self.N, self.E, self.cap = T, H, E, col_capacity
+        kw.pop("fused_amax", None)
+        self.cfg = make_config(fused_amax=False, **kw)
+        self.rowwise = bool(self.cfg.rowwise)
+        self.columnwise = bool(self.cfg.columnwise)
+        self.device = torch.device("cuda", torch.cuda.current_device())
+        handle = ctypes.c_void_p()
+        _raise_if(L.nvfp4_host_pipeline_create_grouped(T, H, E, col_capacity,
+                                                       ctypes.byref(self.cfg), depth,
+                                                       ctypes.byref(handle)),
+                  "nvfp4_host_pipeline_create_grouped")
+        self._h = handle
+
+    def alloc_host_outputs(self):
+        out = {}
+        T, H, E, cap = self.M, self.N, self.E, self.cap
+        if self.rowwise:
+            out["row_codes"] = torch.empty((T, H // 2), dtype=torch.uint8, pin_memory=True)
+            out["row_scales"] = torch.empty((T, H // 16), dtype=torch.uint8, pin_memory=True)
+            out["row_gscale"] = torch.empty((E, 2), dtype=torch.float32, pin_memory=True)
+        if self.columnwise:
+            out["col_codes"] = torch.empty((H, cap // 2), dtype=torch.uint8, pin_memory=True)
+            out["col_scales"] = torch.empty((H, cap // 16), dtype=torch.uint8, pin_memory=True)
+            out["col_gscale"] = torch.empty((E, 2), dtype=torch.float32, pin_memory=True)
+        return out
+
+    def submit(self, x_host, offsets_host, out_host):
+        """Enqueue x_host (pinned BF16 [T, H]) with offsets_host (host int32 [E]); outputs land
+        in out_host (alloc_host_outputs)."""
+        if x_host.device.type != "cpu" or x_host.dtype != torch.bfloat16 or \
+                tuple(x_host.shape) != (self.M, self.N) or not x_host.is_contiguous():
+            raise ValueError("x_host must be a contiguous CPU bfloat16 [%d, %d] tensor"
+                             % (self.M, self.N))
+        if offsets_host.device.type != "cpu" or offsets_host.dtype != torch.int32 or \
+                tuple(offsets_host.shape) != (self.E,) or not offsets_host.is_contiguous():
+            raise ValueError("offsets_host must be a contiguous CPU int32 [%d] tensor" % self.E)
+        L = _lib.load()
+        p = lambda k: ctypes.c_void_p(out_host[k].data_ptr()) if k in out_host else None
+        _raise_if(L.nvfp4_host_pipeline_submit_grouped(
+            self._h, ctypes.c_void_p(x_host.data_ptr()), ctypes.c_void_p(offsets_host.data_ptr()),
+            p("row_codes"), p("row_scales"), p("row_gscale"), p("col_codes"), p("col_scales"),
+            p("col_gscale"), _stream(self.device)), "nvfp4_host_pipeline_submit_grouped")

@@ -117,6 +117,17 @@ def test_host_pipeline_argument_checks_return_before_any_cuda_call(L):
     assert create(24, 64, _cfg(columnwise=1), 2) == 2           # M % 16 with columnwise
     assert L.nvfp4_host_pipeline_create(64, 64, None, 2, ctypes.byref(h)) == 1
     assert L.nvfp4_host_pipeline_submit(None, ctypes.c_void_p(FAKE), *([None] * 7)) == 1
+    grouped = lambda T, H, E, cap, c, depth: L.nvfp4_host_pipeline_create_grouped(
+        T, H, E, cap, ctypes.byref(c), depth, ctypes.byref(h))
+    assert grouped(64, 64, 0, 64, _cfg(), 2) == 1                 # no experts
+    assert grouped(64, 64, 257, 64, _cfg(), 2) == 1               # more than 256
+    assert grouped(64, 64, 2, 64, _cfg(fused_amax=1), 2) == 4     # no single launch here
+    assert grouped(64, 64, 2, 64, _cfg(swizzle_scales=1), 2) == 4
+    assert grouped(64, 24, 2, 64, _cfg(), 2) == 2                 # H % 16
+    assert grouped(64, 64, 2, 72, _cfg(columnwise=1), 2) == 2     # capacity % 16
+    assert grouped(64, 64, 2, 64, _cfg(), 9) == 1                 # depth
+    assert L.nvfp4_host_pipeline_submit_grouped(None, ctypes.c_void_p(FAKE),
+                                                ctypes.c_void_p(FAKE), *([None] * 7)) == 1
     assert L.nvfp4_host_pipeline_join(None, None) == 1
     assert L.nvfp4_host_pipeline_destroy(None) == 0
 

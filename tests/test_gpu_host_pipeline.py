@@ -82,3 +82,49 @@ def test_pipeline_rejects_wrong_host_tensor():
             pipe.submit(torch.zeros((64, 32), dtype=torch.bfloat16), pipe.alloc_host_outputs())
     finally:
         pipe.close()
+
+
+GROUPED_CONFIGS = [
+    ("rowcol_rtne", dict(rowwise=True, columnwise=True)),
+    ("row_rtne_col_rht_sr", dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x5AC3,
+                                 round_col="sr", seed=23)),
+    ("2d_weights", dict(rowwise=True, columnwise=True, block2d=True)),
+]
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+@pytest.mark.parametrize("name,kw", GROUPED_CONFIGS, ids=[c[0] for c in GROUPED_CONFIGS])
+def test_grouped_pipeline_outputs_match_device_quantize(depth, name, kw):
+    """Grouped submissions with different inputs and expert offsets per submission (empty and
+    ragged experts): each host output equals nvfp4_quantize_grouped's on the device copy."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    T, H, E = 400, 784, 5
+    cap = T + 16 * E
+    offs = [np.cumsum(c).astype(np.int32) for c in
+            ([0, 100, 33, 200, 67], [17, 17, 0, 300, 66], [400, 0, 0, 0, 0])]
+    xs = [workloads.normal_with_outliers(T, H, seed=s, fraction=0.003, gain=30.0).pin_memory()
+          for s in (31, 32, 33)]
+    pipe = api.GroupedHostPipeline(T, H, E, cap, depth=depth, **kw)
+    try:
+        outs = []
+        for i in range(5):   # more submissions than slots: every slot is reused
+            o = pipe.alloc_host_outputs()
+            for v in o.values():
+                v.fill_(0x77 if v.dtype == torch.uint8 else float("nan"))
+            pipe.submit(xs[i % 3], torch.from_numpy(offs[i % 3]), o)
+            outs.append(o)
+        pipe.join()
+        torch.cuda.synchronize()
+        for i, o in enumerate(outs):
+            ref = api.alloc_outputs(T, H, torch.device("cuda"), True, True, col_ld=cap, groups=E)
+            for v in ref.values():
+                v.fill_(0x77 if v.dtype == torch.uint8 else float("nan"))
+            api.nvfp4_quantize_grouped(xs[i % 3].cuda(), torch.from_numpy(offs[i % 3]).cuda(),
+                                       col_capacity=cap, out=ref, **kw)
+            torch.cuda.synchronize()
+            assert sorted(o) == sorted(ref)
+            for k in ref:
+                _same(o[k], ref[k], "%s depth %d submission %d %s" % (name, depth, i, k))
+    finally:
+        pipe.close()
