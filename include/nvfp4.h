@@ -195,7 +195,9 @@ nvfp4_status nvfp4_amax_grouped(const void* x, int64_t T, int64_t H, const int32
  *                this call (amax_col is the RHT amax when cfg->rht_col). With block2d both
  *                orientations use amax_row.
  *   col_capacity columns of the columnwise outputs, a multiple of 16, >= sum_e pad16(n_e)
- *                (pad16 rounds a token count up to a multiple of 16). Expert e's columnwise
+ *                (pad16 rounds a token count up to a multiple of 16). A multiple of 32 keeps
+ *                every columnwise row 16-byte aligned, so that the kernel's whole tiles leave
+ *                by TMA store; an odd multiple of 16 takes per-thread stores (slower). Expert e's columnwise
  *                block starts at column sum_{j<e} pad16(n_j); its last partial 16-token block
  *                is zero-padded before the transform and stored in full.
  *   Per expert: amax over its rows and global scale for the rowwise side; RHT amax (or amax)

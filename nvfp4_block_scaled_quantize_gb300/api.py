@@ -132,7 +132,9 @@ def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwi
                            offset=0, out=None, fast_math=False, block2d=False, amax_row=None,
                            amax_col=None):
     """Grouped quantization of a packed BF16 [T, H] tensor; `offsets` is an int32 [E] device
-    tensor of cumulative expert ends. col_capacity defaults to T + 16 * E (always enough).
+    tensor of cumulative expert ends. col_capacity defaults to T + 16 * E rounded up to a
+    multiple of 32 (always enough; a multiple of 32 keeps the columnwise codes' rows 16-byte
+    aligned, so that whole tiles leave by TMA store).
     block2d: 16x16 tiles per expert (stacked expert weights), no RHT or SR. amax_row /
     amax_col (float32 [E] device tensors, e.g. from nvfp4_amax_grouped) skip the amax pass."""
     _check_x(x)
@@ -142,7 +144,7 @@ def nvfp4_quantize_grouped(x, offsets, col_capacity=None, rowwise=True, columnwi
     T, H = x.shape
     E = offsets.shape[0]
     if col_capacity is None:
-        col_capacity = (T + 15) // 16 * 16 + 16 * E
+        col_capacity = ((T + 15) // 16 * 16 + 16 * E + 31) // 32 * 32
     cfg = make_config(rowwise, columnwise, block2d, round_row, round_col, rht_col, sign_mask, seed,
                       offset, fast_math=fast_math)
     if out is None:
