@@ -650,8 +650,8 @@ NVFP4_EXPORT nvfp4_status nvfp4_set_workspace(void* workspace, size_t bytes) {
   DeviceState& st = g_devices[dev];
   nvfp4_status r = init_device(st, dev);
   if (r != NVFP4_OK) return r;
-  // the single-launch amax keeps its counts and epoch on the workspace: a workspace taken into
-  // use starts from zero
+  // the single-launch amax keeps its counts, maxima and claim bits on the workspace: a
+  // workspace taken into use starts from zero
   uint32_t* ws = workspace != nullptr ? static_cast<uint32_t*>(workspace) : st.own;
   if (ws != nullptr && (cudaMemset(ws, 0, kWorkspaceBytes) != cudaSuccess ||
                         cudaDeviceSynchronize() != cudaSuccess))

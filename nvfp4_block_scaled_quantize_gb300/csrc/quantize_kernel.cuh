@@ -192,8 +192,7 @@ __device__ __forceinline__ bool wait_issued(volatile int32_t* issued, int s, int
 // A template parameter, so that each path is compiled on its own.
 // AMAX_ONLY: the amax pass alone, through the same stage ring: per segment max |x| and, with
 // RHT, max |bf16(RHT)| over its zero-padded 16-row column blocks, atomically maxed into
-// a.amax_row / a.amax_col (zeroed by the caller); no codes. Instantiated with ROW and !COL (no
-// lead rows: tiles start on the segments' 16-row blocks).
+// a.amax_row / a.amax_col (zeroed by the caller); no codes. Instantiated with ROW and !COL.
 // FAST_RHT: fast math with the RHT (columnwise codes from the FP32 transform, no BF16
 // round-through). SWZ: both scale outputs in the GEMMs' tiled layout (a.swz_scales).
 // GROUPED: a tensor split into segments (a.offsets); never FUSED or SWZ.
