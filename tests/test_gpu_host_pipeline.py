@@ -128,3 +128,35 @@ def test_grouped_pipeline_outputs_match_device_quantize(depth, name, kw):
                 _same(o[k], ref[k], "%s depth %d submission %d %s" % (name, depth, i, k))
     finally:
         pipe.close()
+
+
+def test_grouped_pipeline_refuses_bad_offsets_on_the_host():
+    """Offsets that decrease, pass T, or need more columns than the capacity are refused before
+    anything is enqueued; a later valid submission still runs."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import ctypes
+    from nvfp4_block_scaled_quantize_gb300 import _lib
+    T, H, E = 128, 256, 3
+    pipe = api.GroupedHostPipeline(T, H, E, 144, depth=1, rowwise=True, columnwise=True)
+    try:
+        x = workloads.normal(T, H, 1.0, seed=5).pin_memory()
+        o = pipe.alloc_host_outputs()
+        L = _lib.load()
+        p = lambda k: ctypes.c_void_p(o[k].data_ptr())  # noqa: E731
+        for bad in ([40, 30, 128], [40, 80, 129], [1, 2, 128]):   # the last needs 160 columns
+            offs = torch.tensor(bad, dtype=torch.int32)
+            st = L.nvfp4_host_pipeline_submit_grouped(
+                pipe._h, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(offs.data_ptr()),
+                p("row_codes"), p("row_scales"), p("row_gscale"), p("col_codes"),
+                p("col_scales"), p("col_gscale"), None)
+            assert _lib.STATUS_NAMES[st] == "NVFP4_ERR_INVALID_ARG", bad
+        pipe.submit(x, torch.tensor([40, 80, 128], dtype=torch.int32), o)
+        pipe.join()
+        torch.cuda.synchronize()
+        ref = api.nvfp4_quantize_grouped(x.cuda(), torch.tensor([40, 80, 128], dtype=torch.int32).cuda(),
+                                         col_capacity=144)
+        for k in ref:
+            _same(o[k], ref[k], k)
+    finally:
+        pipe.close()
