@@ -332,6 +332,27 @@ def test_grouped_many_tiles_per_cta_matches_oracle(mode):
     assert_same(out, ref, "many tiles/%s" % mode)
 
 
+@pytest.mark.parametrize("mode", ["rht_sr", "row_only_sr", "2d_rowcol"])
+def test_grouped_most_experts_matches_oracle(mode):
+    """The largest expert count (256), most experts tiny or empty: tiles shared by up to four
+    experts, deep segment searches, the per-warp tables of slabs in other experts."""
+    rng = np.random.default_rng(0x5EED_0100)
+    counts = rng.integers(0, 40, size=256)
+    counts[rng.random(256) < 0.25] = 0
+    counts[-1] = 0                      # trailing empty experts
+    offs = list(np.cumsum(counts))
+    T, H = int(offs[-1]) + 9, 512       # a tail past the last expert
+    cfg = {
+        "rht_sr": dict(rowwise=True, columnwise=True, rht_col=True, sign_mask=0x9E37,
+                       round_col="sr", seed=31, offset=5),
+        "row_only_sr": dict(rowwise=True, columnwise=False, round_row="sr", seed=32),
+        "2d_rowcol": dict(rowwise=True, columnwise=True, block2d=True),
+    }[mode]
+    x = workloads.normal_with_outliers(T, H, seed=T + 11, fraction=0.01, gain=30.0)
+    out, ref = run_grouped_both(x, offs, **cfg)
+    assert_same(out, ref, "256 experts/%s" % mode)
+
+
 @pytest.mark.parametrize("case", GROUPED_CASES[1:3], ids=lambda c: c[0])
 @pytest.mark.parametrize("mode", ["rn", "rht_sr", "col_only_rht", "2d_rowcol", "2d_col"])
 def test_grouped_with_supplied_amax_matches_oracle(case, mode):
